@@ -1,0 +1,79 @@
+// Internal launch interface between the C ABI (kda_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+struct DecodeParams {
+    const void *q, *k, *v;
+    const float *g;
+    const void *b;
+    const int32_t *slot_ids;
+    float *pool;
+    int64_t num_slots;
+    void *out;
+    int32_t *err_flag;
+    int32_t batch, H, dv;
+    float eps, scale;
+};
+
+struct VerifyParams {
+    const void *q, *k, *v;
+    const float *g;
+    const void *b;
+    const int32_t *slot_ids;
+    const float *pool;
+    int64_t num_slots;
+    void *out;
+    float *rec_k_hat;
+    void *rec_v;
+    float *rec_g;
+    float *rec_beta;
+    int32_t *err_flag;
+    int32_t batch, D, H, dv;
+    float eps, scale;
+};
+
+struct ReplayParams {
+    const float *rec_k_hat;
+    const void *rec_v;
+    const float *rec_g;
+    const float *rec_beta;
+    const int32_t *num_accepted;
+    const int32_t *slot_ids;
+    float *pool;
+    int64_t num_slots;
+    int32_t *err_flag;
+    int32_t batch, D, H, dv;
+};
+
+struct PrefillParams {
+    const int32_t *cu_seqlens;
+    int64_t total_tokens;
+    const void *q, *k, *v;
+    const float *g;
+    const void *b;
+    const int32_t *slot_ids;
+    float *pool;
+    int64_t num_slots;
+    int32_t init_from_pool;
+    void *out;
+    void *workspace;
+    size_t workspace_bytes;
+    int32_t *err_flag;
+    int32_t num_seqs, H, dk, dv;
+    float eps, scale;
+};
+
+// Each launcher returns cudaSuccess or the launch error.
+cudaError_t launch_decode(const DecodeParams &p, int dk, int dtype, cudaStream_t s);
+cudaError_t launch_verify(const VerifyParams &p, int dk, int dtype, cudaStream_t s);
+cudaError_t launch_replay(const ReplayParams &p, int dk, int dtype, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillParams &p, int dtype, cudaStream_t s);
+size_t prefill_workspace_bytes(int H, int dk, int dv, int32_t num_seqs, int64_t total_tokens);
+
+}  // namespace kda

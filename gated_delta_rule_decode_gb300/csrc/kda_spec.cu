@@ -1,0 +1,178 @@
+// ReplaySSM speculative verify (record) and commit (replay) kernels.
+//
+// "2.8x faster Kimi K3 inference on CANN", section 04 "ReplaySSM": while the
+// draft tokens are verified only the per-token update records needed for a
+// replay are kept; once the accepted length is known, the commit starts from
+// the committed state and applies the accepted records in order, so no full
+// state is ever stored per candidate token.
+//
+// verify_kernel: a CTA owns one (sequence, head, block of 16*R state rows),
+// reads those rows once into registers, runs the D draft tokens over them in
+// order (emitting every token's output), writes the records, and never writes
+// the pool.  replay_kernel: a CTA owns the same tile, skips it without any
+// memory access when a = 0, else reads the rows once, applies a records and
+// writes them back.  Both use the row math of the decode kernel, so replaying
+// a records reproduces a decode calls bit for bit.
+#include "kda.h"
+#include "kda_internal.h"
+#include "kda_rowmath.cuh"
+
+namespace kda {
+
+constexpr int kSpecWarps = 4;
+constexpr int kRowStride = kSpecWarps * kGroupsPerWarp;  // 16
+
+template <int DK, typename T, int R>
+__global__ void __launch_bounds__(kSpecWarps * 32) verify_kernel(const VerifyParams p) {
+    constexpr int ROWS = kRowStride * R;
+    const int nblk = p.dv / ROWS;
+    const int64_t item = blockIdx.x;
+    const int blk = (int)(item % nblk);
+    const int64_t sh = item / nblk;
+    const int h = (int)(sh % p.H);
+    const int n = (int)(sh / p.H);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = lane >> 3, l = lane & 7;
+    const int row0 = blk * ROWS + warp * kGroupsPerWarp + grp;
+
+    const int slot = __ldg(p.slot_ids + n);
+    const bool valid = slot >= 0 && (int64_t)slot < p.num_slots;
+    if (slot >= 0 && !valid && blk == 0 && threadIdx.x == 0 && p.err_flag)
+        atomicOr(p.err_flag, KDA_DEVERR_SLOT);
+
+    float s[R][DK / kLanesPerRow];
+    if (valid) {
+        const float *S = p.pool + ((int64_t)slot * p.H + h) * (int64_t)p.dv * DK;
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) load_row<DK>(S + (int64_t)(row0 + rr * kRowStride) * DK, l, s[rr]);
+    }
+    const bool writes_key_record = (blk == 0 && warp == 0 && grp == 0);
+
+    for (int j = 0; j < p.D; ++j) {
+        const int64_t tk = ((int64_t)n * p.D + j) * p.H + h;
+        const T *vrow = static_cast<const T *>(p.v) + tk * p.dv;
+        T *orow = static_cast<T *>(p.out) + tk * p.dv;
+        T *vrec = static_cast<T *>(p.rec_v) + tk * p.dv;
+        TokenCoeffs<DK> tc;
+        const float bb = Elem<T>::load1(static_cast<const T *>(p.b) + tk);
+        make_coeffs<DK, T>(tc, static_cast<const T *>(p.q) + tk * DK,
+                           static_cast<const T *>(p.k) + tk * DK, p.g + tk * DK, bb, p.eps, l);
+        if (writes_key_record) {
+            float *kr = p.rec_k_hat + tk * DK;
+            float *gr = p.rec_g + tk * DK;
+            const float *gi = p.g + tk * DK;
+#pragma unroll
+            for (int jj = 0; jj < DK / 32; ++jj) {
+                const int c = 4 * l + 32 * jj;
+                *reinterpret_cast<float4 *>(kr + c) =
+                    make_float4(tc.kh[4 * jj], tc.kh[4 * jj + 1], tc.kh[4 * jj + 2], tc.kh[4 * jj + 3]);
+                *reinterpret_cast<float4 *>(gr + c) = __ldg(reinterpret_cast<const float4 *>(gi + c));
+            }
+            if (l == 0) p.rec_beta[tk] = tc.beta;
+        }
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            const int row = row0 + rr * kRowStride;
+            const T v_raw = vrow[row];
+            float o = 0.f;
+            if (valid) {
+                float u;
+                const float c = row_update<DK, true>(s[rr], tc, Elem<T>::to_f(v_raw), &u);
+                o = row_output(c, u, tc.kq, p.scale);
+            }
+            if (l == 0) {
+                vrec[row] = v_raw;
+                Elem<T>::store1(orow + row, o);
+            }
+        }
+    }
+}
+
+template <int DK, typename T, int R>
+__global__ void __launch_bounds__(kSpecWarps * 32) replay_kernel(const ReplayParams p) {
+    constexpr int ROWS = kRowStride * R;
+    const int nblk = p.dv / ROWS;
+    const int64_t item = blockIdx.x;
+    const int blk = (int)(item % nblk);
+    const int64_t sh = item / nblk;
+    const int h = (int)(sh % p.H);
+    const int n = (int)(sh / p.H);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = lane >> 3, l = lane & 7;
+    const int row0 = blk * ROWS + warp * kGroupsPerWarp + grp;
+
+    const int a = __ldg(p.num_accepted + n);
+    const int slot = __ldg(p.slot_ids + n);
+    const bool report = (blk == 0 && h == 0 && threadIdx.x == 0 && p.err_flag);
+    if (a < 0 || a > p.D) {
+        if (report) atomicOr(p.err_flag, KDA_DEVERR_ACCEPTED);
+        return;
+    }
+    if (slot < 0) return;
+    if ((int64_t)slot >= p.num_slots) {
+        if (report) atomicOr(p.err_flag, KDA_DEVERR_SLOT);
+        return;
+    }
+    if (a == 0) return;  // nothing accepted: no memory access at all
+
+    float *S = p.pool + ((int64_t)slot * p.H + h) * (int64_t)p.dv * DK;
+    float s[R][DK / kLanesPerRow];
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) load_row<DK>(S + (int64_t)(row0 + rr * kRowStride) * DK, l, s[rr]);
+
+    for (int j = 0; j < a; ++j) {
+        const int64_t tk = ((int64_t)n * p.D + j) * p.H + h;
+        TokenCoeffs<DK> tc;
+        coeffs_from_record<DK>(tc, p.rec_k_hat + tk * DK, p.rec_g + tk * DK, __ldg(p.rec_beta + tk), l);
+        const T *vrec = static_cast<const T *>(p.rec_v) + tk * p.dv;
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            float u;
+            row_update<DK, false>(s[rr], tc, Elem<T>::load1(vrec + row0 + rr * kRowStride), &u);
+        }
+    }
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) store_row<DK>(S + (int64_t)(row0 + rr * kRowStride) * DK, l, s[rr]);
+}
+
+template <int DK, typename T>
+static cudaError_t launch_verify_t(const VerifyParams &p, cudaStream_t st) {
+    constexpr int R = 2;  // 32 rows x dk fp32 held in registers per CTA
+    const int64_t grid = (int64_t)p.batch * p.H * (p.dv / (kRowStride * R));
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    verify_kernel<DK, T, R><<<(unsigned)grid, kSpecWarps * 32, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <int DK, typename T>
+static cudaError_t launch_replay_t(const ReplayParams &p, cudaStream_t st) {
+    constexpr int R = 2;
+    const int64_t grid = (int64_t)p.batch * p.H * (p.dv / (kRowStride * R));
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    replay_kernel<DK, T, R><<<(unsigned)grid, kSpecWarps * 32, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_verify(const VerifyParams &p, int dk, int dtype, cudaStream_t st) {
+    if (dtype == KDA_DT_BF16) {
+        if (dk == 128) return launch_verify_t<128, __nv_bfloat16>(p, st);
+        if (dk == 64) return launch_verify_t<64, __nv_bfloat16>(p, st);
+        return launch_verify_t<32, __nv_bfloat16>(p, st);
+    }
+    if (dk == 128) return launch_verify_t<128, float>(p, st);
+    if (dk == 64) return launch_verify_t<64, float>(p, st);
+    return launch_verify_t<32, float>(p, st);
+}
+
+cudaError_t launch_replay(const ReplayParams &p, int dk, int dtype, cudaStream_t st) {
+    if (dtype == KDA_DT_BF16) {
+        if (dk == 128) return launch_replay_t<128, __nv_bfloat16>(p, st);
+        if (dk == 64) return launch_replay_t<64, __nv_bfloat16>(p, st);
+        return launch_replay_t<32, __nv_bfloat16>(p, st);
+    }
+    if (dk == 128) return launch_replay_t<128, float>(p, st);
+    if (dk == 64) return launch_replay_t<64, float>(p, st);
+    return launch_replay_t<32, float>(p, st);
+}
+
+}  // namespace kda

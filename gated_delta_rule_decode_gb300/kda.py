@@ -1,0 +1,266 @@
+"""Thin Python binding of libkda.so (argument marshalling only).
+
+Every function here checks tensor shapes, dtypes and devices, passes raw
+device pointers and the current CUDA stream to the C ABI declared in
+``include/kda.h``, and raises ``KdaError`` on a negative status.  All
+arithmetic runs in the library's CUDA kernels; there is no CPU or PyTorch
+fallback, and importing this module fails loudly if the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libkda.so")
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = -1
+KDA_ERR_UNSUPPORTED = -2
+KDA_ERR_CUDA = -3
+KDA_ERR_WORKSPACE = -4
+KDA_DT_F32 = 0
+KDA_DT_BF16 = 1
+KDA_DEVERR_SLOT = 1
+KDA_DEVERR_ACCEPTED = 2
+KDA_DEVERR_SEQLENS = 4
+KDA_DEVERR_TIMEOUT = 8
+
+EXPORTED = ("kda_decode", "kda_verify_record", "kda_replay_commit",
+            "kda_prefill_chunked", "kda_prefill_workspace_bytes",
+            "kda_records_bytes", "kda_status_string", "kda_abi_version")
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status}")
+
+
+class KdaDims(ctypes.Structure):
+    _fields_ = [("num_heads", ctypes.c_int32), ("dk", ctypes.c_int32),
+                ("dv", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("eps", ctypes.c_float), ("scale", ctypes.c_float)]
+
+
+class KdaRecords(ctypes.Structure):
+    _fields_ = [("k_hat", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p)]
+
+
+_VP = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_PD = ctypes.POINTER(KdaDims)
+_PR = ctypes.POINTER(KdaRecords)
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libkda.so and declare the C signatures.  Raises if it is missing."""
+    if not os.path.exists(path):
+        raise ImportError(
+            f"libkda.so not found at {path}; build it with "
+            "`python -m gated_delta_rule_decode_gb300.build` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(path)
+    lib.kda_decode.argtypes = [_PD, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                               _I64, _VP, _VP, _VP]
+    lib.kda_verify_record.argtypes = [_PD, _I32, _I32, _VP, _VP, _VP, _VP, _VP,
+                                      _VP, _VP, _I64, _VP, _PR, _VP, _VP]
+    lib.kda_replay_commit.argtypes = [_PD, _I32, _I32, _PR, _VP, _VP, _VP, _I64,
+                                      _VP, _VP]
+    lib.kda_prefill_chunked.argtypes = [_PD, _I32, _VP, _I64, _VP, _VP, _VP,
+                                        _VP, _VP, _VP, _VP, _I64, _I32, _VP,
+                                        _VP, _SZ, _VP, _VP]
+    lib.kda_prefill_workspace_bytes.argtypes = [_PD, _I32, _I64]
+    lib.kda_prefill_workspace_bytes.restype = _SZ
+    lib.kda_records_bytes.argtypes = [_PD, _I32, _I32]
+    lib.kda_records_bytes.restype = _SZ
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_abi_version.argtypes = []
+    for name in ("kda_decode", "kda_verify_record", "kda_replay_commit",
+                 "kda_prefill_chunked", "kda_abi_version"):
+        getattr(lib, name).restype = ctypes.c_int
+    return lib
+
+
+_lib = load_library()
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != KDA_OK:
+        msg = _lib.kda_status_string(status).decode()
+        raise KdaError(status, f"{what} failed ({msg})")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_DT_BF16
+    if t.dtype == torch.float32:
+        return KDA_DT_F32
+    raise TypeError(f"unsupported input dtype {t.dtype} (bf16 or fp32)")
+
+
+def make_dims(num_heads: int, dk: int, dv: int, dtype_code: int,
+              eps: float = 1e-6, scale: float | None = None) -> KdaDims:
+    return KdaDims(int(num_heads), int(dk), int(dv), int(dtype_code), float(eps),
+                   float(scale) if scale is not None else 0.0)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, shape, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+
+
+def decode(q, k, v, g, b, slot_ids, pool, out=None, *, eps=1e-6, scale=None,
+           err_flag=None, stream=None):
+    """One fused decode token per sequence, in place on ``pool``.
+
+    q, k: [B, H, dk]; v: [B, H, dv]; g: [B, H, dk] fp32; b: [B, H];
+    slot_ids: [B] int32; pool: [num_slots, H, dv, dk] fp32.  Returns out.
+    """
+    B, H, dk = k.shape
+    dv = v.shape[2]
+    dt = q.dtype
+    for name, t, shp, d in (("q", q, (B, H, dk), dt), ("k", k, (B, H, dk), dt),
+                            ("v", v, (B, H, dv), dt), ("g", g, (B, H, dk), torch.float32),
+                            ("b", b, (B, H), dt), ("slot_ids", slot_ids, (B,), torch.int32)):
+        _need(t, name, shp, d)
+    _need(pool, "pool", (pool.shape[0], H, dv, dk), torch.float32)
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=dt, device=q.device)
+    _need(out, "out", (B, H, dv), dt)
+    dims = make_dims(H, dk, dv, _dtype_code(q), eps, scale)
+    st = _lib.kda_decode(ctypes.byref(dims), B, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                         _ptr(b), _ptr(slot_ids), _ptr(pool), pool.shape[0], _ptr(out),
+                         _ptr(err_flag), _stream_handle(stream))
+    _check(st, "kda_decode")
+    return out
+
+
+def alloc_records(B, D, H, dk, dv, dtype, device):
+    """Allocate a ReplaySSM record set (dict of tensors) for (B, D)."""
+    return dict(
+        k_hat=torch.empty((B, D, H, dk), dtype=torch.float32, device=device),
+        v=torch.empty((B, D, H, dv), dtype=dtype, device=device),
+        g=torch.empty((B, D, H, dk), dtype=torch.float32, device=device),
+        beta=torch.empty((B, D, H), dtype=torch.float32, device=device))
+
+
+def _records_struct(rec) -> KdaRecords:
+    return KdaRecords(rec["k_hat"].data_ptr(), rec["v"].data_ptr(),
+                      rec["g"].data_ptr(), rec["beta"].data_ptr())
+
+
+def verify_record(q, k, v, g, b, slot_ids, pool, out=None, records=None, *,
+                  eps=1e-6, scale=None, err_flag=None, stream=None):
+    """ReplaySSM verify of D draft tokens; pool is read only.
+
+    q, k: [B, D, H, dk]; v: [B, D, H, dv]; g fp32; b: [B, D, H].
+    Returns (out [B, D, H, dv], records dict).
+    """
+    B, D, H, dk = k.shape
+    dv = v.shape[3]
+    dt = q.dtype
+    for name, t, shp, d in (("q", q, (B, D, H, dk), dt), ("k", k, (B, D, H, dk), dt),
+                            ("v", v, (B, D, H, dv), dt),
+                            ("g", g, (B, D, H, dk), torch.float32),
+                            ("b", b, (B, D, H), dt), ("slot_ids", slot_ids, (B,), torch.int32)):
+        _need(t, name, shp, d)
+    _need(pool, "pool", (pool.shape[0], H, dv, dk), torch.float32)
+    if out is None:
+        out = torch.empty((B, D, H, dv), dtype=dt, device=q.device)
+    _need(out, "out", (B, D, H, dv), dt)
+    if records is None:
+        records = alloc_records(B, D, H, dk, dv, dt, q.device)
+    rs = _records_struct(records)
+    dims = make_dims(H, dk, dv, _dtype_code(q), eps, scale)
+    st = _lib.kda_verify_record(ctypes.byref(dims), B, D, _ptr(q), _ptr(k), _ptr(v),
+                                _ptr(g), _ptr(b), _ptr(slot_ids), _ptr(pool),
+                                pool.shape[0], _ptr(out), ctypes.byref(rs),
+                                _ptr(err_flag), _stream_handle(stream))
+    _check(st, "kda_verify_record")
+    return out, records
+
+
+def replay_commit(records, num_accepted, slot_ids, pool, *, err_flag=None,
+                  stream=None):
+    """Replay the accepted prefix of each sequence's records onto ``pool``."""
+    B, D, H, dk = records["k_hat"].shape
+    dv = records["v"].shape[3]
+    dt = records["v"].dtype
+    _need(num_accepted, "num_accepted", (B,), torch.int32)
+    _need(slot_ids, "slot_ids", (B,), torch.int32)
+    _need(pool, "pool", (pool.shape[0], H, dv, dk), torch.float32)
+    rs = _records_struct(records)
+    dims = make_dims(H, dk, dv, _dtype_code(records["v"]))
+    st = _lib.kda_replay_commit(ctypes.byref(dims), B, D, ctypes.byref(rs),
+                                _ptr(num_accepted), _ptr(slot_ids), _ptr(pool),
+                                pool.shape[0], _ptr(err_flag), _stream_handle(stream))
+    _check(st, "kda_replay_commit")
+    del dt
+
+
+def prefill_workspace_bytes(H, dk, dv, dtype_code, num_seqs, total_tokens) -> int:
+    dims = make_dims(H, dk, dv, dtype_code)
+    return int(_lib.kda_prefill_workspace_bytes(ctypes.byref(dims), int(num_seqs),
+                                                int(total_tokens)))
+
+
+def prefill_chunked(q, k, v, g, b, cu_seqlens, slot_ids, pool, out=None, *,
+                    init_from_pool=False, workspace=None, eps=1e-6, scale=None,
+                    err_flag=None, stream=None):
+    """Chunked prefill of a packed variable-length batch.
+
+    q, k: [T, H, dk]; v: [T, H, dv]; g: [T, H, dk] fp32; b: [T, H];
+    cu_seqlens: [n+1] int32 (device); slot_ids: [n] int32.  The final state of
+    each sequence goes to its slot.  Returns out [T, H, dv].
+    """
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    n = slot_ids.shape[0]
+    dt = q.dtype
+    for name, t, shp, d in (("q", q, (T, H, dk), dt), ("k", k, (T, H, dk), dt),
+                            ("v", v, (T, H, dv), dt), ("g", g, (T, H, dk), torch.float32),
+                            ("b", b, (T, H), dt), ("cu_seqlens", cu_seqlens, (n + 1,), torch.int32),
+                            ("slot_ids", slot_ids, (n,), torch.int32)):
+        _need(t, name, shp, d)
+    _need(pool, "pool", (pool.shape[0], H, dv, dk), torch.float32)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=dt, device=q.device)
+    _need(out, "out", (T, H, dv), dt)
+    code = _dtype_code(q)
+    need = prefill_workspace_bytes(H, dk, dv, code, n, T)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    dims = make_dims(H, dk, dv, code, eps, scale)
+    st = _lib.kda_prefill_chunked(ctypes.byref(dims), n, _ptr(cu_seqlens), T, _ptr(q),
+                                  _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(slot_ids),
+                                  _ptr(pool), pool.shape[0], 1 if init_from_pool else 0,
+                                  _ptr(out), _ptr(workspace), ws_bytes, _ptr(err_flag),
+                                  _stream_handle(stream))
+    _check(st, "kda_prefill_chunked")
+    return out

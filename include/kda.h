@@ -1,0 +1,234 @@
+/*
+ * kda.h: C ABI of the GB300 (sm_103a) Kimi Delta Attention library, libkda.so.
+ *
+ * The library computes the KDA recurrence, i.e. the gated delta rule with one
+ * decay per key channel, over a pool of fp32 states.  For one (sequence, value
+ * head) with state S (dv x dk, "V x K": rows are value channels) and one token
+ * (q, k in R^dk, v in R^dv, g in R^dk, scalar b):
+ *
+ *   q^ = q / sqrt(sum q^2 + eps),  k^ = k / sqrt(sum k^2 + eps)   (Q/K L2Norm)
+ *   alpha_c = exp(g_c),  beta = sigmoid(b)            (gate and beta processing)
+ *   S' = S diag(alpha)                                (state decay)
+ *   u  = beta (v - S' k^)                             (delta rule)
+ *   S  = S' + u k^T                                   (outer-product update)
+ *   o  = scale * S q^                                 (output)
+ *   and S is written back in place                    (final-state write-back)
+ *
+ * Source of the step list: "Ascend day-0 support for Kimi K3"
+ * (hwcomputing.csdn.net/6a695b59...), section "Fused-operator acceleration:
+ * KDA Prefill and Decode dual path" (decode kernel paragraph; prefill in
+ * 64-token chunks; decode/MTP updates run directly on the state pool).
+ * Speculative verify/commit: "2.8x faster Kimi K3 inference on CANN"
+ * (hwcomputing.csdn.net/6ac7907e...), section 04 "ReplaySSM".
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ * - All tensor pointers are DEVICE pointers to contiguous row-major buffers,
+ *   16-byte aligned.  The caller allocates and frees everything; the library
+ *   never allocates device memory and keeps no global mutable state, so calls
+ *   on different streams are independent.
+ * - State pool: float32 [num_slots][H][dv][dk]; the state of (slot, head) is
+ *   one contiguous dv x dk block with dk fastest.
+ * - Slot ids are int32.  A negative slot id marks a padding entry: it is
+ *   skipped (outputs zero, no state access, no error).  A slot id >= num_slots
+ *   is an error: that entry is skipped the same way and KDA_DEVERR_SLOT is
+ *   OR-ed into *err_flag (when err_flag is non-NULL).  The same slot id twice
+ *   in one call is a precondition violation (the result is unspecified).
+ * - dtype: q, k, v, b and outputs share one element type (kda_dtype); g is
+ *   always float32; states and update records are float32.
+ * - Supported head sizes: dk and dv each in {32, 64, 128}.
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *   default stream) and never synchronise the host.  A host-detectable
+ *   argument error returns a negative kda_status and launches nothing.
+ *   A batch of 0 (or 0 tokens) returns KDA_OK and launches nothing.
+ * - Results are deterministic: no atomics touch data, so the same inputs give
+ *   bit-identical outputs and states run to run and regardless of batch order.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = -1,  /* NULL pointer, negative size, misalignment,
+                                  draft length outside 1..16, bad dims        */
+    KDA_ERR_UNSUPPORTED = -2,  /* dk/dv/dtype combination not built           */
+    KDA_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed        */
+    KDA_ERR_WORKSPACE = -4     /* prefill workspace NULL, too small, unaligned*/
+} kda_status;
+
+typedef enum kda_dtype {
+    KDA_DT_F32 = 0,
+    KDA_DT_BF16 = 1
+} kda_dtype;
+
+/* Bits OR-ed into *err_flag by the kernels (device-detected errors). */
+enum {
+    KDA_DEVERR_SLOT = 1,      /* slot id >= num_slots                          */
+    KDA_DEVERR_ACCEPTED = 2,  /* num_accepted outside 0..draft_len             */
+    KDA_DEVERR_SEQLENS = 4,   /* cu_seqlens not non-decreasing / past total_T  */
+    KDA_DEVERR_TIMEOUT = 8    /* an internal bounded wait gave up (prefill)    */
+};
+
+typedef struct kda_dims {
+    int32_t num_heads;  /* H >= 1; q, k, v share the head count               */
+    int32_t dk;         /* key head size, in {32, 64, 128}                    */
+    int32_t dv;         /* value head size, in {32, 64, 128}                  */
+    int32_t dtype;      /* kda_dtype of q, k, v, b and of the outputs         */
+    float eps;          /* L2Norm epsilon inside the sqrt (1e-6 typical), >=0 */
+    float scale;        /* output scale; <= 0 selects dk^-1/2                 */
+} kda_dims;
+
+/*
+ * ReplaySSM update records written by kda_verify_record and consumed by
+ * kda_replay_commit, one per (sequence, draft token, head):
+ *   k_hat  float32 [B][D][H][dk]  normalised key actually used
+ *   v      dtype   [B][D][H][dv]  value (bit copy of the input)
+ *   g      float32 [B][D][H][dk]  raw log-decay (bit copy of the input)
+ *   beta   float32 [B][D][H]      sigmoid(b) actually used
+ * Replaying record j applies exactly the arithmetic the decode kernel applies
+ * for that token, so replaying a records equals a kda_decode calls bit for bit.
+ */
+typedef struct kda_records {
+    float *k_hat;
+    void *v;
+    float *g;
+    float *beta;
+} kda_records;
+
+/*
+ * kda_decode: one token for each of `batch` sequences, fused single launch.
+ * Computes every step listed at the top for token n on the state of
+ * (slot_ids[n], h), for all heads h, and writes the state back in place.
+ * (Decode kernel paragraph of the "KDA Prefill and Decode dual path" section:
+ * one work item per logical sequence x value head.)
+ *
+ *   q, k     dtype  [batch][H][dk]
+ *   v        dtype  [batch][H][dv]
+ *   g        f32    [batch][H][dk]
+ *   b        dtype  [batch][H]
+ *   slot_ids i32    [batch]
+ *   pool     f32    [num_slots][H][dv][dk]   read and written in place
+ *   out      dtype  [batch][H][dv]           written (zero for skipped entries)
+ *   err_flag i32*   optional device word, device errors OR-ed in
+ */
+KDA_API int kda_decode(const kda_dims *dims, int32_t batch, const void *q,
+               const void *k, const void *v, const float *g, const void *b,
+               const int32_t *slot_ids, float *pool, int64_t num_slots,
+               void *out, int32_t *err_flag, void *stream);
+
+/*
+ * kda_verify_record: ReplaySSM verification of `draft_len` (1..16) draft
+ * tokens per sequence.  Runs the recurrence over the draft tokens in order
+ * starting from the committed state of (slot_ids[n], h) WITHOUT writing the
+ * pool, emits the output of every draft token, and stores only the update
+ * records (kda_records) instead of per-token states ("2.8x faster Kimi K3
+ * inference on CANN", section 04 "ReplaySSM").
+ *
+ *   q, k     dtype  [batch][draft_len][H][dk]
+ *   v        dtype  [batch][draft_len][H][dv]
+ *   g        f32    [batch][draft_len][H][dk]
+ *   b        dtype  [batch][draft_len][H]
+ *   pool     f32    [num_slots][H][dv][dk]   read only
+ *   out      dtype  [batch][draft_len][H][dv]
+ *   rec      records sized for (batch, draft_len); all four arrays written
+ *            for every entry, padding and errors included (they only depend
+ *            on the token inputs).
+ */
+KDA_API int kda_verify_record(const kda_dims *dims, int32_t batch, int32_t draft_len,
+                      const void *q, const void *k, const void *v,
+                      const float *g, const void *b, const int32_t *slot_ids,
+                      const float *pool, int64_t num_slots, void *out,
+                      const kda_records *rec, int32_t *err_flag, void *stream);
+
+/*
+ * kda_replay_commit: commit after acceptance.  For each sequence n with
+ * a = num_accepted[n] (0..draft_len), replays records 0..a-1 in order onto
+ * the committed state of (slot_ids[n], h) and writes it back:
+ *   S = S diag(exp g_j);  S = S + beta_j (v_j - S k_hat_j) k_hat_j^T.
+ * a == 0 leaves the state untouched (no memory access).  a outside
+ * 0..draft_len sets KDA_DEVERR_ACCEPTED and skips the sequence.
+ *
+ *   rec          records written by kda_verify_record for the same
+ *                (batch, draft_len, dims)
+ *   num_accepted i32 [batch] device
+ *   slot_ids     i32 [batch] device (normally those given to verify)
+ *   pool         f32 [num_slots][H][dv][dk] read and written in place
+ */
+KDA_API int kda_replay_commit(const kda_dims *dims, int32_t batch, int32_t draft_len,
+                      const kda_records *rec, const int32_t *num_accepted,
+                      const int32_t *slot_ids, float *pool, int64_t num_slots,
+                      int32_t *err_flag, void *stream);
+
+/*
+ * kda_prefill_chunked: chunked prefill of a variable-length batch.
+ * Sequence s covers tokens cu_seqlens[s] .. cu_seqlens[s+1]-1 of the packed
+ * token axis.  The tokens are processed in 64-token chunks (the last chunk of
+ * a sequence may be partial); within a chunk the work is put in WY/UT form:
+ *   gamma = in-chunk cumulative sum of g (gate accumulation),
+ *   T = (I + A)^-1 for the strictly lower-triangular beta-scaled decayed key
+ *   Gram matrix A, W = T diag(beta) K~, U' = T diag(beta) V, and across chunks
+ *   U = U' - W S^T,  O = scale (Q~ S^T + P U),  S <- S diag(e^gamma_C) + U^T K^.
+ * ("KDA Prefill and Decode dual path": prefill takes 64-token chunks and
+ * organises Q/K normalisation, gate accumulation and chunk KDA as batched
+ * computation.)  The result equals the token-by-token recurrence up to
+ * rounding.
+ *
+ *   cu_seqlens     i32 [num_seqs+1] device, non-decreasing, cu[0] = 0,
+ *                  cu[num_seqs] <= total_tokens
+ *   q, k           dtype [total_tokens][H][dk]
+ *   v              dtype [total_tokens][H][dv]
+ *   g              f32   [total_tokens][H][dk]
+ *   b              dtype [total_tokens][H]
+ *   slot_ids       i32   [num_seqs] device; the final state of sequence s is
+ *                  written to slot slot_ids[s]
+ *   init_from_pool 0: start from a zero state; 1: start from the slot's state
+ *   out            dtype [total_tokens][H][dv]
+ *   workspace      device scratch of at least
+ *                  kda_prefill_workspace_bytes(dims, num_seqs, total_tokens)
+ *                  bytes, 256-byte aligned, owned by the caller; its contents
+ *                  on entry do not matter and are undefined on return.
+ *                  Calls sharing one workspace must not overlap on the GPU.
+ */
+KDA_API int kda_prefill_chunked(const kda_dims *dims, int32_t num_seqs,
+                        const int32_t *cu_seqlens, int64_t total_tokens,
+                        const void *q, const void *k, const void *v,
+                        const float *g, const void *b,
+                        const int32_t *slot_ids, float *pool,
+                        int64_t num_slots, int32_t init_from_pool, void *out,
+                        void *workspace, size_t workspace_bytes,
+                        int32_t *err_flag, void *stream);
+
+/* Workspace bytes kda_prefill_chunked needs for this shape (0 on bad dims). */
+KDA_API size_t kda_prefill_workspace_bytes(const kda_dims *dims, int32_t num_seqs,
+                                   int64_t total_tokens);
+
+/* Total bytes of the four record arrays for (batch, draft_len). */
+KDA_API size_t kda_records_bytes(const kda_dims *dims, int32_t batch,
+                         int32_t draft_len);
+
+/* Static description of a status code ("ok", "invalid argument", ...). */
+KDA_API const char *kda_status_string(int status);
+
+/* KDA_ABI_VERSION of the built library. */
+KDA_API int kda_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,42 @@
+"""Shared helpers for the parity tests (tolerances, conversions, sampling)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+# Element-wise |x - ref| <= atol + rtol * |ref|, against fp64 oracle values
+# (outputs first rounded to the output dtype).  bf16 inputs: max-abs 2e-3 /
+# rel 1e-2; fp32 inputs: 1e-4 / 1e-4.
+TOL = {torch.bfloat16: (2e-3, 1e-2), torch.float32: (1e-4, 1e-4)}
+
+
+def tol_for(dtype):
+    return TOL[dtype]
+
+
+def to_np64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def round_to(x: np.ndarray, dtype) -> np.ndarray:
+    """Round fp64 oracle values to the output dtype (RNE), back to fp64."""
+    return torch.from_numpy(np.asarray(x, np.float64)).to(dtype).to(torch.float64).numpy()
+
+
+def assert_close(got, ref, atol, rtol, what=""):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    err = np.abs(got - ref)
+    bound = atol + rtol * np.abs(ref)
+    bad = ~(err <= bound)
+    if bad.any():
+        idx = np.argwhere(bad)[0]
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance "
+            f"(atol {atol}, rtol {rtol}); first at {tuple(idx)}: got {got[tuple(idx)]}, "
+            f"ref {ref[tuple(idx)]}; max abs err {err.max():.3e}")
+
+
+def err_flag(device="cuda"):
+    return torch.zeros(1, dtype=torch.int32, device=device)

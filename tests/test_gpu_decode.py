@@ -1,0 +1,134 @@
+"""GPU parity of kda_decode against the fp64 oracle (through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_decode_gb300 import inputs
+from kda_testutil import assert_close, err_flag, round_to, to_np64, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+def _kda():
+    from gated_delta_rule_decode_gb300 import kda
+    return kda
+
+
+def test_tiny_eight_sequential_decode_tokens_fp32():
+    """2 sequences x 2 heads, dk = dv = 32, 8 decode calls, fp32, zero state."""
+    kda = _kda()
+    w = inputs.WORKLOADS["tiny_decode_2x2_d32_8tok_f32"]
+    x = inputs.decode_inputs(w["B"], w["H"], w["dk"], w["dv"], dtype="f32",
+                             num_slots=w["num_slots"], seed=0, g_mean=2.0,
+                             zero_state=True, tokens=w["tokens"])
+    pool_ref = to_np64(x.pool)
+    pool = x.pool.cuda()
+    slots = x.slot_ids.cuda()
+    atol, rtol = tol_for(torch.float32)
+    flag = err_flag()
+    for t in range(w["tokens"]):
+        out = kda.decode(x.q[t].cuda(), x.k[t].cuda(), x.v[t].cuda(), x.g[t].cuda(),
+                         x.b[t].cuda(), slots, pool, err_flag=flag)
+        o_ref, pool_ref, e = oracle.decode(x.q[t], x.k[t], x.v[t], x.g[t], x.b[t],
+                                           x.slot_ids, pool_ref)
+        assert e == 0
+        assert_close(to_np64(out), o_ref, atol, rtol, f"token {t} output")
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    got = to_np64(pool)
+    assert_close(got, pool_ref, atol, rtol, "final states")
+    untouched = [s for s in range(w["num_slots"]) if s not in set(x.slot_ids.tolist())]
+    assert torch.equal(pool.cpu()[untouched], x.pool[untouched])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 64), (128, 128), (64, 128), (128, 32)])
+def test_decode_parity_shapes(dtype, dk, dv):
+    kda = _kda()
+    B, H, NS = 7, 3, 11
+    x = inputs.decode_inputs(B, H, dk, dv, dtype=dtype, num_slots=NS, seed=dk + dv,
+                             g_mean=3.0, pool_std=0.02)
+    slots = x.slot_ids.clone()
+    slots[2] = -1           # padding
+    slots[5] = NS + 3       # out of range -> error flag
+    pool = x.pool.cuda()
+    flag = err_flag()
+    out = kda.decode(x.q.cuda(), x.k.cuda(), x.v.cuda(), x.g.cuda(), x.b.cuda(),
+                     slots.cuda(), pool, err_flag=flag)
+    o_ref, p_ref, e = oracle.decode(x.q, x.k, x.v, x.g, x.b, slots, x.pool)
+    torch.cuda.synchronize()
+    assert e == H
+    assert flag.item() == kda.KDA_DEVERR_SLOT
+    dt = inputs.torch_dtype(dtype)
+    atol, rtol = tol_for(dt)
+    assert_close(to_np64(out), round_to(o_ref, dt), atol, rtol, "outputs")
+    assert torch.all(out[2] == 0) and torch.all(out[5] == 0)
+    assert_close(to_np64(pool), p_ref, atol, rtol, "pool")
+    touched = {int(s) for s in slots.tolist() if 0 <= s < NS}
+    untouched = [s for s in range(NS) if s not in touched]
+    assert torch.equal(pool.cpu()[untouched], x.pool[untouched])
+
+
+def test_decode_deterministic_and_batch_order_invariant():
+    kda = _kda()
+    B, H, dk, dv, NS = 33, 4, 128, 128, 64
+    x = inputs.decode_inputs(B, H, dk, dv, dtype="bf16", num_slots=NS, seed=5)
+    args = [t.cuda() for t in (x.q, x.k, x.v, x.g, x.b)]
+    slots = x.slot_ids.cuda()
+    p1 = x.pool.cuda()
+    p2 = x.pool.cuda()
+    o1 = kda.decode(*args, slots, p1)
+    o2 = kda.decode(*args, slots, p2)
+    assert torch.equal(o1, o2) and torch.equal(p1, p2)
+    perm = torch.randperm(B, generator=torch.Generator().manual_seed(1)).cuda()
+    p3 = x.pool.cuda()
+    o3 = kda.decode(*[a[perm].contiguous() for a in args], slots[perm].contiguous(), p3)
+    assert torch.equal(o3, o1[perm])
+    assert torch.equal(p3, p1)
+
+
+def test_decode_empty_batch_and_bad_arguments():
+    kda = _kda()
+    H, dk, dv = 2, 64, 64
+    pool = torch.zeros((4, H, dv, dk), device="cuda")
+    e = lambda *s: torch.empty(s, device="cuda")  # noqa: E731
+    out = kda.decode(e(0, H, dk), e(0, H, dk), e(0, H, dv), e(0, H, dk), e(0, H),
+                     torch.empty(0, dtype=torch.int32, device="cuda"), pool)
+    assert out.shape == (0, H, dv)
+    # unsupported head size is refused before any launch
+    with pytest.raises(kda.KdaError) as ei:
+        kda.decode(e(1, H, 48), e(1, H, 48), e(1, H, dv), e(1, H, 48), e(1, H),
+                   torch.zeros(1, dtype=torch.int32, device="cuda"),
+                   torch.zeros((4, H, dv, 48), device="cuda"))
+    assert ei.value.status == kda.KDA_ERR_UNSUPPORTED
+
+
+def test_decode_full_size_sampled():
+    """256 sequences x 32 heads, dk = dv = 128, bf16, 4096-slot pool (8 GiB):
+    the launch configuration the benchmark times; outputs and states checked
+    on a sample of (sequence, head) pairs, untouched slots bit-exact."""
+    kda = _kda()
+    w = inputs.WORKLOADS["decode_b256_h32_d128_pool4096_bf16"]
+    B, H, dk, dv, NS = w["B"], w["H"], w["dk"], w["dv"], w["num_slots"]
+    x = inputs.decode_inputs(B, H, dk, dv, dtype="bf16", num_slots=NS, seed=0,
+                             g_mean=3.0, pool_std=0.02, device="cuda")
+    rng = np.random.default_rng(0)
+    sample_n = np.sort(rng.choice(B, 12, replace=False))
+    sample_slots = x.slot_ids[torch.as_tensor(sample_n, device="cuda")].long()
+    before = x.pool[sample_slots].cpu()          # [12, H, dv, dk]
+    pool_before = x.pool.clone()
+    flag = err_flag()
+    out = kda.decode(x.q, x.k, x.v, x.g, x.b, x.slot_ids, x.pool, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    sn = torch.as_tensor(sample_n)
+    o_ref, p_ref, e = oracle.decode(x.q.cpu()[sn], x.k.cpu()[sn], x.v.cpu()[sn],
+                                    x.g.cpu()[sn], x.b.cpu()[sn],
+                                    torch.arange(len(sample_n), dtype=torch.int32), before)
+    atol, rtol = tol_for(torch.bfloat16)
+    assert_close(to_np64(out.cpu()[sn]), round_to(o_ref, torch.bfloat16), atol, rtol, "outputs")
+    assert_close(to_np64(x.pool[sample_slots].cpu()), p_ref, atol, rtol, "states")
+    touched = torch.zeros(NS, dtype=torch.bool, device="cuda")
+    touched[x.slot_ids.long()] = True
+    assert torch.equal(x.pool[~touched], pool_before[~touched])

@@ -1,0 +1,168 @@
+"""GPU parity of the ReplaySSM verify/commit pair against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_decode_gb300 import inputs
+from kda_testutil import assert_close, err_flag, round_to, to_np64, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+def _kda():
+    from gated_delta_rule_decode_gb300 import kda
+    return kda
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dk,dv,D", [(32, 32, 1), (64, 64, 7), (128, 128, 7), (128, 64, 16)])
+def test_verify_parity_records_and_pool_untouched(dtype, dk, dv, D):
+    kda = _kda()
+    B, H, NS = 5, 3, 9
+    x = inputs.verify_inputs(B, D, H, dk, dv, dtype=dtype, num_slots=NS, seed=dk + D)
+    slots = x.slot_ids.clone()
+    slots[1] = -1
+    pool = x.pool.cuda()
+    pool_before = pool.clone()
+    flag = err_flag()
+    out, rec = kda.verify_record(x.q.cuda(), x.k.cuda(), x.v.cuda(), x.g.cuda(),
+                                 x.b.cuda(), slots.cuda(), pool, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    assert torch.equal(pool, pool_before)
+    o_ref, r_ref, e = oracle.verify(x.q, x.k, x.v, x.g, x.b, slots, x.pool)
+    dt = inputs.torch_dtype(dtype)
+    atol, rtol = tol_for(dt)
+    assert_close(to_np64(out), round_to(o_ref, dt), atol, rtol, "verify outputs")
+    assert torch.all(out[1] == 0)
+    # records: normalised key (fp32 rounding of the fp64 value), bit copies of
+    # v and g, and beta = sigmoid(b)
+    assert_close(to_np64(rec["k_hat"]), r_ref["k_hat"], 1e-6, 1e-5, "k_hat records")
+    assert torch.equal(rec["v"].cpu(), x.v)
+    assert torch.equal(rec["g"].cpu(), x.g)
+    assert_close(to_np64(rec["beta"]), r_ref["beta"], 1e-7, 1e-6, "beta records")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dk,dv", [(32, 64), (128, 128)])
+def test_replay_equals_decode_bitwise_and_oracle(dtype, dk, dv):
+    kda = _kda()
+    B, D, H, NS = 8, 7, 2, 12
+    x = inputs.verify_inputs(B, D, H, dk, dv, dtype=dtype, num_slots=NS, seed=3 + dk)
+    acc = torch.tensor([0, 1, 2, 3, 4, 5, 6, 7], dtype=torch.int32)
+    pool_v = x.pool.cuda()
+    slots = x.slot_ids.cuda()
+    _, rec = kda.verify_record(x.q.cuda(), x.k.cuda(), x.v.cuda(), x.g.cuda(),
+                               x.b.cuda(), slots, pool_v)
+    pool_r = x.pool.cuda()
+    flag = err_flag()
+    kda.replay_commit(rec, acc.cuda(), slots, pool_r, err_flag=flag)
+    # reference 1: the decode kernel applied a_n times (bit-exact expected)
+    pool_d = x.pool.cuda()
+    for j in range(D):
+        live = (acc > j)
+        if not live.any():
+            break
+        idx = torch.nonzero(live).flatten()
+        kda.decode(*[t[idx, j].contiguous().cuda() for t in (x.q, x.k, x.v, x.g, x.b)],
+                   slots[idx.cuda()].contiguous(), pool_d)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    assert torch.equal(pool_r, pool_d), "replay differs from repeated decode"
+    # reference 2: fp64 recurrence over the accepted prefix of the ORIGINAL inputs
+    p_ref = to_np64(x.pool)
+    for n in range(B):
+        a = int(acc[n])
+        s = int(x.slot_ids[n])
+        for h in range(H):
+            if a == 0:
+                continue
+            _, S = oracle.recurrence(x.q[n, :a, h], x.k[n, :a, h], x.v[n, :a, h],
+                                     x.g[n, :a, h], x.b[n, :a, h], S0=p_ref[s, h])
+            p_ref[s, h] = S
+    atol, rtol = tol_for(inputs.torch_dtype(dtype))
+    assert_close(to_np64(pool_r), p_ref, atol, rtol, "committed states")
+    # a = 0 leaves the slot's bytes untouched
+    s0 = int(x.slot_ids[0])
+    assert torch.equal(pool_r[s0].cpu(), x.pool[s0])
+
+
+def test_verify_outputs_equal_sequential_decode_bitwise():
+    kda = _kda()
+    B, D, H, dk, dv, NS = 6, 7, 4, 128, 128, 16
+    x = inputs.verify_inputs(B, D, H, dk, dv, dtype="bf16", num_slots=NS, seed=17)
+    slots = x.slot_ids.cuda()
+    out, _ = kda.verify_record(x.q.cuda(), x.k.cuda(), x.v.cuda(), x.g.cuda(),
+                               x.b.cuda(), slots, x.pool.cuda())
+    pool_d = x.pool.cuda()
+    for j in range(D):
+        oj = kda.decode(*[t[:, j].contiguous().cuda() for t in (x.q, x.k, x.v, x.g, x.b)],
+                        slots, pool_d)
+        assert torch.equal(oj, out[:, j])
+
+
+def test_replay_rejects_bad_accepted_length_and_slot():
+    kda = _kda()
+    B, D, H, dk, dv, NS = 3, 4, 2, 64, 64, 6
+    x = inputs.verify_inputs(B, D, H, dk, dv, dtype="bf16", num_slots=NS, seed=2)
+    slots = x.slot_ids.clone()
+    _, rec = kda.verify_record(x.q.cuda(), x.k.cuda(), x.v.cuda(), x.g.cuda(),
+                               x.b.cuda(), slots.cuda(), x.pool.cuda())
+    pool = x.pool.cuda()
+    flag = err_flag()
+    kda.replay_commit(rec, torch.tensor([D + 1, 0, 2], dtype=torch.int32).cuda(),
+                      slots.cuda(), pool, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == kda.KDA_DEVERR_ACCEPTED
+    assert torch.equal(pool[int(slots[0])].cpu(), x.pool[int(slots[0])])
+    assert not torch.equal(pool[int(slots[2])].cpu(), x.pool[int(slots[2])])
+    flag.zero_()
+    slots2 = slots.clone()
+    slots2[2] = NS
+    kda.replay_commit(rec, torch.tensor([1, 1, 2], dtype=torch.int32).cuda(),
+                      slots2.cuda(), x.pool.cuda(), err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == kda.KDA_DEVERR_SLOT
+    with pytest.raises(kda.KdaError):
+        kda.verify_record(*[torch.zeros((1, 17, H, d), device="cuda", dtype=torch.bfloat16)
+                            for d in (dk, dk, dv)],
+                          torch.zeros((1, 17, H, dk), device="cuda"),
+                          torch.zeros((1, 17, H), device="cuda", dtype=torch.bfloat16),
+                          torch.zeros(1, dtype=torch.int32, device="cuda"),
+                          torch.zeros((1, H, dv, dk), device="cuda"))
+
+
+def test_verify_commit_full_size_sampled():
+    """128 sequences x 7 draft tokens x 32 heads, dk = dv = 128, bf16, 4096-slot
+    pool, accepted length uniform on 0..7: the configuration the benchmark
+    times.  Sampled sequences are checked against the oracle."""
+    kda = _kda()
+    w = inputs.WORKLOADS["verify_commit_b128_d7_h32_d128_bf16"]
+    B, D, H, dk, dv, NS = w["B"], w["D"], w["H"], w["dk"], w["dv"], w["num_slots"]
+    x = inputs.verify_inputs(B, D, H, dk, dv, dtype="bf16", num_slots=NS, seed=0,
+                             device="cuda")
+    rng = np.random.default_rng(1)
+    sn = torch.as_tensor(np.sort(rng.choice(B, 8, replace=False)))
+    ss = x.slot_ids.cpu()[sn].long()
+    before = x.pool[ss.cuda()].cpu()
+    pool_before = x.pool.clone()
+    flag = err_flag()
+    out, rec = kda.verify_record(x.q, x.k, x.v, x.g, x.b, x.slot_ids, x.pool, err_flag=flag)
+    torch.cuda.synchronize()
+    assert torch.equal(x.pool, pool_before)
+    kda.replay_commit(rec, x.num_accepted, x.slot_ids, x.pool, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    cpu = lambda t: t.cpu()[sn]  # noqa: E731
+    local = torch.arange(len(sn), dtype=torch.int32)
+    o_ref, r_ref, _ = oracle.verify(cpu(x.q), cpu(x.k), cpu(x.v), cpu(x.g), cpu(x.b),
+                                    local, before)
+    p_ref, _ = oracle.replay(r_ref, cpu(x.num_accepted), local, before)
+    atol, rtol = tol_for(torch.bfloat16)
+    assert_close(to_np64(out.cpu()[sn]), round_to(o_ref, torch.bfloat16), atol, rtol,
+                 "verify outputs")
+    assert_close(to_np64(x.pool[ss.cuda()].cpu()), p_ref, atol, rtol, "committed states")
+    touched = torch.zeros(NS, dtype=torch.bool, device="cuda")
+    touched[x.slot_ids.long()[x.num_accepted > 0]] = True
+    assert torch.equal(x.pool[~touched], pool_before[~touched])
