@@ -22,9 +22,43 @@ namespace kda {
 constexpr int kSpecWarps = 4;
 constexpr int kRowStride = kSpecWarps * kGroupsPerWarp;  // 16
 
+constexpr int kMaxDraft = 16;
+
+// Per-token coefficients of all draft tokens, staged in shared memory so that
+// the sequential token loop never waits on global memory.  Each 8-lane group
+// computes one token with the decode kernel's routine (same lane mapping,
+// same bits) and stores it at channel positions.
+template <int DK, int ROWS>
+struct SpecSmem {
+    float kh[kMaxDraft][DK];
+    float qh[kMaxDraft][DK];
+    float al[kMaxDraft][DK];
+    float beta[kMaxDraft];
+    float kq[kMaxDraft];
+    float v[kMaxDraft][ROWS];
+};
+
+template <int DK>
+__device__ __forceinline__ void put_lane_vec(float *dst, int l, const float (&x)[DK / kLanesPerRow]) {
+#pragma unroll
+    for (int j = 0; j < DK / 32; ++j)
+        *reinterpret_cast<float4 *>(dst + 4 * l + 32 * j) =
+            make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+}
+
+template <int DK>
+__device__ __forceinline__ void get_lane_vec(const float *src, int l, float (&x)[DK / kLanesPerRow]) {
+#pragma unroll
+    for (int j = 0; j < DK / 32; ++j) {
+        const float4 t = *reinterpret_cast<const float4 *>(src + 4 * l + 32 * j);
+        x[4 * j] = t.x; x[4 * j + 1] = t.y; x[4 * j + 2] = t.z; x[4 * j + 3] = t.w;
+    }
+}
+
 template <int DK, typename T, int R>
 __global__ void __launch_bounds__(kSpecWarps * 32) verify_kernel(const VerifyParams p) {
     constexpr int ROWS = kRowStride * R;
+    __shared__ __align__(16) SpecSmem<DK, ROWS> sm;
     const int nblk = p.dv / ROWS;
     const int64_t item = blockIdx.x;
     const int blk = (int)(item % nblk);
@@ -33,7 +67,8 @@ __global__ void __launch_bounds__(kSpecWarps * 32) verify_kernel(const VerifyPar
     const int n = (int)(sh / p.H);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = lane >> 3, l = lane & 7;
-    const int row0 = blk * ROWS + warp * kGroupsPerWarp + grp;
+    const int gid = warp * kGroupsPerWarp + grp;  // 0..15
+    const int row0 = blk * ROWS + gid;
 
     const int slot = __ldg(p.slot_ids + n);
     const bool valid = slot >= 0 && (int64_t)slot < p.num_slots;
@@ -46,44 +81,62 @@ __global__ void __launch_bounds__(kSpecWarps * 32) verify_kernel(const VerifyPar
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) load_row<DK>(S + (int64_t)(row0 + rr * kRowStride) * DK, l, s[rr]);
     }
-    const bool writes_key_record = (blk == 0 && warp == 0 && grp == 0);
 
-    for (int j = 0; j < p.D; ++j) {
+    // Phase 1: group gid prepares draft token gid (all tokens in parallel).
+    if (gid < p.D) {
+        const int j = gid;
         const int64_t tk = ((int64_t)n * p.D + j) * p.H + h;
-        const T *vrow = static_cast<const T *>(p.v) + tk * p.dv;
-        T *orow = static_cast<T *>(p.out) + tk * p.dv;
-        T *vrec = static_cast<T *>(p.rec_v) + tk * p.dv;
         TokenCoeffs<DK> tc;
         const float bb = Elem<T>::load1(static_cast<const T *>(p.b) + tk);
         make_coeffs<DK, T>(tc, static_cast<const T *>(p.q) + tk * DK,
                            static_cast<const T *>(p.k) + tk * DK, p.g + tk * DK, bb, p.eps, l);
-        if (writes_key_record) {
+        put_lane_vec<DK>(sm.kh[j], l, tc.kh);
+        put_lane_vec<DK>(sm.qh[j], l, tc.qh);
+        put_lane_vec<DK>(sm.al[j], l, tc.alpha);
+        if (l == 0) { sm.beta[j] = tc.beta; sm.kq[j] = tc.kq; }
+        if (blk == 0) {  // the key, gate and beta records (one writer per token)
             float *kr = p.rec_k_hat + tk * DK;
             float *gr = p.rec_g + tk * DK;
             const float *gi = p.g + tk * DK;
+            put_lane_vec<DK>(kr, l, tc.kh);
 #pragma unroll
-            for (int jj = 0; jj < DK / 32; ++jj) {
-                const int c = 4 * l + 32 * jj;
-                *reinterpret_cast<float4 *>(kr + c) =
-                    make_float4(tc.kh[4 * jj], tc.kh[4 * jj + 1], tc.kh[4 * jj + 2], tc.kh[4 * jj + 3]);
-                *reinterpret_cast<float4 *>(gr + c) = __ldg(reinterpret_cast<const float4 *>(gi + c));
-            }
+            for (int jj = 0; jj < DK / 32; ++jj)
+                *reinterpret_cast<float4 *>(gr + 4 * l + 32 * jj) =
+                    __ldg(reinterpret_cast<const float4 *>(gi + 4 * l + 32 * jj));
             if (l == 0) p.rec_beta[tk] = tc.beta;
         }
+    }
+    // this CTA's value rows of every draft token; value records are bit copies
+    for (int idx = threadIdx.x; idx < p.D * ROWS; idx += kSpecWarps * 32) {
+        const int j = idx / ROWS, r = idx % ROWS;
+        const int64_t tk = ((int64_t)n * p.D + j) * p.H + h;
+        const int64_t off = tk * p.dv + blk * ROWS + r;
+        const T raw = static_cast<const T *>(p.v)[off];
+        static_cast<T *>(p.rec_v)[off] = raw;
+        sm.v[j][r] = Elem<T>::to_f(raw);
+    }
+    __syncthreads();
+
+    // Phase 2: the draft tokens in order over the rows held in registers.
+    for (int j = 0; j < p.D; ++j) {
+        const int64_t tk = ((int64_t)n * p.D + j) * p.H + h;
+        T *orow = static_cast<T *>(p.out) + tk * p.dv;
+        TokenCoeffs<DK> tc;
+        get_lane_vec<DK>(sm.kh[j], l, tc.kh);
+        get_lane_vec<DK>(sm.qh[j], l, tc.qh);
+        get_lane_vec<DK>(sm.al[j], l, tc.alpha);
+        tc.beta = sm.beta[j];
+        tc.kq = sm.kq[j];
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
             const int row = row0 + rr * kRowStride;
-            const T v_raw = vrow[row];
             float o = 0.f;
             if (valid) {
                 float u;
-                const float c = row_update<DK, true>(s[rr], tc, Elem<T>::to_f(v_raw), &u);
+                const float c = row_update<DK, true>(s[rr], tc, sm.v[j][gid + rr * kRowStride], &u);
                 o = row_output(c, u, tc.kq, p.scale);
             }
-            if (l == 0) {
-                vrec[row] = v_raw;
-                Elem<T>::store1(orow + row, o);
-            }
+            if (l == 0) Elem<T>::store1(orow + row, o);
         }
     }
 }
@@ -91,6 +144,7 @@ __global__ void __launch_bounds__(kSpecWarps * 32) verify_kernel(const VerifyPar
 template <int DK, typename T, int R>
 __global__ void __launch_bounds__(kSpecWarps * 32) replay_kernel(const ReplayParams p) {
     constexpr int ROWS = kRowStride * R;
+    __shared__ __align__(16) SpecSmem<DK, ROWS> sm;
     const int nblk = p.dv / ROWS;
     const int64_t item = blockIdx.x;
     const int blk = (int)(item % nblk);
@@ -99,7 +153,8 @@ __global__ void __launch_bounds__(kSpecWarps * 32) replay_kernel(const ReplayPar
     const int n = (int)(sh / p.H);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = lane >> 3, l = lane & 7;
-    const int row0 = blk * ROWS + warp * kGroupsPerWarp + grp;
+    const int gid = warp * kGroupsPerWarp + grp;
+    const int row0 = blk * ROWS + gid;
 
     const int a = __ldg(p.num_accepted + n);
     const int slot = __ldg(p.slot_ids + n);
@@ -120,15 +175,31 @@ __global__ void __launch_bounds__(kSpecWarps * 32) replay_kernel(const ReplayPar
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) load_row<DK>(S + (int64_t)(row0 + rr * kRowStride) * DK, l, s[rr]);
 
-    for (int j = 0; j < a; ++j) {
-        const int64_t tk = ((int64_t)n * p.D + j) * p.H + h;
+    // Phase 1: group gid loads record gid (all accepted records in parallel).
+    if (gid < a) {
+        const int64_t tk = ((int64_t)n * p.D + gid) * p.H + h;
         TokenCoeffs<DK> tc;
         coeffs_from_record<DK>(tc, p.rec_k_hat + tk * DK, p.rec_g + tk * DK, __ldg(p.rec_beta + tk), l);
-        const T *vrec = static_cast<const T *>(p.rec_v) + tk * p.dv;
+        put_lane_vec<DK>(sm.kh[gid], l, tc.kh);
+        put_lane_vec<DK>(sm.al[gid], l, tc.alpha);
+        if (l == 0) sm.beta[gid] = tc.beta;
+    }
+    for (int idx = threadIdx.x; idx < a * ROWS; idx += kSpecWarps * 32) {
+        const int j = idx / ROWS, r = idx % ROWS;
+        const int64_t tk = ((int64_t)n * p.D + j) * p.H + h;
+        sm.v[j][r] = Elem<T>::load1(static_cast<const T *>(p.rec_v) + tk * p.dv + blk * ROWS + r);
+    }
+    __syncthreads();
+
+    for (int j = 0; j < a; ++j) {
+        TokenCoeffs<DK> tc;
+        get_lane_vec<DK>(sm.kh[j], l, tc.kh);
+        get_lane_vec<DK>(sm.al[j], l, tc.alpha);
+        tc.beta = sm.beta[j];
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
             float u;
-            row_update<DK, false>(s[rr], tc, Elem<T>::load1(vrec + row0 + rr * kRowStride), &u);
+            row_update<DK, false>(s[rr], tc, sm.v[j][gid + rr * kRowStride], &u);
         }
     }
 #pragma unroll
