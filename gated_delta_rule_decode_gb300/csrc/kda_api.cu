@@ -128,7 +128,8 @@ int kda_replay_commit(const kda_dims *dims, int32_t batch, int32_t draft_len,
 
 size_t kda_prefill_workspace_bytes(const kda_dims *dims, int32_t num_seqs, int64_t total_tokens) {
     if (check_dims(dims) != KDA_OK || num_seqs < 0 || total_tokens < 0) return 0;
-    return kda::prefill_workspace_bytes(dims->num_heads, dims->dk, dims->dv, num_seqs, total_tokens);
+    return kda::prefill_workspace_bytes(dims->num_heads, dims->dk, dims->dv, dims->dtype, num_seqs,
+                                        total_tokens);
 }
 
 int kda_prefill_chunked(const kda_dims *dims, int32_t num_seqs, const int32_t *cu_seqlens,
@@ -145,7 +146,7 @@ int kda_prefill_chunked(const kda_dims *dims, int32_t num_seqs, const int32_t *c
         return KDA_ERR_INVALID_ARG;
     if (num_slots > 0 && !all_aligned({pool})) return KDA_ERR_INVALID_ARG;
     if (total_tokens > (int64_t)0x7fffffff) return KDA_ERR_INVALID_ARG;
-    const size_t need = kda::prefill_workspace_bytes(dims->num_heads, dims->dk, dims->dv,
+    const size_t need = kda::prefill_workspace_bytes(dims->num_heads, dims->dk, dims->dv, dims->dtype,
                                                      num_seqs, total_tokens);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
                      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))

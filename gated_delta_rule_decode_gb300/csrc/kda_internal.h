@@ -74,6 +74,10 @@ cudaError_t launch_decode(const DecodeParams &p, int dk, int dtype, cudaStream_t
 cudaError_t launch_verify(const VerifyParams &p, int dk, int dtype, cudaStream_t s);
 cudaError_t launch_replay(const ReplayParams &p, int dk, int dtype, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams &p, int dtype, cudaStream_t s);
-size_t prefill_workspace_bytes(int H, int dk, int dv, int32_t num_seqs, int64_t total_tokens);
+size_t prefill_workspace_bytes(int H, int dk, int dv, int dtype, int32_t num_seqs, int64_t total_tokens);
+
+// Tensor-core prefill (dk = dv = 128, bf16): needs only the chunk plan.
+bool prefill_tc_supported(int dk, int dv, int dtype);
+cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s);
 
 }  // namespace kda

@@ -461,12 +461,22 @@ static cudaError_t launch_dtype(const PrefillParams &p, cudaStream_t st) {
 
 }  // namespace prefill
 
-size_t prefill_workspace_bytes(int H, int dk, int dv, int32_t num_seqs, int64_t total_tokens) {
+size_t prefill_workspace_bytes(int H, int dk, int dv, int dtype, int32_t num_seqs, int64_t total_tokens) {
     const prefill::WsLayout L = prefill::ws_layout(dk, dv, num_seqs, total_tokens);
+    if (prefill_tc_supported(dk, dv, dtype)) return L.plan_bytes;
     return L.plan_bytes + (size_t)L.max_chunks * (size_t)H * L.chunk_bytes;
 }
 
 cudaError_t launch_prefill(const PrefillParams &p, int dtype, cudaStream_t st) {
+    if (prefill_tc_supported(p.dk, p.dv, dtype)) {
+        // tensor-core path: the plan validates cu_seqlens, then one CTA per
+        // (sequence, head) walks the chunks
+        prefill::plan_kernel<<<1, 32, 0, st>>>(p.cu_seqlens, p.num_seqs, p.total_tokens,
+                                               static_cast<int32_t *>(p.workspace), p.err_flag);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return launch_prefill_tc(p, st);
+    }
     if (dtype == KDA_DT_BF16) return prefill::launch_dtype<__nv_bfloat16>(p, st);
     return prefill::launch_dtype<float>(p, st);
 }
