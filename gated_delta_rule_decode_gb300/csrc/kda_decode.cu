@@ -119,7 +119,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_bulk_kernel(const DecodePa
     make_coeffs<DK, T>(tc, static_cast<const T *>(p.q) + sh * DK, static_cast<const T *>(p.k) + sh * DK,
                        p.g + sh * DK, bb, p.eps, l);
     __syncthreads();  // barrier initialised before anyone waits on it
-    if (!mbar_wait(&bar, 0)) {
+    // the outcome is made CTA-uniform so that no thread skips a later barrier
+    if (__syncthreads_and(mbar_wait(&bar, 0)) == 0) {
         if (threadIdx.x == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
         mbar_wait(&bar, 0);  // bounded second chance for the copy in flight
         return;

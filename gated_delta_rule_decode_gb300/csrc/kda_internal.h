@@ -76,8 +76,10 @@ cudaError_t launch_replay(const ReplayParams &p, int dk, int dtype, cudaStream_t
 cudaError_t launch_prefill(const PrefillParams &p, int dtype, cudaStream_t s);
 size_t prefill_workspace_bytes(int H, int dk, int dv, int dtype, int32_t num_seqs, int64_t total_tokens);
 
-// Tensor-core prefill (dk = dv = 128, bf16): needs only the chunk plan.
+// Tensor-core prefill (dk = dv = 128, bf16): a prep kernel over all chunks
+// writes per-(chunk, head) operand images, a chain kernel walks the chunks.
 bool prefill_tc_supported(int dk, int dv, int dtype);
+size_t prefill_tc_workspace_bytes(int H, int32_t num_seqs, int64_t total_tokens);
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t s);
 
 }  // namespace kda

@@ -463,14 +463,15 @@ static cudaError_t launch_dtype(const PrefillParams &p, cudaStream_t st) {
 
 size_t prefill_workspace_bytes(int H, int dk, int dv, int dtype, int32_t num_seqs, int64_t total_tokens) {
     const prefill::WsLayout L = prefill::ws_layout(dk, dv, num_seqs, total_tokens);
-    if (prefill_tc_supported(dk, dv, dtype)) return L.plan_bytes;
+    if (prefill_tc_supported(dk, dv, dtype)) return prefill_tc_workspace_bytes(H, num_seqs, total_tokens);
     return L.plan_bytes + (size_t)L.max_chunks * (size_t)H * L.chunk_bytes;
 }
 
 cudaError_t launch_prefill(const PrefillParams &p, int dtype, cudaStream_t st) {
     if (prefill_tc_supported(p.dk, p.dv, dtype)) {
-        // tensor-core path: the plan validates cu_seqlens, then one CTA per
-        // (sequence, head) walks the chunks
+        // tensor-core path: the plan validates cu_seqlens and numbers the
+        // chunks, the prep kernel builds every chunk's operands, the chain
+        // kernel walks them
         prefill::plan_kernel<<<1, 32, 0, st>>>(p.cu_seqlens, p.num_seqs, p.total_tokens,
                                                static_cast<int32_t *>(p.workspace), p.err_flag);
         cudaError_t e = cudaGetLastError();

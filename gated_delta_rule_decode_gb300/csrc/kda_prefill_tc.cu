@@ -1,34 +1,34 @@
 // Tensor-core chunked prefill (tcgen05 + TMEM), dk = dv = 128, bf16 inputs.
 //
-// One CTA (4 warps) owns one (sequence, head) and walks its 64-token chunks
-// in order ("Ascend day-0 support for Kimi K3", section "KDA Prefill and
-// Decode dual path": 64-token chunks, with Q/K normalisation, gate
-// accumulation and the chunk KDA organised as batched computation).  The
-// chunk form (WY/UT, gamma = in-chunk cumulative gate per key channel):
+// "Ascend day-0 support for Kimi K3", section "KDA Prefill and Decode dual
+// path": the prefill takes 64-token chunks and organises Q/K normalisation,
+// gate accumulation and the chunk KDA as batched computation.  The chunk
+// form (WY/UT; gamma = in-chunk cumulative gate per key channel):
 //
 //   A = strict-lower( beta_r sum_c k^_r k^_j e^{gamma_r - gamma_j} ),
 //   P = lower( sum_c q^_r k^_j e^{gamma_r - gamma_j} ),  T = (I + A)^-1
-//   W^T = (beta K~)^T T^T,  U'^T = (beta V)^T T^T            (WY factors)
+//   W^T = (beta K~)^T T^T,  U'^T = (beta V)^T T^T                (WY factors)
 //   U^T = U'^T - S W^T,  O^T = scale (S Q~^T + U^T P^T),
-//   S <- S diag(e^{gamma_C}) + U^T K^                        (chunk step)
+//   S <- S diag(e^{gamma_C}) + U^T K^                            (chunk step)
 //
-// The fp32 state S (dv x dk) never leaves tensor memory: it is the A operand
-// of the MMAs that read it (TMEM lane = value row, column = key channel) and
-// the accumulator of the rank-64 update.  All five products run on tcgen05
-// in kind::tf32 with fp32 accumulation; B operands are staged in shared
-// memory in the K-major 128-byte-swizzled layout.
+// Two kernels, both on tcgen05 (kind::tf32, fp32 accumulate):
 //
-// TMEM columns (512 allocated, one CTA per SM):
-//   [0,128)   S                         [128,256) D1: S W^T | S Q~^T + U^T P^T
-//   [256,320) U^T (Q~^T during prep)    [320,384) G = [K+;Q+] K-^T (A' | P)
-//   [384,448) W^T                       [448,512) U'^T
-//   During prep D1 holds the A operands (beta K~)^T and (beta V)^T.
+// prep_tc_kernel  one CTA per (chunk, head), all chunks of all sequences in
+//   parallel over the whole GPU.  Computes everything that does not depend on
+//   the state and writes, per (chunk, head), an operand image that the chain
+//   kernel copies into shared memory with one bulk copy:
+//     [W; Q~] (128 x 128), P (64 x 64), K^^T (128 x 64) as K-major 128B-swizzled
+//     tf32 tiles, e^{gamma_C} (128) and U'^T (128 x 64, plain fp32).
+// chain_tc_kernel  one CTA per (sequence, head) walks the chunks in order.
+//   The fp32 state never leaves tensor memory: it is the A operand of
+//   D1 = S [W; Q~]^T and the accumulator of S += U^T K^.  The operand image of
+//   chunk c+1 is in flight (bulk copy, double-buffered) while chunk c computes.
 //
-// Decay factors: with ref = gamma at token 31 of the chunk, K+ = k^ e^{gamma-ref},
-// Q+ = q^ e^{gamma-ref}, K- = k^ e^{ref-gamma}, so that K+ K-^T carries
-// e^{gamma_r - gamma_j}.  A chunk whose gamma spans more than 80 (natural
-// units) around ref on some channel would overflow these factors; such a
-// chunk computes A and P with one exp per (r, j, c) on the CUDA cores.
+// Decay factors in the A/P product: with ref = gamma at token 31 of the chunk,
+// K+ = k^ e^{gamma-ref}, Q+ = q^ e^{gamma-ref}, K- = k^ e^{ref-gamma}, so that
+// [K+; Q+] K-^T carries e^{gamma_r - gamma_j}.  A chunk whose gamma spans more
+// than 80 (natural units) around ref on some channel would overflow these
+// factors; that chunk computes A and P with one exp per (r, j, c) instead.
 #include <stdint.h>
 
 #include "kda.h"
@@ -40,45 +40,31 @@
 namespace kda {
 namespace prefill_tc {
 
-constexpr int C = 64;    // chunk length
-constexpr int D = 128;   // dk = dv
+constexpr int C = 64;   // chunk length
+constexpr int D = 128;  // dk = dv
 constexpr int kThreads = 128;
-constexpr int TM_S = 0, TM_D1 = 128, TM_UT = 256, TM_G = 320, TM_WT = 384, TM_UPT = 448;
-constexpr int TM_BKT = TM_D1, TM_BVT = TM_D1 + 64, TM_QT = TM_UT;
-constexpr uint32_t TM_COLS = 512;
 constexpr float kSpanLimit = 80.f;
 
-struct Smem {
-    unsigned char bufA[128 * 128 * 4];  // [K+;Q+] then [W;Q~]   (128 rows x K 128)
-    unsigned char bufKM[64 * 128 * 4];  // K-                     (64 rows x K 128)
-    unsigned char bufT[64 * 64 * 4];    // T                      (64 rows x K 64)
-    unsigned char bufP[64 * 64 * 4];    // P                      (64 rows x K 64)
-    unsigned char bufKT[128 * 64 * 4];  // K^^T                   (128 rows x K 64)
-    float As[C][C + 1];
-    float Ts[C][C + 1];
-    float Xs[3][16][17];
-    float invk[C], invq[C], beta[C];
-    float egc[D];
-    uint64_t bar;
-    uint32_t tmem_base;
-};
+// Operand image of one (chunk, head) in the workspace (bytes).
+constexpr uint32_t IMG_BW = 0;                         // [W; Q~]  128 rows x K 128
+constexpr uint32_t IMG_P = IMG_BW + 128 * 128 * 4;     // P        64 rows x K 64
+constexpr uint32_t IMG_KT = IMG_P + 64 * 64 * 4;       // K^^T     128 rows x K 64
+constexpr uint32_t IMG_TILES = IMG_KT + 128 * 64 * 4;  // = 112 KiB, one bulk copy
+constexpr uint32_t IMG_EGC = IMG_TILES;                // e^{gamma_C}, 128 fp32
+constexpr uint32_t IMG_UPT = IMG_EGC + 1024;           // U'^T plain [128][64] fp32
+constexpr uint32_t IMG_BYTES = IMG_UPT + 128 * 64 * 4;
 
-constexpr size_t kSmemBytes = sizeof(Smem) + 1024;
+__host__ __device__ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline size_t plan_bytes(int32_t num_seqs) {
+    return round_up(sizeof(int32_t) * ((size_t)num_seqs + 2), 1024);
+}
+__host__ __device__ inline int64_t max_chunks(int32_t num_seqs, int64_t total_tokens) {
+    return (total_tokens + C - 1) / C + num_seqs;
+}
 
 __device__ __forceinline__ void st_sw(unsigned char *tile, int rows, int row, int k, float x) {
     *reinterpret_cast<float *>(tile + tc::sw128_off(row, k, rows)) = x;
-}
-
-// Bounded wait on the CTA's MMA barrier; records a timeout.  The result is
-// made uniform across the CTA so that every thread leaves the chunk loop
-// together.
-__device__ __forceinline__ bool wait_mma(Smem &sm, uint32_t &phase, int32_t *err_flag) {
-    const bool mine = mbar_wait(&sm.bar, phase & 1);
-    phase ^= 1;
-    const bool ok = __syncthreads_and(mine) != 0;
-    if (!ok && threadIdx.x == 0 && err_flag) atomicOr(err_flag, KDA_DEVERR_TIMEOUT);
-    tc::fence_after_sync();
-    return ok;
 }
 
 __device__ __forceinline__ void sync_for_mma() {
@@ -88,177 +74,198 @@ __device__ __forceinline__ void sync_for_mma() {
     tc::fence_after_sync();
 }
 
+// Bounded wait on an MMA-completion barrier; the result is made uniform across
+// the CTA and a timeout is recorded in the error flag.
+__device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t &phase, int32_t *err_flag) {
+    const bool mine = mbar_wait(bar, phase & 1);
+    phase ^= 1;
+    const bool ok = __syncthreads_and(mine) != 0;
+    if (!ok && threadIdx.x == 0 && err_flag) atomicOr(err_flag, KDA_DEVERR_TIMEOUT);
+    tc::fence_after_sync();
+    return ok;
+}
+
+// Sequence s owning global chunk index c (plan[s] <= c < plan[s+1]).
+__device__ inline int find_seq(const int32_t *plan, int n, int32_t c) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (plan[mid] <= c) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// ================================================================== prep
+
+// TMEM columns of the prep kernel.
+constexpr int PT_BKT = 0, PT_BVT = 64, PT_G = 128, PT_WT = 192, PT_UPT = 256;
+constexpr uint32_t PT_COLS = 512;
+
+struct PrepSmem {
+    unsigned char bufKQ[128 * 128 * 4];  // [K+; Q+]  (A of the A/P product)
+    unsigned char bufKM[64 * 128 * 4];   // K-        (B of the A/P product)
+    unsigned char bufT[64 * 64 * 4];     // T         (B of the WY products)
+    float As[C][C + 1];
+    float Ts[C][C + 1];
+    float Xs[3][16][17];
+    float invk[C], invq[C], beta[C];
+    uint64_t bar;
+    uint32_t tmem_base;
+};
+constexpr size_t kPrepSmem = sizeof(PrepSmem) + 1024;
+
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const PrefillParams p) {
     extern __shared__ unsigned char smem_raw[];
-    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    PrepSmem &sm =
+        *reinterpret_cast<PrepSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int32_t *plan = static_cast<const int32_t *>(p.workspace);
     const int n = p.num_seqs;
     if (plan[n + 1] == 0) return;
-    const int s = blockIdx.x, h = blockIdx.y, H = p.H;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int32_t cs = p.cu_seqlens[s], ce = p.cu_seqlens[s + 1];
+    const int32_t chunk = blockIdx.x;
+    if (chunk >= plan[n]) return;
+    const int h = blockIdx.y, H = p.H;
+    const int s = find_seq(plan, n, chunk);
     const int slot = p.slot_ids[s];
+    if (slot < 0 || (int64_t)slot >= p.num_slots) return;  // the chain writes zeros
+    const int64_t t0 = (int64_t)p.cu_seqlens[s] + (int64_t)(chunk - plan[s]) * C;
+    const int L = (int)((int64_t)p.cu_seqlens[s + 1] - t0 < C ? (int64_t)p.cu_seqlens[s + 1] - t0 : C);
+    const int tid = threadIdx.x, warp = tid >> 5;
     const T *q = static_cast<const T *>(p.q);
     const T *k = static_cast<const T *>(p.k);
     const T *v = static_cast<const T *>(p.v);
     const T *bb = static_cast<const T *>(p.b);
-    T *out = static_cast<T *>(p.out);
-    const int64_t tok_stride = (int64_t)H * D;
+    const int64_t tok_stride = (int64_t)H * D, hoff = (int64_t)h * D;
+    unsigned char *img = static_cast<unsigned char *>(p.workspace) + plan_bytes(n) +
+                         ((size_t)chunk * H + h) * (size_t)IMG_BYTES;
 
-    if (slot < 0 || (int64_t)slot >= p.num_slots) {
-        for (int64_t t = cs; t < ce; ++t) Elem<T>::store1(out + t * tok_stride + (int64_t)h * D + tid, 0.f);
-        if (slot >= 0 && h == 0 && tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_SLOT);
-        return;
-    }
-
-    if (warp == 0) tc::tmem_alloc(&sm.tmem_base, TM_COLS);
+    if (warp == 0) tc::tmem_alloc(&sm.tmem_base, PT_COLS);
     if (tid == 0) {
         mbar_init(&sm.bar, 1);
         fence_barrier_init();
+    }
+
+    // ---- 1a. inverse norms (thread = token row) and beta
+    {
+        const int r = tid & 63;
+        const bool isq = tid >= 64;
+        float inv = 0.f;
+        if (r < L) {
+            const T *row = (isq ? q : k) + (t0 + r) * tok_stride + hoff;
+            float ss = 0.f;
+#pragma unroll 8
+            for (int j = 0; j < D; j += 4) {
+                const float4 x = Elem<T>::load4(row + j);
+                ss = fmaf(x.x, x.x, ss);
+                ss = fmaf(x.y, x.y, ss);
+                ss = fmaf(x.z, x.z, ss);
+                ss = fmaf(x.w, x.w, ss);
+            }
+            inv = rsqrtf(ss + p.eps);
+        }
+        if (isq) {
+            sm.invq[r] = inv;
+        } else {
+            sm.invk[r] = inv;
+            sm.beta[r] = (r < L) ? sigmoid_f(Elem<T>::load1(bb + (t0 + r) * H + h)) : 0.f;
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tm = sm.tmem_base;
     uint32_t phase = 0;
-    bool ok = true;
-    float *Sg = p.pool + ((int64_t)slot * H + h) * (int64_t)D * D;
 
-    // initial state: TMEM lane i = value row i
-#pragma unroll 1
-    for (int c0 = 0; c0 < D; c0 += 16) {
-        float vv[16];
+    // ---- 1b. thread = key channel c (and value row i = c)
+    const int c = tid;
+    float gam[C];
+    {
+        float acc = 0.f;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) vv[j] = p.init_from_pool ? Sg[(int64_t)tid * D + c0 + j] : 0.f;
-        tc::st16(tc::lane_addr(tm, warp, TM_S + c0), vv);
+        for (int r = 0; r < C; ++r) {
+            if (r < L) acc += __ldg(p.g + (t0 + r) * tok_stride + hoff + c);
+            gam[r] = acc;
+        }
+    }
+    float gC = gam[0];
+#pragma unroll
+    for (int r = 1; r < C; ++r)
+        if (r == L - 1) gC = gam[r];
+    const float ref = gam[31];
+    float span = 0.f;
+#pragma unroll
+    for (int r = 0; r < C; ++r) span = fmaxf(span, fabsf(gam[r] - ref));
+    reinterpret_cast<float *>(img + IMG_EGC)[c] = expf(gC);
+    const bool unsafe = __syncthreads_or(span > kSpanLimit) != 0;
+    {
+        const float eref = expf(ref);
+        const float egcref = expf(gC - ref);
+        float bkt[16], bvt[16];
+        float kt4[4];
+#pragma unroll
+        for (int r = 0; r < C; ++r) {
+            const bool valid = r < L;
+            const int64_t off = (t0 + r) * tok_stride + hoff + c;
+            const float kx = valid ? Elem<T>::load1(k + off) * sm.invk[r] : 0.f;
+            const float qx = valid ? Elem<T>::load1(q + off) * sm.invq[r] : 0.f;
+            const float vx = valid ? Elem<T>::load1(v + off) : 0.f;
+            float ktil, qtil, khat_end;
+            if (!unsafe) {
+                const float E = __expf(gam[r] - ref);
+                const float Ei = __expf(ref - gam[r]);
+                const float kp = kx * E, qp = qx * E;
+                st_sw(sm.bufKQ, 128, r, c, kp);
+                st_sw(sm.bufKQ, 128, 64 + r, c, qp);
+                st_sw(sm.bufKM, 64, r, c, kx * Ei);
+                ktil = kp * eref;
+                qtil = qp * eref;
+                khat_end = kx * Ei * egcref;
+            } else {
+                // plain [64][128] copies of k^, q^ and gamma for the exact path
+                reinterpret_cast<float *>(sm.bufKQ)[r * D + c] = kx;
+                reinterpret_cast<float *>(sm.bufKQ)[C * D + r * D + c] = qx;
+                reinterpret_cast<float *>(sm.bufKM)[r * D + c] = gam[r];
+                const float eg = expf(gam[r]);
+                ktil = kx * eg;
+                qtil = qx * eg;
+                khat_end = kx * expf(gC - gam[r]);
+            }
+            st_sw(img + IMG_BW, 128, 64 + r, c, qtil);  // Q~ rows of [W; Q~]
+            kt4[r & 3] = valid ? khat_end : 0.f;
+            if ((r & 3) == 3)
+                *reinterpret_cast<float4 *>(img + IMG_KT + tc::sw128_off(c, r - 3, 128)) =
+                    make_float4(kt4[0], kt4[1], kt4[2], kt4[3]);
+            bkt[r & 15] = sm.beta[r] * ktil;
+            bvt[r & 15] = sm.beta[r] * vx;
+            if ((r & 15) == 15) {
+                tc::st16(tc::lane_addr(tm, warp, PT_BKT + (r - 15)), bkt);
+                tc::st16(tc::lane_addr(tm, warp, PT_BVT + (r - 15)), bvt);
+            }
+        }
     }
     tc::wait_st();
+    sync_for_mma();
 
-    const int nchunks = (ce - cs + C - 1) / C;
-    for (int ci = 0; ci < nchunks && ok; ++ci) {
-        const int64_t t0 = (int64_t)cs + (int64_t)ci * C;
-        const int L = (int)((int64_t)ce - t0 < C ? (int64_t)ce - t0 : C);
-        const int64_t hoff = (int64_t)h * D;
-
-        // ---- 1a. inverse norms (thread = token row) and beta
-        {
-            const int r = tid & 63;
-            const bool isq = tid >= 64;
-            float inv = 0.f;
-            if (r < L) {
-                const T *row = (isq ? q : k) + (t0 + r) * tok_stride + hoff;
-                float ss = 0.f;
-#pragma unroll 8
-                for (int j = 0; j < D; j += 4) {
-                    const float4 x = Elem<T>::load4(row + j);
-                    ss = fmaf(x.x, x.x, ss);
-                    ss = fmaf(x.y, x.y, ss);
-                    ss = fmaf(x.z, x.z, ss);
-                    ss = fmaf(x.w, x.w, ss);
-                }
-                inv = rsqrtf(ss + p.eps);
-            }
-            if (isq) {
-                sm.invq[r] = inv;
-            } else {
-                sm.invk[r] = inv;
-                sm.beta[r] = (r < L) ? sigmoid_f(Elem<T>::load1(bb + (t0 + r) * H + h)) : 0.f;
-            }
+    bool ok = true;
+    // ---- 2. A and P
+    if (!unsafe) {
+        if (tid == 0) {
+            constexpr uint32_t id = tc::idesc_tf32(128, 64);
+            const uint32_t a0 = tc::smem_u32(sm.bufKQ), b0 = tc::smem_u32(sm.bufKM);
+#pragma unroll
+            for (int ks = 0; ks < D / 8; ++ks)
+                tc::mma_tf32_ss(tm + PT_G, tc::desc_tf32_kstep(a0, 128, ks), tc::desc_tf32_kstep(b0, 64, ks), id,
+                                ks > 0);
+            tc::commit(&sm.bar);
         }
-        __syncthreads();
-
-        // ---- 1b. thread = key channel c: gate cumsum and the chunk operands
-        const int c = tid;
-        float gam[C];
-        {
-            float acc = 0.f;
-#pragma unroll
-            for (int r = 0; r < C; ++r) {
-                if (r < L) acc += __ldg(p.g + (t0 + r) * tok_stride + hoff + c);
-                gam[r] = acc;
-            }
-        }
-        float gC = gam[0];
-#pragma unroll
-        for (int r = 1; r < C; ++r)
-            if (r == L - 1) gC = gam[r];
-        const float ref = gam[31];
-        float span = 0.f;
-#pragma unroll
-        for (int r = 0; r < C; ++r) span = fmaxf(span, fabsf(gam[r] - ref));
-        sm.egc[c] = expf(gC);
-        const bool unsafe = __syncthreads_or(span > kSpanLimit) != 0;
-
-        {
-            const float eref = expf(ref);
-            const float egcref = expf(gC - ref);
-            float bkt[16], qt[16], bvt[16];
-            float kt4[4];
-#pragma unroll
-            for (int r = 0; r < C; ++r) {
-                const bool valid = r < L;
-                const int64_t off = (t0 + r) * tok_stride + hoff + c;
-                const float kx = valid ? Elem<T>::load1(k + off) * sm.invk[r] : 0.f;
-                const float qx = valid ? Elem<T>::load1(q + off) * sm.invq[r] : 0.f;
-                const float vx = valid ? Elem<T>::load1(v + off) : 0.f;
-                float ktil, qtil, khat_end;
-                if (!unsafe) {
-                    const float E = __expf(gam[r] - ref);
-                    const float Ei = __expf(ref - gam[r]);
-                    const float kp = kx * E, qp = qx * E;
-                    st_sw(sm.bufA, 128, r, c, kp);
-                    st_sw(sm.bufA, 128, 64 + r, c, qp);
-                    st_sw(sm.bufKM, 64, r, c, kx * Ei);
-                    ktil = kp * eref;
-                    qtil = qp * eref;
-                    khat_end = kx * Ei * egcref;
-                } else {
-                    // plain [64][128] copies of k^, q^ and gamma for the exact path
-                    reinterpret_cast<float *>(sm.bufA)[r * D + c] = kx;
-                    reinterpret_cast<float *>(sm.bufA)[C * D + r * D + c] = qx;
-                    reinterpret_cast<float *>(sm.bufKM)[r * D + c] = gam[r];
-                    const float eg = expf(gam[r]);
-                    ktil = kx * eg;
-                    qtil = qx * eg;
-                    khat_end = kx * expf(gC - gam[r]);
-                }
-                kt4[r & 3] = valid ? khat_end : 0.f;
-                if ((r & 3) == 3)
-                    *reinterpret_cast<float4 *>(sm.bufKT + tc::sw128_off(c, r - 3, 128)) =
-                        make_float4(kt4[0], kt4[1], kt4[2], kt4[3]);
-                bkt[r & 15] = sm.beta[r] * ktil;
-                qt[r & 15] = qtil;
-                bvt[r & 15] = sm.beta[r] * vx;  // thread c is also value row i = c
-                if ((r & 15) == 15) {
-                    tc::st16(tc::lane_addr(tm, warp, TM_BKT + (r - 15)), bkt);
-                    tc::st16(tc::lane_addr(tm, warp, TM_QT + (r - 15)), qt);
-                    tc::st16(tc::lane_addr(tm, warp, TM_BVT + (r - 15)), bvt);
-                }
-            }
-        }
-        tc::wait_st();
-        sync_for_mma();
-
-        // ---- 2. A and P
-        if (!unsafe) {
-            if (tid == 0) {
-                constexpr uint32_t id = tc::idesc_tf32(128, 64);
-                const uint32_t a0 = tc::smem_u32(sm.bufA), b0 = tc::smem_u32(sm.bufKM);
-#pragma unroll
-                for (int ks = 0; ks < D / 8; ++ks)
-                    tc::mma_tf32_ss(tm + TM_G, tc::desc_tf32_kstep(a0, 128, ks), tc::desc_tf32_kstep(b0, 64, ks),
-                                    id, ks > 0);
-                tc::commit(&sm.bar);
-            }
-            ok = wait_mma(sm, phase, p.err_flag);
-            if (!ok) break;
-            // lanes 0..63: rows of A' ; lanes 64..127: rows of P
+        ok = wait_mma(&sm.bar, phase, p.err_flag);
+        if (ok) {
+            // lanes 0..63: rows of A'; lanes 64..127: rows of P
             const int r = tid & 63;
             float g16[16];
 #pragma unroll
             for (int j0 = 0; j0 < C; j0 += 16) {
-                tc::ld16(tc::lane_addr(tm, warp, TM_G + j0), g16);
+                tc::ld16(tc::lane_addr(tm, warp, PT_G + j0), g16);
                 tc::wait_ld();
                 if (tid < 64) {
 #pragma unroll
@@ -270,35 +277,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
 #pragma unroll
                     for (int jj = 0; jj < 16; jj += 4) {
                         const int j = j0 + jj;
-                        *reinterpret_cast<float4 *>(sm.bufP + tc::sw128_off(r, j, 64)) =
+                        *reinterpret_cast<float4 *>(img + IMG_P + tc::sw128_off(r, j, 64)) =
                             make_float4(j <= r ? g16[jj] : 0.f, j + 1 <= r ? g16[jj + 1] : 0.f,
                                         j + 2 <= r ? g16[jj + 2] : 0.f, j + 3 <= r ? g16[jj + 3] : 0.f);
                     }
                 }
             }
-        } else {
-            // exact path: one exp per (r, j, c)
-            const float *kh = reinterpret_cast<const float *>(sm.bufA);
-            const float *qh = kh + C * D;
-            const float *gm = reinterpret_cast<const float *>(sm.bufKM);
-            for (int idx = tid; idx < C * C; idx += kThreads) {
-                const int r = idx / C, j = idx % C;
-                float a = 0.f, pp = 0.f;
-                if (j <= r) {
-                    for (int cc = 0; cc < D; ++cc) {
-                        const float m = kh[j * D + cc] * expf(gm[r * D + cc] - gm[j * D + cc]);
-                        a = fmaf(kh[r * D + cc], m, a);
-                        pp = fmaf(qh[r * D + cc], m, pp);
-                    }
-                }
-                sm.As[r][j] = (j < r) ? sm.beta[r] * a : 0.f;
-                *reinterpret_cast<float *>(sm.bufP + tc::sw128_off(r, j, 64)) = (j <= r) ? pp : 0.f;
-            }
         }
-        __syncthreads();
+    } else {
+        const float *kh = reinterpret_cast<const float *>(sm.bufKQ);
+        const float *qh = kh + C * D;
+        const float *gm = reinterpret_cast<const float *>(sm.bufKM);
+        for (int idx = tid; idx < C * C; idx += kThreads) {
+            const int r = idx / C, j = idx % C;
+            float a = 0.f, pp = 0.f;
+            if (j <= r) {
+                for (int cc = 0; cc < D; ++cc) {
+                    const float m = kh[j * D + cc] * expf(gm[r * D + cc] - gm[j * D + cc]);
+                    a = fmaf(kh[r * D + cc], m, a);
+                    pp = fmaf(qh[r * D + cc], m, pp);
+                }
+            }
+            sm.As[r][j] = (j < r) ? sm.beta[r] * a : 0.f;
+            *reinterpret_cast<float *>(img + IMG_P + tc::sw128_off(r, j, 64)) = (j <= r) ? pp : 0.f;
+        }
+    }
+    __syncthreads();
 
+    if (ok) {
         // ---- 2c. T = (I + A)^-1: diagonal 16x16 blocks by forward
-        // substitution, then off-diagonal blocks T_IJ = -T_II sum_K A_IK T_KJ
+        // substitution, then T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ by distance
         for (int idx = tid; idx < C * (C + 1); idx += kThreads) (&sm.Ts[0][0])[idx] = 0.f;
         __syncthreads();
         if (tid < 64) {
@@ -354,92 +362,200 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
 #pragma unroll
             for (int ks = 0; ks < C / 8; ++ks) {
                 const uint64_t bd = tc::desc_tf32_kstep(b0, 64, ks);
-                tc::mma_tf32_ts(tm + TM_WT, tm + TM_BKT + 8 * ks, bd, id, ks > 0);
-                tc::mma_tf32_ts(tm + TM_UPT, tm + TM_BVT + 8 * ks, bd, id, ks > 0);
+                tc::mma_tf32_ts(tm + PT_WT, tm + PT_BKT + 8 * ks, bd, id, ks > 0);
+                tc::mma_tf32_ts(tm + PT_UPT, tm + PT_BVT + 8 * ks, bd, id, ks > 0);
             }
             tc::commit(&sm.bar);
         }
-        ok = wait_mma(sm, phase, p.err_flag);
-        if (!ok) break;
-        // [W; Q~] into bufA as the B operand of the chunk step (thread = channel)
-        {
+        ok = wait_mma(&sm.bar, phase, p.err_flag);
+        if (ok) {
             float w16[16];
+            float *upt = reinterpret_cast<float *>(img + IMG_UPT) + (size_t)tid * C;
 #pragma unroll
             for (int r0 = 0; r0 < C; r0 += 16) {
-                tc::ld16(tc::lane_addr(tm, warp, TM_WT + r0), w16);
+                tc::ld16(tc::lane_addr(tm, warp, PT_WT + r0), w16);  // lane c: W[r][c]
                 tc::wait_ld();
 #pragma unroll
-                for (int rr = 0; rr < 16; ++rr) st_sw(sm.bufA, 128, r0 + rr, c, w16[rr]);
-                tc::ld16(tc::lane_addr(tm, warp, TM_QT + r0), w16);
+                for (int rr = 0; rr < 16; ++rr) st_sw(img + IMG_BW, 128, r0 + rr, c, w16[rr]);
+                tc::ld16(tc::lane_addr(tm, warp, PT_UPT + r0), w16);  // lane i: U'^T[i][r]
                 tc::wait_ld();
 #pragma unroll
-                for (int rr = 0; rr < 16; ++rr) st_sw(sm.bufA, 128, 64 + r0 + rr, c, w16[rr]);
+                for (int rr = 0; rr < 16; rr += 4)
+                    *reinterpret_cast<float4 *>(upt + r0 + rr) =
+                        make_float4(w16[rr], w16[rr + 1], w16[rr + 2], w16[rr + 3]);
             }
         }
-        sync_for_mma();
+    }
+    if (!ok) mbar_wait(&sm.bar, (phase ^ 1) & 1);  // let a late MMA finish (bounded)
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tm, PT_COLS);
+}
 
-        // ---- 4. D1 = S [W; Q~]^T
+// ================================================================== chain
+
+// TMEM columns of the chain kernel.
+constexpr int CT_S = 0, CT_D1 = 128, CT_UT = 256;
+constexpr uint32_t CT_COLS = 512;
+
+struct ChainSmem {
+    unsigned char stage[2][IMG_TILES];  // [W;Q~] | P | K^^T, double-buffered
+    float egc[2][D];
+    uint64_t full[2];
+    uint64_t mma;
+    uint32_t tmem_base;
+};
+constexpr size_t kChainSmem = sizeof(ChainSmem) + 1024;
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    ChainSmem &sm =
+        *reinterpret_cast<ChainSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int32_t *plan = static_cast<const int32_t *>(p.workspace);
+    const int n = p.num_seqs;
+    if (plan[n + 1] == 0) return;
+    const int s = blockIdx.x, h = blockIdx.y, H = p.H;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int32_t cs = p.cu_seqlens[s], ce = p.cu_seqlens[s + 1];
+    const int slot = p.slot_ids[s];
+    T *out = static_cast<T *>(p.out);
+    const int64_t tok_stride = (int64_t)H * D, hoff = (int64_t)h * D;
+    if (slot < 0 || (int64_t)slot >= p.num_slots) {
+        for (int64_t t = cs; t < ce; ++t) Elem<T>::store1(out + t * tok_stride + hoff + tid, 0.f);
+        if (slot >= 0 && h == 0 && tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_SLOT);
+        return;
+    }
+    const int nchunks = plan[s + 1] - plan[s];
+    const unsigned char *ws = static_cast<const unsigned char *>(p.workspace) + plan_bytes(n);
+    auto image = [&](int ci) {
+        return ws + ((size_t)(plan[s] + ci) * H + h) * (size_t)IMG_BYTES;
+    };
+
+    if (warp == 0) tc::tmem_alloc(&sm.tmem_base, CT_COLS);
+    if (tid == 0) {
+        mbar_init(&sm.full[0], 1);
+        mbar_init(&sm.full[1], 1);
+        mbar_init(&sm.mma, 1);
+        fence_barrier_init();
+        if (nchunks > 0) {
+            mbar_arrive_expect_tx(&sm.full[0], IMG_TILES + D * 4);
+            bulk_g2s(sm.stage[0], image(0), IMG_TILES, &sm.full[0]);
+            bulk_g2s(sm.egc[0], image(0) + IMG_EGC, D * 4, &sm.full[0]);
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = sm.tmem_base;
+    float *Sg = p.pool + ((int64_t)slot * H + h) * (int64_t)D * D;
+    {
+        float vv[16];
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 16) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) vv[j] = p.init_from_pool ? Sg[(int64_t)tid * D + c0 + j] : 0.f;
+            tc::st16(tc::lane_addr(tm, warp, CT_S + c0), vv);
+        }
+        tc::wait_st();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+
+    uint32_t mphase = 0;
+    bool ok = true;
+    for (int ci = 0; ci < nchunks; ++ci) {
+        const int st = ci & 1;
+        const int64_t t0 = (int64_t)cs + (int64_t)ci * C;
+        const int L = (int)((int64_t)ce - t0 < C ? (int64_t)ce - t0 : C);
+        // prefetch the next chunk's image into the other stage (its previous
+        // user, chunk ci-1, has finished all its MMAs and reads)
+        if (tid == 0 && ci + 1 < nchunks) {
+            mbar_arrive_expect_tx(&sm.full[st ^ 1], IMG_TILES + D * 4);
+            bulk_g2s(sm.stage[st ^ 1], image(ci + 1), IMG_TILES, &sm.full[st ^ 1]);
+            bulk_g2s(sm.egc[st ^ 1], image(ci + 1) + IMG_EGC, D * 4, &sm.full[st ^ 1]);
+        }
+        // this thread's row of U'^T (value row i = tid), in flight during MMA 1
+        float upt[C];
+        {
+            const float4 *src = reinterpret_cast<const float4 *>(image(ci) + IMG_UPT) + (size_t)tid * (C / 4);
+#pragma unroll
+            for (int j = 0; j < C / 4; ++j) {
+                const float4 x = __ldg(src + j);
+                upt[4 * j] = x.x; upt[4 * j + 1] = x.y; upt[4 * j + 2] = x.z; upt[4 * j + 3] = x.w;
+            }
+        }
+        const bool landed = mbar_wait(&sm.full[st], (ci >> 1) & 1);
+        if (__syncthreads_and(landed) == 0) {
+            if (tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
+            ok = false;
+            break;
+        }
+        tc::fence_after_sync();
+        const uint32_t sb = tc::smem_u32(sm.stage[st]);
+
+        // ---- D1 = S [W; Q~]^T
         if (tid == 0) {
             constexpr uint32_t id = tc::idesc_tf32(128, 128);
-            const uint32_t b0 = tc::smem_u32(sm.bufA);
 #pragma unroll
             for (int ks = 0; ks < D / 8; ++ks)
-                tc::mma_tf32_ts(tm + TM_D1, tm + TM_S + 8 * ks, tc::desc_tf32_kstep(b0, 128, ks), id, ks > 0);
-            tc::commit(&sm.bar);
+                tc::mma_tf32_ts(tm + CT_D1, tm + CT_S + 8 * ks, tc::desc_tf32_kstep(sb + IMG_BW, 128, ks), id,
+                                ks > 0);
+            tc::commit(&sm.mma);
         }
-        ok = wait_mma(sm, phase, p.err_flag);
+        ok = wait_mma(&sm.mma, mphase, p.err_flag);
         if (!ok) break;
-        // U^T = U'^T - S W^T (thread = value row i); S <- S diag(e^{gamma_C})
+        // U^T = U'^T - S W^T;  S <- S diag(e^{gamma_C})
         {
-            float a16[16], b16[16];
+            float a16[16];
 #pragma unroll
             for (int r0 = 0; r0 < C; r0 += 16) {
-                tc::ld16(tc::lane_addr(tm, warp, TM_UPT + r0), a16);
-                tc::ld16(tc::lane_addr(tm, warp, TM_D1 + r0), b16);
+                tc::ld16(tc::lane_addr(tm, warp, CT_D1 + r0), a16);
                 tc::wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) a16[j] -= b16[j];
-                tc::st16(tc::lane_addr(tm, warp, TM_UT + r0), a16);
+                for (int j = 0; j < 16; ++j) a16[j] = upt[r0 + j] - a16[j];
+                tc::st16(tc::lane_addr(tm, warp, CT_UT + r0), a16);
             }
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 16) {
-                tc::ld16(tc::lane_addr(tm, warp, TM_S + c0), a16);
+                tc::ld16(tc::lane_addr(tm, warp, CT_S + c0), a16);
                 tc::wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) a16[j] *= sm.egc[c0 + j];
-                tc::st16(tc::lane_addr(tm, warp, TM_S + c0), a16);
+                for (int j = 0; j < 16; ++j) a16[j] *= sm.egc[st][c0 + j];
+                tc::st16(tc::lane_addr(tm, warp, CT_S + c0), a16);
             }
             tc::wait_st();
         }
         sync_for_mma();
-
-        // ---- 5. O^T += U^T P^T ; S += U^T K^
+        // ---- O^T += U^T P^T ;  S += U^T K^
         if (tid == 0) {
             constexpr uint32_t id64 = tc::idesc_tf32(128, 64);
             constexpr uint32_t id128 = tc::idesc_tf32(128, 128);
-            const uint32_t bp = tc::smem_u32(sm.bufP), bk = tc::smem_u32(sm.bufKT);
 #pragma unroll
             for (int ks = 0; ks < C / 8; ++ks) {
-                tc::mma_tf32_ts(tm + TM_D1 + 64, tm + TM_UT + 8 * ks, tc::desc_tf32_kstep(bp, 64, ks), id64, 1);
-                tc::mma_tf32_ts(tm + TM_S, tm + TM_UT + 8 * ks, tc::desc_tf32_kstep(bk, 128, ks), id128, 1);
+                tc::mma_tf32_ts(tm + CT_D1 + 64, tm + CT_UT + 8 * ks, tc::desc_tf32_kstep(sb + IMG_P, 64, ks), id64,
+                                1);
+                tc::mma_tf32_ts(tm + CT_S, tm + CT_UT + 8 * ks, tc::desc_tf32_kstep(sb + IMG_KT, 128, ks), id128,
+                                1);
             }
-            tc::commit(&sm.bar);
+            tc::commit(&sm.mma);
         }
-        ok = wait_mma(sm, phase, p.err_flag);
+        ok = wait_mma(&sm.mma, mphase, p.err_flag);
         if (!ok) break;
         {
             float o16[16];
             const float scale = p.scale;
 #pragma unroll
             for (int r0 = 0; r0 < C; r0 += 16) {
-                tc::ld16(tc::lane_addr(tm, warp, TM_D1 + 64 + r0), o16);
+                tc::ld16(tc::lane_addr(tm, warp, CT_D1 + 64 + r0), o16);
                 tc::wait_ld();
 #pragma unroll
                 for (int rr = 0; rr < 16; ++rr)
-                    if (r0 + rr < L)
-                        Elem<T>::store1(out + (t0 + r0 + rr) * tok_stride + hoff + tid, scale * o16[rr]);
+                    if (r0 + rr < L) Elem<T>::store1(out + (t0 + r0 + rr) * tok_stride + hoff + tid, scale * o16[rr]);
             }
         }
+        fence_proxy_async_smem();  // this stage's e^{gamma_C} reads before its next bulk refill
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
@@ -449,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
         float s16[16];
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 16) {
-            tc::ld16(tc::lane_addr(tm, warp, TM_S + c0), s16);
+            tc::ld16(tc::lane_addr(tm, warp, CT_S + c0), s16);
             tc::wait_ld();
 #pragma unroll
             for (int j = 0; j < 16; j += 4)
@@ -457,13 +573,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const PrefillPa
                     make_float4(s16[j], s16[j + 1], s16[j + 2], s16[j + 3]);
         }
     } else {
-        // bounded: let the MMA group whose wait gave up finish before the
-        // tensor memory is released (its phase is the one before `phase`)
-        mbar_wait(&sm.bar, (phase ^ 1) & 1);
+        // bounded waits so that no MMA or bulk copy is still writing when the
+        // CTA releases its memory
+        mbar_wait(&sm.mma, (mphase ^ 1) & 1);
+        mbar_wait(&sm.full[0], 0);
+        mbar_wait(&sm.full[1], 0);
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tm, TM_COLS);
+    if (warp == 0) tc::tmem_dealloc(tm, CT_COLS);
 }
 
 }  // namespace prefill_tc
@@ -476,13 +594,26 @@ bool prefill_tc_supported(int dk, int dv, int dtype) {
     return KDA_PREFILL_TC && dtype == KDA_DT_BF16 && dk == 128 && dv == 128;
 }
 
+size_t prefill_tc_workspace_bytes(int H, int32_t num_seqs, int64_t total_tokens) {
+    using namespace prefill_tc;
+    return plan_bytes(num_seqs) + (size_t)max_chunks(num_seqs, total_tokens) * (size_t)H * IMG_BYTES;
+}
+
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
     using namespace prefill_tc;
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<__nv_bfloat16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(prep_tc_kernel<__nv_bfloat16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)p.num_seqs, (unsigned)p.H);
-    prefill_tc_kernel<__nv_bfloat16><<<grid, kThreads, kSmemBytes, st>>>(p);
+    e = cudaFuncSetAttribute(chain_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kChainSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t mc = max_chunks(p.num_seqs, p.total_tokens);
+    if (mc > 0) {
+        prep_tc_kernel<__nv_bfloat16><<<dim3((unsigned)mc, (unsigned)p.H), kThreads, kPrepSmem, st>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    chain_tc_kernel<__nv_bfloat16><<<dim3((unsigned)p.num_seqs, (unsigned)p.H), kThreads, kChainSmem, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -83,27 +83,36 @@ __global__ void __launch_bounds__(kSpecWarps * 32) verify_kernel(const VerifyPar
     }
 
     // Phase 1: group gid prepares draft token gid (all tokens in parallel).
-    if (gid < p.D) {
-        const int j = gid;
+    // Every lane of the warp runs make_coeffs, whose reductions are full-warp
+    // shuffles: groups past the last draft token recompute the last token
+    // and discard the result.
+    {
+        const bool mine = gid < p.D;
+        const int j = mine ? gid : p.D - 1;
         const int64_t tk = ((int64_t)n * p.D + j) * p.H + h;
         TokenCoeffs<DK> tc;
         const float bb = Elem<T>::load1(static_cast<const T *>(p.b) + tk);
         make_coeffs<DK, T>(tc, static_cast<const T *>(p.q) + tk * DK,
                            static_cast<const T *>(p.k) + tk * DK, p.g + tk * DK, bb, p.eps, l);
-        put_lane_vec<DK>(sm.kh[j], l, tc.kh);
-        put_lane_vec<DK>(sm.qh[j], l, tc.qh);
-        put_lane_vec<DK>(sm.al[j], l, tc.alpha);
-        if (l == 0) { sm.beta[j] = tc.beta; sm.kq[j] = tc.kq; }
-        if (blk == 0) {  // the key, gate and beta records (one writer per token)
-            float *kr = p.rec_k_hat + tk * DK;
-            float *gr = p.rec_g + tk * DK;
-            const float *gi = p.g + tk * DK;
-            put_lane_vec<DK>(kr, l, tc.kh);
+        if (mine) {
+            put_lane_vec<DK>(sm.kh[j], l, tc.kh);
+            put_lane_vec<DK>(sm.qh[j], l, tc.qh);
+            put_lane_vec<DK>(sm.al[j], l, tc.alpha);
+            if (l == 0) {
+                sm.beta[j] = tc.beta;
+                sm.kq[j] = tc.kq;
+            }
+            if (blk == 0) {  // the key, gate and beta records (one writer per token)
+                float *kr = p.rec_k_hat + tk * DK;
+                float *gr = p.rec_g + tk * DK;
+                const float *gi = p.g + tk * DK;
+                put_lane_vec<DK>(kr, l, tc.kh);
 #pragma unroll
-            for (int jj = 0; jj < DK / 32; ++jj)
-                *reinterpret_cast<float4 *>(gr + 4 * l + 32 * jj) =
-                    __ldg(reinterpret_cast<const float4 *>(gi + 4 * l + 32 * jj));
-            if (l == 0) p.rec_beta[tk] = tc.beta;
+                for (int jj = 0; jj < DK / 32; ++jj)
+                    *reinterpret_cast<float4 *>(gr + 4 * l + 32 * jj) =
+                        __ldg(reinterpret_cast<const float4 *>(gi + 4 * l + 32 * jj));
+                if (l == 0) p.rec_beta[tk] = tc.beta;
+            }
         }
     }
     // this CTA's value rows of every draft token; value records are bit copies

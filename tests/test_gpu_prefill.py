@@ -103,6 +103,23 @@ def test_prefill_strong_decay():
     assert_close(to_np64(pool), p_ref, atol, rtol, "states")
 
 
+@pytest.mark.parametrize("g_mean", [-3.0, 0.0, 6.0])
+def test_prefill_decay_range_bf16_d128(g_mean):
+    """Strong decay (alpha ~ 0.05 per token: some chunks take the exact
+    per-element decay path), moderate decay, and almost no decay, on the
+    dk = dv = 128 bf16 shape."""
+    kda = _kda()
+    x = inputs.prefill_inputs([150, 64], 2, 128, 128, dtype="bf16", num_slots=2, seed=9,
+                              g_mean=g_mean, zero_state=False)
+    out, pool = _run(kda, x, init=True)
+    o_ref, p_ref, _ = oracle.prefill(x.q, x.k, x.v, x.g, x.b, x.cu_seqlens, x.slot_ids, x.pool,
+                                     init_from_pool=True)
+    atol, rtol = tol_for(torch.bfloat16)
+    assert torch.isfinite(out.float()).all()
+    assert_close(to_np64(out), round_to(o_ref, torch.bfloat16), atol, rtol, "outputs")
+    assert_close(to_np64(pool), p_ref, atol, rtol, "states")
+
+
 def _full_size_sampled(T, heads_checked, seed=0):
     kda = _kda()
     H, dk, dv = 32, 128, 128
