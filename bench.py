@@ -226,36 +226,38 @@ def run_decode(args, world, rank, kda, peaks, sampler):
     B, H = w["B"], w["H"]
     stream = torch.cuda.current_stream()
     outs = torch.empty((B, H, w["dv"]), dtype=torch.bfloat16, device="cuda")
+    # one prepared C-ABI call per (input batch, slot set): the timed loop only
+    # launches (no Python marshalling between kernels)
+    calls = {}
+    for bi, bt in enumerate(batches):
+        for si, ss in enumerate(slot_sets):
+            calls[(bi, si)] = kda.decode(bt.q, bt.k, bt.v, bt.g, bt.b, ss, pool, outs,
+                                         stream=stream, _prepare=True)
 
     def step(i):
-        bt = batches[i % len(batches)]
-        kda.decode(bt.q, bt.k, bt.v, bt.g, bt.b, slot_sets[i % len(slot_sets)], pool, outs)
+        calls[(i % len(batches), i % len(slot_sets))]()
 
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     sampler.mark_on()
     t0.record(stream)
     for i in range(args.steps):
-        ev[i][0].record(stream)
         step(args.warmup + i)
-        ev[i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
     sampler.mark_off()
     barrier(world)
     total_ms = t0.elapsed_time(t1)
-    kern_ms = [a.elapsed_time(b) for a, b in ev]
     ms_per_step = max_over_ranks(total_ms / args.steps, world)
     units = B * H
     value = sum_over_ranks(units * args.steps, world) / (ms_per_step * args.steps / 1e3)
-    avg_kernel_s = statistics.mean(kern_ms) / 1e3
+    # one kernel per step: its average duration is the step time
+    avg_kernel_s = total_ms / args.steps / 1e3
     achieved = DECODE_BYTES_PER_TH * units / avg_kernel_s / 1e9
     digest = kernel_source_digest(["kda_decode.cu", "kda_rowmath.cuh"])
     traffic = ncu_traffic("decode_kernel", digest)
@@ -264,7 +266,7 @@ def run_decode(args, world, rank, kda, peaks, sampler):
                 "traffic": traffic, "kernel": "kda::decode_kernel<128,bf16,2>",
                 "algorithmic_bytes_per_launch": DECODE_BYTES_PER_TH * units,
                 "peak_source": f"{peaks['source']} hbm_gbs (copy)",
-                "median_kernel_us": round(statistics.median(kern_ms) * 1e3, 2)}
+                "avg_kernel_us": round(avg_kernel_s * 1e6, 2)}
 
     # e2e: host buffers through the same C ABI entry point
     pinned = {}
@@ -305,26 +307,26 @@ def run_decode(args, world, rank, kda, peaks, sampler):
            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4), "steps": n_e2e}
     del pool
     return dict(value=value, ms_per_step=ms_per_step, roofline=roofline, e2e=e2e,
-                launches=args.steps, kernel_us=statistics.mean(kern_ms) * 1e3)
+                launches=args.steps, kernel_us=avg_kernel_s * 1e6)
 
 
 # --------------------------------------------------------------------------- extra paths
 
 def time_launches(fn, n, warmup=3):
+    """Average microseconds per call of fn(i) over n back-to-back calls,
+    bracketed by one pair of CUDA events on the launching stream."""
     for i in range(warmup):
         fn(i)
     torch.cuda.synchronize()
     s = torch.cuda.current_stream()
-    evs = []
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(s)
     for i in range(n):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(s)
         fn(warmup + i)
-        b.record(s)
-        evs.append((a, b))
+    b.record(s)
     torch.cuda.synchronize()
-    return [a.elapsed_time(b) * 1e3 for a, b in evs]  # microseconds
+    return a.elapsed_time(b) * 1e3 / n
 
 
 def run_spec(kda, peaks):
@@ -339,15 +341,17 @@ def run_spec(kda, peaks):
     rec = kda.alloc_records(B, D, H, dk, dv, torch.bfloat16, "cuda")
     acc = x.num_accepted
     n = 30
-    tv = time_launches(lambda i: kda.verify_record(x.q, x.k, x.v, x.g, x.b, sets[i % len(sets)],
-                                                   x.pool, out, rec), n)
+    vcalls = [kda.verify_record(x.q, x.k, x.v, x.g, x.b, ss, x.pool, out, rec, _prepare=True)
+              for ss in sets]
+    tv = time_launches(lambda i: vcalls[i % len(sets)](), n)
     kda.verify_record(x.q, x.k, x.v, x.g, x.b, x.slot_ids, x.pool, out, rec)
-    tc = time_launches(lambda i: kda.replay_commit(rec, acc, sets[i % len(sets)], x.pool), n)
+    ccalls = [kda.replay_commit(rec, acc, ss, x.pool, _prepare=True) for ss in sets]
+    tc = time_launches(lambda i: ccalls[i % len(sets)](), n)
     a_list = acc.tolist()
     vbytes = B * H * verify_bytes_per_sh(D)
     cbytes = H * sum(commit_bytes_per_sh(a) for a in a_list)
-    vt = statistics.mean(tv) / 1e6
-    ct = statistics.mean(tc) / 1e6
+    vt = tv / 1e6
+    ct = tc / 1e6
     return {
         "workload": "verify_commit_b128_d7_h32_d128_bf16",
         "verify": {"us": round(vt * 1e6, 2), "GB/s": round(vbytes / vt / 1e9, 1),
@@ -367,12 +371,11 @@ def run_prefill(kda, peaks, T=8192, H=32, steps=10, key="prefill_t8192_h32_d128_
     ws_bytes = kda.prefill_workspace_bytes(H, 128, 128, kda.KDA_DT_BF16, 1, T)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
     try:
-        ts = time_launches(lambda i: kda.prefill_chunked(x.q, x.k, x.v, x.g, x.b, x.cu_seqlens,
-                                                         x.slot_ids, x.pool, out, workspace=ws),
-                           steps, warmup=2)
+        call = kda.prefill_chunked(x.q, x.k, x.v, x.g, x.b, x.cu_seqlens, x.slot_ids, x.pool, out,
+                                   workspace=ws, _prepare=True)
+        t = time_launches(lambda i: call(), steps, warmup=2) / 1e6
     except kda.KdaError as e:
         return {"workload": key, "unavailable": str(e)}
-    t = statistics.mean(ts) / 1e6
     bytes_ = T * H * PREFILL_BYTES_PER_TH + H * 128 * 128 * 4
     flops = T * H * PREFILL_FLOP_PER_TH
     t_roof = max(bytes_ / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
@@ -409,8 +412,7 @@ def run_longmix(kda, peaks):
         for t in range(256):
             kda.decode(x.q[t], x.k[t], x.v[t], x.g[t], x.b[t], slots, pool, out[t], stream=s)
     ts = time_launches(lambda i: graph.replay(), 5, warmup=2)
-    res["decode_256_steps_b1_h32"] = {"us_per_step": round(statistics.mean(ts) / 256, 3),
-                                      "graph": True}
+    res["decode_256_steps_b1_h32"] = {"us_per_step": round(ts / 256, 3), "graph": True}
     del pool, x, out, graph
     # 1024 x 64 heads over a 16384-slot pool (64 GiB)
     B2, H2, NS2 = 1024, 64, 16384
@@ -425,9 +427,9 @@ def run_longmix(kda, peaks):
     perm = torch.randperm(NS2, generator=gen, device="cuda").to(torch.int32)
     sets = [perm[i * B2:(i + 1) * B2].contiguous() for i in range(NS2 // B2)]
     out2 = torch.empty((B2, H2, 128), dtype=torch.bfloat16, device="cuda")
-    ts = time_launches(lambda i: kda.decode(big.q, big.k, big.v, big.g, big.b, sets[i % len(sets)],
-                                            big.pool, out2), 10)
-    t = statistics.mean(ts) / 1e6
+    dcalls = [kda.decode(big.q, big.k, big.v, big.g, big.b, ss, big.pool, out2, _prepare=True)
+              for ss in sets]
+    t = time_launches(lambda i: dcalls[i % len(sets)](), 10) / 1e6
     bytes_ = B2 * H2 * DECODE_BYTES_PER_TH
     res["decode_b1024_h64"] = {"us": round(t * 1e6, 1), "token_heads_per_s": round(B2 * H2 / t, 1),
                                "GB/s": round(bytes_ / t / 1e9, 1),

@@ -587,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
 }  // namespace prefill_tc
 
 #ifndef KDA_PREFILL_TC
-#define KDA_PREFILL_TC 0
+#define KDA_PREFILL_TC 1
 #endif
 
 bool prefill_tc_supported(int dk, int dv, int dtype) {

@@ -134,8 +134,22 @@ def _need(t: torch.Tensor, name: str, shape, dtype=None):
         raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
 
 
+class _Prepared:
+    """A C-ABI call with its arguments already marshalled; calling it launches
+    again on the same buffers (used to time launches without Python overhead)."""
+
+    def __init__(self, fn, args, name, keep, result):
+        self._fn, self._args, self._name = fn, args, name
+        self._keep = keep          # ctypes structs the arguments point to
+        self.result = result
+
+    def __call__(self):
+        _check(self._fn(*self._args), self._name)
+        return self.result
+
+
 def decode(q, k, v, g, b, slot_ids, pool, out=None, *, eps=1e-6, scale=None,
-           err_flag=None, stream=None):
+           err_flag=None, stream=None, _prepare=False):
     """One fused decode token per sequence, in place on ``pool``.
 
     q, k: [B, H, dk]; v: [B, H, dv]; g: [B, H, dk] fp32; b: [B, H];
@@ -153,10 +167,11 @@ def decode(q, k, v, g, b, slot_ids, pool, out=None, *, eps=1e-6, scale=None,
         out = torch.empty((B, H, dv), dtype=dt, device=q.device)
     _need(out, "out", (B, H, dv), dt)
     dims = make_dims(H, dk, dv, _dtype_code(q), eps, scale)
-    st = _lib.kda_decode(ctypes.byref(dims), B, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
-                         _ptr(b), _ptr(slot_ids), _ptr(pool), pool.shape[0], _ptr(out),
-                         _ptr(err_flag), _stream_handle(stream))
-    _check(st, "kda_decode")
+    args = (ctypes.byref(dims), B, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(slot_ids),
+            _ptr(pool), pool.shape[0], _ptr(out), _ptr(err_flag), _stream_handle(stream))
+    if _prepare:
+        return _Prepared(_lib.kda_decode, args, "kda_decode", (dims,), out)
+    _check(_lib.kda_decode(*args), "kda_decode")
     return out
 
 
@@ -175,7 +190,7 @@ def _records_struct(rec) -> KdaRecords:
 
 
 def verify_record(q, k, v, g, b, slot_ids, pool, out=None, records=None, *,
-                  eps=1e-6, scale=None, err_flag=None, stream=None):
+                  eps=1e-6, scale=None, err_flag=None, stream=None, _prepare=False):
     """ReplaySSM verify of D draft tokens; pool is read only.
 
     q, k: [B, D, H, dk]; v: [B, D, H, dv]; g fp32; b: [B, D, H].
@@ -197,16 +212,18 @@ def verify_record(q, k, v, g, b, slot_ids, pool, out=None, records=None, *,
         records = alloc_records(B, D, H, dk, dv, dt, q.device)
     rs = _records_struct(records)
     dims = make_dims(H, dk, dv, _dtype_code(q), eps, scale)
-    st = _lib.kda_verify_record(ctypes.byref(dims), B, D, _ptr(q), _ptr(k), _ptr(v),
-                                _ptr(g), _ptr(b), _ptr(slot_ids), _ptr(pool),
-                                pool.shape[0], _ptr(out), ctypes.byref(rs),
-                                _ptr(err_flag), _stream_handle(stream))
-    _check(st, "kda_verify_record")
+    args = (ctypes.byref(dims), B, D, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b),
+            _ptr(slot_ids), _ptr(pool), pool.shape[0], _ptr(out), ctypes.byref(rs),
+            _ptr(err_flag), _stream_handle(stream))
+    if _prepare:
+        return _Prepared(_lib.kda_verify_record, args, "kda_verify_record", (dims, rs),
+                         (out, records))
+    _check(_lib.kda_verify_record(*args), "kda_verify_record")
     return out, records
 
 
 def replay_commit(records, num_accepted, slot_ids, pool, *, err_flag=None,
-                  stream=None):
+                  stream=None, _prepare=False):
     """Replay the accepted prefix of each sequence's records onto ``pool``."""
     B, D, H, dk = records["k_hat"].shape
     dv = records["v"].shape[3]
@@ -216,11 +233,12 @@ def replay_commit(records, num_accepted, slot_ids, pool, *, err_flag=None,
     _need(pool, "pool", (pool.shape[0], H, dv, dk), torch.float32)
     rs = _records_struct(records)
     dims = make_dims(H, dk, dv, _dtype_code(records["v"]))
-    st = _lib.kda_replay_commit(ctypes.byref(dims), B, D, ctypes.byref(rs),
-                                _ptr(num_accepted), _ptr(slot_ids), _ptr(pool),
-                                pool.shape[0], _ptr(err_flag), _stream_handle(stream))
-    _check(st, "kda_replay_commit")
+    args = (ctypes.byref(dims), B, D, ctypes.byref(rs), _ptr(num_accepted), _ptr(slot_ids),
+            _ptr(pool), pool.shape[0], _ptr(err_flag), _stream_handle(stream))
     del dt
+    if _prepare:
+        return _Prepared(_lib.kda_replay_commit, args, "kda_replay_commit", (dims, rs), None)
+    _check(_lib.kda_replay_commit(*args), "kda_replay_commit")
 
 
 def prefill_workspace_bytes(H, dk, dv, dtype_code, num_seqs, total_tokens) -> int:
@@ -231,7 +249,7 @@ def prefill_workspace_bytes(H, dk, dv, dtype_code, num_seqs, total_tokens) -> in
 
 def prefill_chunked(q, k, v, g, b, cu_seqlens, slot_ids, pool, out=None, *,
                     init_from_pool=False, workspace=None, eps=1e-6, scale=None,
-                    err_flag=None, stream=None):
+                    err_flag=None, stream=None, _prepare=False):
     """Chunked prefill of a packed variable-length batch.
 
     q, k: [T, H, dk]; v: [T, H, dv]; g: [T, H, dk] fp32; b: [T, H];
@@ -257,10 +275,11 @@ def prefill_chunked(q, k, v, g, b, cu_seqlens, slot_ids, pool, out=None, *,
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     dims = make_dims(H, dk, dv, code, eps, scale)
-    st = _lib.kda_prefill_chunked(ctypes.byref(dims), n, _ptr(cu_seqlens), T, _ptr(q),
-                                  _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(slot_ids),
-                                  _ptr(pool), pool.shape[0], 1 if init_from_pool else 0,
-                                  _ptr(out), _ptr(workspace), ws_bytes, _ptr(err_flag),
-                                  _stream_handle(stream))
-    _check(st, "kda_prefill_chunked")
+    args = (ctypes.byref(dims), n, _ptr(cu_seqlens), T, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+            _ptr(b), _ptr(slot_ids), _ptr(pool), pool.shape[0], 1 if init_from_pool else 0,
+            _ptr(out), _ptr(workspace), ws_bytes, _ptr(err_flag), _stream_handle(stream))
+    if _prepare:
+        return _Prepared(_lib.kda_prefill_chunked, args, "kda_prefill_chunked",
+                         (dims, workspace), out)
+    _check(_lib.kda_prefill_chunked(*args), "kda_prefill_chunked")
     return out
