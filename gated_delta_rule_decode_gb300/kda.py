@@ -30,7 +30,8 @@ KDA_DEVERR_TIMEOUT = 8
 
 EXPORTED = ("kda_decode", "kda_verify_record", "kda_replay_commit",
             "kda_prefill_chunked", "kda_prefill_workspace_bytes",
-            "kda_records_bytes", "kda_status_string", "kda_abi_version")
+            "kda_records_bytes", "kda_status_string", "kda_abi_version",
+            "kda_prefill_chunked_static", "kda_static_scratch_bytes")
 
 
 class KdaError(RuntimeError):
@@ -74,6 +75,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kda_prefill_chunked.argtypes = [_PD, _I32, _VP, _I64, _VP, _VP, _VP,
                                         _VP, _VP, _VP, _VP, _I64, _I32, _VP,
                                         _VP, _SZ, _VP, _VP]
+    lib.kda_prefill_chunked_static.argtypes = [_PD, _I32, _VP, _I64, _VP, _VP, _VP, _VP,
+                                               _VP, _VP, _VP, _I64, _I32, _VP, _VP, _VP]
+    lib.kda_prefill_chunked_static.restype = ctypes.c_int
+    lib.kda_static_scratch_bytes.argtypes = []
+    lib.kda_static_scratch_bytes.restype = _SZ
     lib.kda_prefill_workspace_bytes.argtypes = [_PD, _I32, _I64]
     lib.kda_prefill_workspace_bytes.restype = _SZ
     lib.kda_records_bytes.argtypes = [_PD, _I32, _I32]

@@ -213,6 +213,45 @@ KDA_API int kda_prefill_chunked(const kda_dims *dims, int32_t num_seqs,
                         void *workspace, size_t workspace_bytes,
                         int32_t *err_flag, void *stream);
 
+/*
+ * kda_prefill_chunked_static: kda_prefill_chunked without a caller-provided
+ * workspace, for callers that cannot allocate device memory at the point of
+ * the call: code that runs while a CUDA graph is being captured (where
+ * cudaMalloc is not allowed), serving engines whose device memory is planned
+ * up front and owned by another allocator, and plug-in hosts that hand the
+ * library only its inputs and outputs.  (The source pages have no
+ * counterpart; this is an interface convenience of this library.)
+ *
+ * The scratch is a fixed device array inside the library of
+ * KDA_STATIC_SCRATCH_BYTES bytes, reserved on every GPU that loads the
+ * library until the process exits.  Arguments and results are exactly those
+ * of kda_prefill_chunked, minus workspace/workspace_bytes.
+ *   - Returns KDA_ERR_WORKSPACE, launching nothing, when
+ *     kda_prefill_workspace_bytes(dims, num_seqs, total_tokens) exceeds
+ *     KDA_STATIC_SCRATCH_BYTES (about 440 (chunk, head) pairs at
+ *     dk = dv = 128 bf16; split larger batches into several calls).
+ *   - Calls no allocating routine (no cudaMalloc/cudaFree).
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress); make that first call before any stream
+ *     capture.  It returns KDA_ERR_CUDA if the lookup fails.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's bytes; nothing in it needs to start at zero.  Calls that overlap
+ *     on the GPU (different streams, or different host threads) race on it:
+ *     order them, or use kda_prefill_chunked with separate workspaces.
+ */
+#define KDA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+
+KDA_API int kda_prefill_chunked_static(const kda_dims *dims, int32_t num_seqs,
+                                       const int32_t *cu_seqlens, int64_t total_tokens,
+                                       const void *q, const void *k, const void *v,
+                                       const float *g, const void *b,
+                                       const int32_t *slot_ids, float *pool,
+                                       int64_t num_slots, int32_t init_from_pool,
+                                       void *out, int32_t *err_flag, void *stream);
+
+/* KDA_STATIC_SCRATCH_BYTES of the built library. */
+KDA_API size_t kda_static_scratch_bytes(void);
+
 /* Workspace bytes kda_prefill_chunked needs for this shape (0 on bad dims). */
 KDA_API size_t kda_prefill_workspace_bytes(const kda_dims *dims, int32_t num_seqs,
                                    int64_t total_tokens);
