@@ -97,25 +97,37 @@ __device__ inline int find_seq(const int32_t *plan, int n, int32_t c) {
 
 // ================================================================== prep
 
-// TMEM columns of the prep kernel.
-constexpr int PT_BKT = 0, PT_BVT = 64, PT_G = 128, PT_WT = 192, PT_UPT = 256;
-constexpr uint32_t PT_COLS = 512;
+// TMEM columns of the prep kernel (256 per CTA, so two CTAs share an SM):
+// W^T is written over G once G has been read.
+constexpr int PT_BKT = 0, PT_BVT = 64, PT_G = 128, PT_WT = 128, PT_UPT = 192;
+constexpr uint32_t PT_COLS = 256;
 
-struct PrepSmem {
-    unsigned char bufKQ[128 * 128 * 4];  // [K+; Q+]  (A of the A/P product)
-    unsigned char bufKM[64 * 128 * 4];   // K-        (B of the A/P product)
-    unsigned char bufT[64 * 64 * 4];     // T         (B of the WY products)
+// Scratch of the UT inverse, laid over the [K+; Q+] tile once the A/P
+// product that reads it has completed.
+struct InvScratch {
     float As[C][C + 1];
     float Ts[C][C + 1];
     float Xs[3][16][17];
+};
+
+struct PrepSmem {
+    union {
+        unsigned char bufKQ[128 * 128 * 4];  // [K+; Q+]  (A of the A/P product)
+        InvScratch inv;
+    };
+    union {
+        unsigned char bufKM[64 * 128 * 4];   // K-        (B of the A/P product)
+        unsigned char bufT[64 * 64 * 4];     // T         (B of the WY products)
+    };
     float invk[C], invq[C], beta[C];
     uint64_t bar;
     uint32_t tmem_base;
 };
 constexpr size_t kPrepSmem = sizeof(PrepSmem) + 1024;
+static_assert(sizeof(InvScratch) <= 128 * 128 * 4, "inverse scratch must fit the [K+; Q+] tile");
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParams p) {
     extern __shared__ unsigned char smem_raw[];
     PrepSmem &sm =
         *reinterpret_cast<PrepSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -271,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const PrefillParam
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
                         const int j = j0 + jj;
-                        sm.As[r][j] = (j < r) ? sm.beta[r] * g16[jj] : 0.f;
+                        sm.inv.As[r][j] = (j < r) ? sm.beta[r] * g16[jj] : 0.f;
                     }
                 } else {
 #pragma unroll
@@ -285,10 +297,14 @@ __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const PrefillParam
             }
         }
     } else {
+        // exact path; A goes to registers first because its scratch overlays k^
         const float *kh = reinterpret_cast<const float *>(sm.bufKQ);
         const float *qh = kh + C * D;
         const float *gm = reinterpret_cast<const float *>(sm.bufKM);
-        for (int idx = tid; idx < C * C; idx += kThreads) {
+        float areg[C * C / kThreads];
+#pragma unroll 1
+        for (int it = 0; it < C * C / kThreads; ++it) {
+            const int idx = tid + it * kThreads;
             const int r = idx / C, j = idx % C;
             float a = 0.f, pp = 0.f;
             if (j <= r) {
@@ -298,8 +314,14 @@ __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const PrefillParam
                     pp = fmaf(qh[r * D + cc], m, pp);
                 }
             }
-            sm.As[r][j] = (j < r) ? sm.beta[r] * a : 0.f;
+            areg[it] = (j < r) ? sm.beta[r] * a : 0.f;
             *reinterpret_cast<float *>(img + IMG_P + tc::sw128_off(r, j, 64)) = (j <= r) ? pp : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int it = 0; it < C * C / kThreads; ++it) {
+            const int idx = tid + it * kThreads;
+            sm.inv.As[idx / C][idx % C] = areg[it];
         }
     }
     __syncthreads();
@@ -307,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const PrefillParam
     if (ok) {
         // ---- 2c. T = (I + A)^-1: diagonal 16x16 blocks by forward
         // substitution, then T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ by distance
-        for (int idx = tid; idx < C * (C + 1); idx += kThreads) (&sm.Ts[0][0])[idx] = 0.f;
+        for (int idx = tid; idx < C * (C + 1); idx += kThreads) (&sm.inv.Ts[0][0])[idx] = 0.f;
         __syncthreads();
         if (tid < 64) {
             const int I = tid >> 4, j = tid & 15, o = 16 * I;
@@ -317,11 +339,11 @@ __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const PrefillParam
                 float acc = (r == j) ? 1.f : 0.f;
 #pragma unroll
                 for (int m = 0; m < 16; ++m)
-                    if (m < r && m >= j) acc = fmaf(-sm.As[o + r][o + m], col[m], acc);
+                    if (m < r && m >= j) acc = fmaf(-sm.inv.As[o + r][o + m], col[m], acc);
                 col[r] = (r >= j) ? acc : 0.f;
             }
 #pragma unroll
-            for (int r = 0; r < 16; ++r) sm.Ts[o + r][o + j] = col[r];
+            for (int r = 0; r < 16; ++r) sm.inv.Ts[o + r][o + j] = col[r];
         }
         __syncthreads();
         for (int dist = 1; dist < 4; ++dist) {
@@ -333,8 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const PrefillParam
                 for (int K = J; K < I; ++K)
 #pragma unroll
                     for (int kk = 0; kk < 16; ++kk)
-                        x = fmaf(sm.As[16 * I + r][16 * K + kk], sm.Ts[16 * K + kk][16 * J + j], x);
-                sm.Xs[bi][r][j] = x;
+                        x = fmaf(sm.inv.As[16 * I + r][16 * K + kk], sm.inv.Ts[16 * K + kk][16 * J + j], x);
+                sm.inv.Xs[bi][r][j] = x;
             }
             __syncthreads();
             for (int idx = tid; idx < nb * 256; idx += kThreads) {
@@ -343,15 +365,15 @@ __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const PrefillParam
                 float t = 0.f;
 #pragma unroll
                 for (int m = 0; m < 16; ++m)
-                    if (m <= r) t = fmaf(sm.Ts[16 * I + r][16 * I + m], sm.Xs[bi][m][j], t);
-                sm.Ts[16 * I + r][16 * J + j] = -t;
+                    if (m <= r) t = fmaf(sm.inv.Ts[16 * I + r][16 * I + m], sm.inv.Xs[bi][m][j], t);
+                sm.inv.Ts[16 * I + r][16 * J + j] = -t;
             }
             __syncthreads();
         }
         for (int idx = tid; idx < C * C / 4; idx += kThreads) {
             const int r = idx / (C / 4), j = (idx % (C / 4)) * 4;
             *reinterpret_cast<float4 *>(sm.bufT + tc::sw128_off(r, j, 64)) =
-                make_float4(sm.Ts[r][j], sm.Ts[r][j + 1], sm.Ts[r][j + 2], sm.Ts[r][j + 3]);
+                make_float4(sm.inv.Ts[r][j], sm.inv.Ts[r][j + 1], sm.inv.Ts[r][j + 2], sm.inv.Ts[r][j + 3]);
         }
         sync_for_mma();
 
@@ -465,6 +487,18 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
 
     uint32_t mphase = 0;
     bool ok = true;
+    // this thread's row of U'^T (value row i = tid): the next chunk's row is
+    // loaded into registers while the current chunk computes
+    float upt[C];
+    auto load_upt = [&](int ci, float (&dst)[C]) {
+        const float4 *src = reinterpret_cast<const float4 *>(image(ci) + IMG_UPT) + (size_t)tid * (C / 4);
+#pragma unroll
+        for (int j = 0; j < C / 4; ++j) {
+            const float4 x = __ldg(src + j);
+            dst[4 * j] = x.x; dst[4 * j + 1] = x.y; dst[4 * j + 2] = x.z; dst[4 * j + 3] = x.w;
+        }
+    };
+    if (nchunks > 0) load_upt(0, upt);
     for (int ci = 0; ci < nchunks; ++ci) {
         const int st = ci & 1;
         const int64_t t0 = (int64_t)cs + (int64_t)ci * C;
@@ -476,16 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
             bulk_g2s(sm.stage[st ^ 1], image(ci + 1), IMG_TILES, &sm.full[st ^ 1]);
             bulk_g2s(sm.egc[st ^ 1], image(ci + 1) + IMG_EGC, D * 4, &sm.full[st ^ 1]);
         }
-        // this thread's row of U'^T (value row i = tid), in flight during MMA 1
-        float upt[C];
-        {
-            const float4 *src = reinterpret_cast<const float4 *>(image(ci) + IMG_UPT) + (size_t)tid * (C / 4);
-#pragma unroll
-            for (int j = 0; j < C / 4; ++j) {
-                const float4 x = __ldg(src + j);
-                upt[4 * j] = x.x; upt[4 * j + 1] = x.y; upt[4 * j + 2] = x.z; upt[4 * j + 3] = x.w;
-            }
-        }
+        float upn[C];
+        if (ci + 1 < nchunks) load_upt(ci + 1, upn);
         const bool landed = mbar_wait(&sm.full[st], (ci >> 1) & 1);
         if (__syncthreads_and(landed) == 0) {
             if (tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
@@ -555,6 +581,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
                     if (r0 + rr < L) Elem<T>::store1(out + (t0 + r0 + rr) * tok_stride + hoff + tid, scale * o16[rr]);
             }
         }
+#pragma unroll
+        for (int j = 0; j < C; ++j) upt[j] = upn[j];
         fence_proxy_async_smem();  // this stage's e^{gamma_C} reads before its next bulk refill
         tc::fence_before_sync();
         __syncthreads();
