@@ -143,13 +143,14 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
     const int64_t t0 = (int64_t)p.cu_seqlens[s] + (int64_t)(chunk - plan[s]) * C;
     const int L = (int)((int64_t)p.cu_seqlens[s + 1] - t0 < C ? (int64_t)p.cu_seqlens[s + 1] - t0 : C);
     const int tid = threadIdx.x, warp = tid >> 5;
-    const T *q = static_cast<const T *>(p.q);
-    const T *k = static_cast<const T *>(p.k);
-    const T *v = static_cast<const T *>(p.v);
-    const T *bb = static_cast<const T *>(p.b);
+    const T *__restrict__ q = static_cast<const T *>(p.q);
+    const T *__restrict__ k = static_cast<const T *>(p.k);
+    const T *__restrict__ v = static_cast<const T *>(p.v);
+    const T *__restrict__ bb = static_cast<const T *>(p.b);
+    const float *__restrict__ gptr = p.g;
     const int64_t tok_stride = (int64_t)H * D, hoff = (int64_t)h * D;
-    unsigned char *img = static_cast<unsigned char *>(p.workspace) + plan_bytes(n) +
-                         ((size_t)chunk * H + h) * (size_t)IMG_BYTES;
+    unsigned char *__restrict__ img = static_cast<unsigned char *>(p.workspace) + plan_bytes(n) +
+                                      ((size_t)chunk * H + h) * (size_t)IMG_BYTES;
 
     if (warp == 0) tc::tmem_alloc(&sm.tmem_base, PT_COLS);
     if (tid == 0) {
@@ -195,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
         float acc = 0.f;
 #pragma unroll
         for (int r = 0; r < C; ++r) {
-            if (r < L) acc += __ldg(p.g + (t0 + r) * tok_stride + hoff + c);
+            if (r < L) acc += __ldg(gptr + (t0 + r) * tok_stride + hoff + c);
             gam[r] = acc;
         }
     }
@@ -214,13 +215,24 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
         const float egcref = expf(gC - ref);
         float bkt[16], bvt[16];
         float kt4[4];
+        // 16 tokens at a time: all their loads are issued before any use
+        float kb[16], qb[16], vb[16];
 #pragma unroll
         for (int r = 0; r < C; ++r) {
+            if ((r & 15) == 0) {
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) {
+                    const bool ok_r = r + rr < L;
+                    const int64_t off = (t0 + r + rr) * tok_stride + hoff + c;
+                    kb[rr] = ok_r ? Elem<T>::load1(k + off) : 0.f;
+                    qb[rr] = ok_r ? Elem<T>::load1(q + off) : 0.f;
+                    vb[rr] = ok_r ? Elem<T>::load1(v + off) : 0.f;
+                }
+            }
             const bool valid = r < L;
-            const int64_t off = (t0 + r) * tok_stride + hoff + c;
-            const float kx = valid ? Elem<T>::load1(k + off) * sm.invk[r] : 0.f;
-            const float qx = valid ? Elem<T>::load1(q + off) * sm.invq[r] : 0.f;
-            const float vx = valid ? Elem<T>::load1(v + off) : 0.f;
+            const float kx = kb[r & 15] * sm.invk[r];
+            const float qx = qb[r & 15] * sm.invq[r];
+            const float vx = vb[r & 15];
             float ktil, qtil, khat_end;
             if (!unsafe) {
                 const float E = __expf(gam[r] - ref);
@@ -532,24 +544,30 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
         }
         ok = wait_mma(&sm.mma, mphase, p.err_flag);
         if (!ok) break;
-        // U^T = U'^T - S W^T;  S <- S diag(e^{gamma_C})
+        // U^T = U'^T - S W^T;  S <- S diag(e^{gamma_C})  (loads batched
+        // behind one wait per 64 columns)
         {
-            float a16[16];
+            float a[4][16];
 #pragma unroll
-            for (int r0 = 0; r0 < C; r0 += 16) {
-                tc::ld16(tc::lane_addr(tm, warp, CT_D1 + r0), a16);
-                tc::wait_ld();
+            for (int q4 = 0; q4 < 4; ++q4) tc::ld16(tc::lane_addr(tm, warp, CT_D1 + 16 * q4), a[q4]);
+            tc::wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) a16[j] = upt[r0 + j] - a16[j];
-                tc::st16(tc::lane_addr(tm, warp, CT_UT + r0), a16);
+            for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) a[q4][j] = upt[16 * q4 + j] - a[q4][j];
+                tc::st16(tc::lane_addr(tm, warp, CT_UT + 16 * q4), a[q4]);
             }
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 16) {
-                tc::ld16(tc::lane_addr(tm, warp, CT_S + c0), a16);
+            for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) tc::ld16(tc::lane_addr(tm, warp, CT_S + 64 * half + 16 * q4), a[q4]);
                 tc::wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) a16[j] *= sm.egc[st][c0 + j];
-                tc::st16(tc::lane_addr(tm, warp, CT_S + c0), a16);
+                for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) a[q4][j] *= sm.egc[st][64 * half + 16 * q4 + j];
+                    tc::st16(tc::lane_addr(tm, warp, CT_S + 64 * half + 16 * q4), a[q4]);
+                }
             }
             tc::wait_st();
         }
@@ -570,16 +588,17 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
         ok = wait_mma(&sm.mma, mphase, p.err_flag);
         if (!ok) break;
         {
-            float o16[16];
+            float o[4][16];
             const float scale = p.scale;
 #pragma unroll
-            for (int r0 = 0; r0 < C; r0 += 16) {
-                tc::ld16(tc::lane_addr(tm, warp, CT_D1 + 64 + r0), o16);
-                tc::wait_ld();
+            for (int q4 = 0; q4 < 4; ++q4) tc::ld16(tc::lane_addr(tm, warp, CT_D1 + 64 + 16 * q4), o[q4]);
+            tc::wait_ld();
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
                 for (int rr = 0; rr < 16; ++rr)
-                    if (r0 + rr < L) Elem<T>::store1(out + (t0 + r0 + rr) * tok_stride + hoff + tid, scale * o16[rr]);
-            }
+                    if (16 * q4 + rr < L)
+                        Elem<T>::store1(out + (t0 + 16 * q4 + rr) * tok_stride + hoff + tid, scale * o[q4][rr]);
         }
 #pragma unroll
         for (int j = 0; j < C; ++j) upt[j] = upn[j];
