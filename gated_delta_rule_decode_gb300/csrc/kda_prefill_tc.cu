@@ -107,7 +107,6 @@ constexpr uint32_t PT_COLS = 256;
 struct InvScratch {
     float As[C][C + 1];
     float Ts[C][C + 1];
-    float Xs[3][16][17];
 };
 
 struct PrepSmem {
@@ -120,6 +119,7 @@ struct PrepSmem {
         unsigned char bufT[64 * 64 * 4];     // T         (B of the WY products)
     };
     float invk[C], invq[C], beta[C];
+    float xs[3][16][17];  // off-diagonal partial products of the UT inverse
     uint64_t bar;
     uint32_t tmem_base;
 };
@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
         if (r < L) {
             const T *row = (isq ? q : k) + (t0 + r) * tok_stride + hoff;
             float ss = 0.f;
-#pragma unroll 8
+#pragma unroll 4
             for (int j = 0; j < D; j += 4) {
                 const float4 x = Elem<T>::load4(row + j);
                 ss = fmaf(x.x, x.x, ss);
@@ -190,81 +190,80 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
     uint32_t phase = 0;
 
     // ---- 1b. thread = key channel c (and value row i = c)
+    // pass 1 over the gates: ref = gamma at token 31, gamma_C, and the range
+    // of gamma (rows past the chunk's end repeat gamma_C)
     const int c = tid;
-    float gam[C];
+    // (compact loops: every CTA runs this code once, so code size, not
+    // unrolling, decides its speed)
+    float ref = 0.f, gC = 0.f, gmin = 0.f, gmax = 0.f;
     {
         float acc = 0.f;
-#pragma unroll
+#pragma unroll 8
         for (int r = 0; r < C; ++r) {
-            if (r < L) acc += __ldg(gptr + (t0 + r) * tok_stride + hoff + c);
-            gam[r] = acc;
+            acc += (r < L) ? __ldg(gptr + (t0 + r) * tok_stride + hoff + c) : 0.f;
+            if (r == 31) ref = acc;
+            if (r == L - 1) gC = acc;
+            gmin = r == 0 ? acc : fminf(gmin, acc);
+            gmax = r == 0 ? acc : fmaxf(gmax, acc);
         }
     }
-    float gC = gam[0];
-#pragma unroll
-    for (int r = 1; r < C; ++r)
-        if (r == L - 1) gC = gam[r];
-    const float ref = gam[31];
-    float span = 0.f;
-#pragma unroll
-    for (int r = 0; r < C; ++r) span = fmaxf(span, fabsf(gam[r] - ref));
+    const float span = fmaxf(gmax - ref, ref - gmin);
     reinterpret_cast<float *>(img + IMG_EGC)[c] = expf(gC);
     const bool unsafe = __syncthreads_or(span > kSpanLimit) != 0;
+    // pass 2: 16 tokens at a time, all of their loads issued before any use
     {
         const float eref = expf(ref);
         const float egcref = expf(gC - ref);
-        float bkt[16], bvt[16];
-        float kt4[4];
-        // 16 tokens at a time: all their loads are issued before any use
-        float kb[16], qb[16], vb[16];
+        float acc = 0.f;
+#pragma unroll 1
+        for (int r0 = 0; r0 < C; r0 += 16) {
+            float kb[16], qb[16], vb[16], gb[16];
 #pragma unroll
-        for (int r = 0; r < C; ++r) {
-            if ((r & 15) == 0) {
+            for (int rr = 0; rr < 16; ++rr) {
+                const bool ok_r = r0 + rr < L;
+                const int64_t off = (t0 + r0 + rr) * tok_stride + hoff + c;
+                kb[rr] = ok_r ? Elem<T>::load1(k + off) : 0.f;
+                qb[rr] = ok_r ? Elem<T>::load1(q + off) : 0.f;
+                vb[rr] = ok_r ? Elem<T>::load1(v + off) : 0.f;
+                gb[rr] = ok_r ? __ldg(gptr + off) : 0.f;
+            }
+            float bkt[16], bvt[16];
 #pragma unroll
-                for (int rr = 0; rr < 16; ++rr) {
-                    const bool ok_r = r + rr < L;
-                    const int64_t off = (t0 + r + rr) * tok_stride + hoff + c;
-                    kb[rr] = ok_r ? Elem<T>::load1(k + off) : 0.f;
-                    qb[rr] = ok_r ? Elem<T>::load1(q + off) : 0.f;
-                    vb[rr] = ok_r ? Elem<T>::load1(v + off) : 0.f;
+            for (int rr = 0; rr < 16; ++rr) {
+                const int r = r0 + rr;
+                const bool valid = r < L;
+                acc += gb[rr];
+                const float gam = acc;
+                const float kx = kb[rr] * sm.invk[r];
+                const float qx = qb[rr] * sm.invq[r];
+                float ktil, qtil, khat_end;
+                if (!unsafe) {
+                    const float E = __expf(gam - ref);
+                    const float Ei = __expf(ref - gam);
+                    const float kp = kx * E, qp = qx * E;
+                    st_sw(sm.bufKQ, 128, r, c, kp);
+                    st_sw(sm.bufKQ, 128, 64 + r, c, qp);
+                    st_sw(sm.bufKM, 64, r, c, kx * Ei);
+                    ktil = kp * eref;
+                    qtil = qp * eref;
+                    khat_end = kx * Ei * egcref;
+                } else {
+                    // plain [64][128] copies of k^, q^ and gamma for the exact path
+                    reinterpret_cast<float *>(sm.bufKQ)[r * D + c] = kx;
+                    reinterpret_cast<float *>(sm.bufKQ)[C * D + r * D + c] = qx;
+                    reinterpret_cast<float *>(sm.bufKM)[r * D + c] = gam;
+                    const float eg = expf(gam);
+                    ktil = kx * eg;
+                    qtil = qx * eg;
+                    khat_end = kx * expf(gC - gam);
                 }
+                st_sw(img + IMG_BW, 128, 64 + r, c, qtil);  // Q~ rows of [W; Q~]
+                st_sw(img + IMG_KT, 128, c, r, valid ? khat_end : 0.f);
+                bkt[rr] = sm.beta[r] * ktil;
+                bvt[rr] = sm.beta[r] * vb[rr];
             }
-            const bool valid = r < L;
-            const float kx = kb[r & 15] * sm.invk[r];
-            const float qx = qb[r & 15] * sm.invq[r];
-            const float vx = vb[r & 15];
-            float ktil, qtil, khat_end;
-            if (!unsafe) {
-                const float E = __expf(gam[r] - ref);
-                const float Ei = __expf(ref - gam[r]);
-                const float kp = kx * E, qp = qx * E;
-                st_sw(sm.bufKQ, 128, r, c, kp);
-                st_sw(sm.bufKQ, 128, 64 + r, c, qp);
-                st_sw(sm.bufKM, 64, r, c, kx * Ei);
-                ktil = kp * eref;
-                qtil = qp * eref;
-                khat_end = kx * Ei * egcref;
-            } else {
-                // plain [64][128] copies of k^, q^ and gamma for the exact path
-                reinterpret_cast<float *>(sm.bufKQ)[r * D + c] = kx;
-                reinterpret_cast<float *>(sm.bufKQ)[C * D + r * D + c] = qx;
-                reinterpret_cast<float *>(sm.bufKM)[r * D + c] = gam[r];
-                const float eg = expf(gam[r]);
-                ktil = kx * eg;
-                qtil = qx * eg;
-                khat_end = kx * expf(gC - gam[r]);
-            }
-            st_sw(img + IMG_BW, 128, 64 + r, c, qtil);  // Q~ rows of [W; Q~]
-            kt4[r & 3] = valid ? khat_end : 0.f;
-            if ((r & 3) == 3)
-                *reinterpret_cast<float4 *>(img + IMG_KT + tc::sw128_off(c, r - 3, 128)) =
-                    make_float4(kt4[0], kt4[1], kt4[2], kt4[3]);
-            bkt[r & 15] = sm.beta[r] * ktil;
-            bvt[r & 15] = sm.beta[r] * vx;
-            if ((r & 15) == 15) {
-                tc::st16(tc::lane_addr(tm, warp, PT_BKT + (r - 15)), bkt);
-                tc::st16(tc::lane_addr(tm, warp, PT_BVT + (r - 15)), bvt);
-            }
+            tc::st16(tc::lane_addr(tm, warp, PT_BKT + r0), bkt);
+            tc::st16(tc::lane_addr(tm, warp, PT_BVT + r0), bvt);
         }
     }
     tc::wait_st();
@@ -339,46 +338,57 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
     __syncthreads();
 
     if (ok) {
-        // ---- 2c. T = (I + A)^-1: diagonal 16x16 blocks by forward
-        // substitution, then T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ by distance
-        for (int idx = tid; idx < C * (C + 1); idx += kThreads) (&sm.inv.Ts[0][0])[idx] = 0.f;
-        __syncthreads();
-        if (tid < 64) {
-            const int I = tid >> 4, j = tid & 15, o = 16 * I;
+        // ---- 2c. T = (I + A)^-1 (unit lower triangular), blocked by 16:
+        // the four diagonal blocks by forward substitution (one column per
+        // thread, in registers), then the blocks below the diagonal in order of
+        // distance d: X = sum_{K=J}^{I-1} A_IK T_KJ, T_IJ = -T_II X.
+        if (tid < C) {
+            const int I = tid >> 4, jj = tid & 15, o = 16 * I;
             float col[16];
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
-                float acc = (r == j) ? 1.f : 0.f;
+                float acc = (r == jj) ? 1.f : 0.f;
 #pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    if (m < r && m >= j) acc = fmaf(-sm.inv.As[o + r][o + m], col[m], acc);
-                col[r] = (r >= j) ? acc : 0.f;
+                for (int m = 0; m < r; ++m)
+                    if (m >= jj) acc = fmaf(-sm.inv.As[o + r][o + m], col[m], acc);
+                col[r] = (r >= jj) ? acc : 0.f;
             }
 #pragma unroll
-            for (int r = 0; r < 16; ++r) sm.inv.Ts[o + r][o + j] = col[r];
+            for (int r = 0; r < 16; ++r) sm.inv.Ts[o + r][o + jj] = col[r];
+        } else {
+            // zero the blocks above the diagonal
+            for (int idx = tid - C; idx < C * C; idx += kThreads - C) {
+                const int r = idx / C, j = idx % C;
+                if ((j >> 4) > (r >> 4)) sm.inv.Ts[r][j] = 0.f;
+            }
         }
         __syncthreads();
-        for (int dist = 1; dist < 4; ++dist) {
-            const int nb = 4 - dist;
+#pragma unroll 1
+        for (int d = 1; d < 4; ++d) {
+            const int nb = 4 - d;
+#pragma unroll 1
             for (int idx = tid; idx < nb * 256; idx += kThreads) {
-                const int bi = idx >> 8, e = idx & 255, r = e >> 4, j = e & 15;
-                const int I = bi + dist, J = bi;
-                float x = 0.f;
-                for (int K = J; K < I; ++K)
+                const int J = idx >> 8, I = J + d, r = (idx >> 4) & 15, jj = idx & 15;
+                float x0 = 0.f, x1 = 0.f;
+#pragma unroll 1
+                for (int K = J; K < I; ++K) {
 #pragma unroll
-                    for (int kk = 0; kk < 16; ++kk)
-                        x = fmaf(sm.inv.As[16 * I + r][16 * K + kk], sm.inv.Ts[16 * K + kk][16 * J + j], x);
-                sm.inv.Xs[bi][r][j] = x;
+                    for (int kk = 0; kk < 16; kk += 2) {
+                        x0 = fmaf(sm.inv.As[16 * I + r][16 * K + kk], sm.inv.Ts[16 * K + kk][16 * J + jj], x0);
+                        x1 = fmaf(sm.inv.As[16 * I + r][16 * K + kk + 1], sm.inv.Ts[16 * K + kk + 1][16 * J + jj], x1);
+                    }
+                }
+                sm.xs[J][r][jj] = x0 + x1;
             }
             __syncthreads();
+#pragma unroll 1
             for (int idx = tid; idx < nb * 256; idx += kThreads) {
-                const int bi = idx >> 8, e = idx & 255, r = e >> 4, j = e & 15;
-                const int I = bi + dist, J = bi;
+                const int J = idx >> 8, I = J + d, r = (idx >> 4) & 15, jj = idx & 15;
                 float t = 0.f;
 #pragma unroll
                 for (int m = 0; m < 16; ++m)
-                    if (m <= r) t = fmaf(sm.inv.Ts[16 * I + r][16 * I + m], sm.inv.Xs[bi][m][j], t);
-                sm.inv.Ts[16 * I + r][16 * J + j] = -t;
+                    if (m <= r) t = fmaf(sm.inv.Ts[16 * I + r][16 * I + m], sm.xs[J][m][jj], t);
+                sm.inv.Ts[16 * I + r][16 * J + jj] = -t;
             }
             __syncthreads();
         }
@@ -428,8 +438,11 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
 
 // ================================================================== chain
 
-// TMEM columns of the chain kernel.
-constexpr int CT_S = 0, CT_D1 = 128, CT_UT = 256;
+// TMEM columns of the chain kernel.  The state ping-pongs between two
+// regions: while D1 = S [W; Q~]^T reads the current one, the threads write the
+// decayed copy S diag(e^{gamma_C}) into the other, which then accumulates
+// U^T K^ and becomes the next chunk's state.
+constexpr int CT_S0 = 0, CT_S1 = 128, CT_D1 = 256, CT_UT = 384;
 constexpr uint32_t CT_COLS = 512;
 
 struct ChainSmem {
@@ -489,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
         for (int c0 = 0; c0 < D; c0 += 16) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) vv[j] = p.init_from_pool ? Sg[(int64_t)tid * D + c0 + j] : 0.f;
-            tc::st16(tc::lane_addr(tm, warp, CT_S + c0), vv);
+            tc::st16(tc::lane_addr(tm, warp, CT_S0 + c0), vv);
         }
         tc::wait_st();
     }
@@ -522,8 +535,6 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
             bulk_g2s(sm.stage[st ^ 1], image(ci + 1), IMG_TILES, &sm.full[st ^ 1]);
             bulk_g2s(sm.egc[st ^ 1], image(ci + 1) + IMG_EGC, D * 4, &sm.full[st ^ 1]);
         }
-        float upn[C];
-        if (ci + 1 < nchunks) load_upt(ci + 1, upn);
         const bool landed = mbar_wait(&sm.full[st], (ci >> 1) & 1);
         if (__syncthreads_and(landed) == 0) {
             if (tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
@@ -532,73 +543,122 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
         }
         tc::fence_after_sync();
         const uint32_t sb = tc::smem_u32(sm.stage[st]);
+        const int s_cur = (ci & 1) ? CT_S1 : CT_S0;
+        const int s_nxt = (ci & 1) ? CT_S0 : CT_S1;
 
         // ---- D1 = S [W; Q~]^T
         if (tid == 0) {
             constexpr uint32_t id = tc::idesc_tf32(128, 128);
 #pragma unroll
             for (int ks = 0; ks < D / 8; ++ks)
-                tc::mma_tf32_ts(tm + CT_D1, tm + CT_S + 8 * ks, tc::desc_tf32_kstep(sb + IMG_BW, 128, ks), id,
+                tc::mma_tf32_ts(tm + CT_D1, tm + s_cur + 8 * ks, tc::desc_tf32_kstep(sb + IMG_BW, 128, ks), id,
                                 ks > 0);
             tc::commit(&sm.mma);
         }
+        // the next chunk's U'^T rows start loading while MMA 1 runs
+        float upn[C];
+        if (ci + 1 < nchunks) load_upt(ci + 1, upn);
+        // meanwhile: S_next = S diag(e^{gamma_C}), first half of the columns
+        // (MMA 1 only reads S); the second half overlaps the P product below
+        {
+            float a[2][16];
+#pragma unroll
+            for (int quarter = 0; quarter < 2; ++quarter) {
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2)
+                    tc::ld16(tc::lane_addr(tm, warp, s_cur + 32 * quarter + 16 * q2), a[q2]);
+                tc::wait_ld();
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) a[q2][j] *= sm.egc[st][32 * quarter + 16 * q2 + j];
+                    tc::st16(tc::lane_addr(tm, warp, s_nxt + 32 * quarter + 16 * q2), a[q2]);
+                }
+            }
+        }
         ok = wait_mma(&sm.mma, mphase, p.err_flag);
         if (!ok) break;
-        // U^T = U'^T - S W^T;  S <- S diag(e^{gamma_C})  (loads batched
-        // behind one wait per 64 columns)
+        // U^T = U'^T - S W^T
         {
-            float a[4][16];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) tc::ld16(tc::lane_addr(tm, warp, CT_D1 + 16 * q4), a[q4]);
-            tc::wait_ld();
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) a[q4][j] = upt[16 * q4 + j] - a[q4][j];
-                tc::st16(tc::lane_addr(tm, warp, CT_UT + 16 * q4), a[q4]);
-            }
+            float a[2][16];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) tc::ld16(tc::lane_addr(tm, warp, CT_S + 64 * half + 16 * q4), a[q4]);
+                for (int q2 = 0; q2 < 2; ++q2) tc::ld16(tc::lane_addr(tm, warp, CT_D1 + 32 * half + 16 * q2), a[q2]);
                 tc::wait_ld();
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
+                for (int q2 = 0; q2 < 2; ++q2) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) a[q4][j] *= sm.egc[st][64 * half + 16 * q4 + j];
-                    tc::st16(tc::lane_addr(tm, warp, CT_S + 64 * half + 16 * q4), a[q4]);
+                    for (int j = 0; j < 16; ++j) a[q2][j] = upt[32 * half + 16 * q2 + j] - a[q2][j];
+                    tc::st16(tc::lane_addr(tm, warp, CT_UT + 32 * half + 16 * q2), a[q2]);
                 }
             }
             tc::wait_st();
         }
         sync_for_mma();
-        // ---- O^T += U^T P^T ;  S += U^T K^
+        // ---- O^T += U^T P^T (needs no state) while the rest of S is decayed
         if (tid == 0) {
             constexpr uint32_t id64 = tc::idesc_tf32(128, 64);
-            constexpr uint32_t id128 = tc::idesc_tf32(128, 128);
 #pragma unroll
-            for (int ks = 0; ks < C / 8; ++ks) {
+            for (int ks = 0; ks < C / 8; ++ks)
                 tc::mma_tf32_ts(tm + CT_D1 + 64, tm + CT_UT + 8 * ks, tc::desc_tf32_kstep(sb + IMG_P, 64, ks), id64,
                                 1);
-                tc::mma_tf32_ts(tm + CT_S, tm + CT_UT + 8 * ks, tc::desc_tf32_kstep(sb + IMG_KT, 128, ks), id128,
-                                1);
+        }
+        {
+            float a[2][16];
+#pragma unroll
+            for (int quarter = 2; quarter < 4; ++quarter) {
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2)
+                    tc::ld16(tc::lane_addr(tm, warp, s_cur + 32 * quarter + 16 * q2), a[q2]);
+                tc::wait_ld();
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) a[q2][j] *= sm.egc[st][32 * quarter + 16 * q2 + j];
+                    tc::st16(tc::lane_addr(tm, warp, s_nxt + 32 * quarter + 16 * q2), a[q2]);
+                }
             }
+            tc::wait_st();
+        }
+        sync_for_mma();
+        // ---- S_next += U^T K^
+        if (tid == 0) {
+            constexpr uint32_t id128 = tc::idesc_tf32(128, 128);
+#pragma unroll
+            for (int ks = 0; ks < C / 8; ++ks)
+                tc::mma_tf32_ts(tm + s_nxt, tm + CT_UT + 8 * ks, tc::desc_tf32_kstep(sb + IMG_KT, 128, ks), id128,
+                                1);
             tc::commit(&sm.mma);
         }
         ok = wait_mma(&sm.mma, mphase, p.err_flag);
         if (!ok) break;
+        // O^T (lane = value row i, column = token r) goes out through the
+        // stage buffer this chunk no longer needs: transposed to [r][i] in
+        // shared memory, then written with 16-byte stores per token row
         {
-            float o[4][16];
+            T *ot = reinterpret_cast<T *>(sm.stage[st]);  // [C][D]
             const float scale = p.scale;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) tc::ld16(tc::lane_addr(tm, warp, CT_D1 + 64 + 16 * q4), o[q4]);
-            tc::wait_ld();
+            for (int half = 0; half < 2; ++half) {
+                float o[2][16];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
+                for (int q2 = 0; q2 < 2; ++q2) tc::ld16(tc::lane_addr(tm, warp, CT_D1 + 64 + 32 * half + 16 * q2), o[q2]);
+                tc::wait_ld();
 #pragma unroll
-                for (int rr = 0; rr < 16; ++rr)
-                    if (16 * q4 + rr < L)
-                        Elem<T>::store1(out + (t0 + 16 * q4 + rr) * tok_stride + hoff + tid, scale * o[q4][rr]);
+                for (int q2 = 0; q2 < 2; ++q2)
+#pragma unroll
+                    for (int rr = 0; rr < 16; ++rr)
+                        Elem<T>::store1(ot + (32 * half + 16 * q2 + rr) * D + tid, scale * o[q2][rr]);
+            }
+            __syncthreads();
+            constexpr int V = 16 / sizeof(T);  // elements per 16-byte vector
+            for (int idx = tid; idx < C * D / V; idx += kThreads) {
+                const int r = idx / (D / V), i0 = (idx % (D / V)) * V;
+                if (r < L)
+                    *reinterpret_cast<uint4 *>(out + (t0 + r) * tok_stride + hoff + i0) =
+                        *reinterpret_cast<const uint4 *>(ot + r * D + i0);
+            }
         }
 #pragma unroll
         for (int j = 0; j < C; ++j) upt[j] = upn[j];
@@ -610,9 +670,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
 
     if (ok) {
         float s16[16];
+        const int s_fin = (nchunks & 1) ? CT_S1 : CT_S0;
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 16) {
-            tc::ld16(tc::lane_addr(tm, warp, CT_S + c0), s16);
+            tc::ld16(tc::lane_addr(tm, warp, s_fin + c0), s16);
             tc::wait_ld();
 #pragma unroll
             for (int j = 0; j < 16; j += 4)
