@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams 
     float *S = p.pool + ((int64_t)slot * p.H + h) * (int64_t)p.dv * DK;
 
     // Issue the state loads first: they do not depend on the token.
-    float s[R][DK / kLanesPerRow];
+    LaneVec<DK> s[R];
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) load_row<DK>(S + (int64_t)(row0 + rr * 16) * DK, l, s[rr]);
 
@@ -128,20 +128,13 @@ __global__ void __launch_bounds__(kWarps * 32) decode_bulk_kernel(const DecodePa
 #pragma unroll
     for (int rr = 0; rr < ROWS / 16; ++rr) {
         const int row = rr * 16 + gid;
-        float s[DK / kLanesPerRow];
+        LaneVec<DK> s;
         float *sp = st + row * DK;
-#pragma unroll
-        for (int j = 0; j < DK / 32; ++j) {
-            const float4 t = *reinterpret_cast<const float4 *>(sp + 4 * l + 32 * j);
-            s[4 * j] = t.x; s[4 * j + 1] = t.y; s[4 * j + 2] = t.z; s[4 * j + 3] = t.w;
-        }
+        load_lane_vec_smem<DK>(sp, l, s);
         float u;
         const float c = row_update<DK, true>(s, tc, Elem<T>::load1(vrow + row), &u);
         if (l == 0) Elem<T>::store1(orow + row, row_output(c, u, tc.kq, p.scale));
-#pragma unroll
-        for (int j = 0; j < DK / 32; ++j)
-            *reinterpret_cast<float4 *>(sp + 4 * l + 32 * j) =
-                make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]);
+        store_lane_vec<DK>(sp, l, s);
     }
     fence_proxy_async_smem();
     __syncthreads();

@@ -158,6 +158,13 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
         fence_barrier_init();
     }
 
+    // This channel's 64 gates are requested first so that their latency
+    // overlaps the row loads of the norms below (thread = key channel c).
+    const int c = tid;
+    float gall[C];
+#pragma unroll
+    for (int r = 0; r < C; ++r) gall[r] = (r < L) ? __ldg(gptr + (t0 + r) * tok_stride + hoff + c) : 0.f;
+
     // ---- 1a. inverse norms (thread = token row) and beta
     {
         const int r = tid & 63;
@@ -191,16 +198,14 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
 
     // ---- 1b. thread = key channel c (and value row i = c)
     // pass 1 over the gates: ref = gamma at token 31, gamma_C, and the range
-    // of gamma (rows past the chunk's end repeat gamma_C)
-    const int c = tid;
-    // (compact loops: every CTA runs this code once, so code size, not
-    // unrolling, decides its speed)
+    // of gamma (rows past the chunk's end repeat gamma_C).  (The loops of this
+    // kernel stay compact: every CTA runs them once, so code size decides.)
     float ref = 0.f, gC = 0.f, gmin = 0.f, gmax = 0.f;
     {
         float acc = 0.f;
-#pragma unroll 8
+#pragma unroll
         for (int r = 0; r < C; ++r) {
-            acc += (r < L) ? __ldg(gptr + (t0 + r) * tok_stride + hoff + c) : 0.f;
+            acc += gall[r];
             if (r == 31) ref = acc;
             if (r == L - 1) gC = acc;
             gmin = r == 0 ? acc : fminf(gmin, acc);

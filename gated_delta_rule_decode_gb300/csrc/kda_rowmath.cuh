@@ -5,9 +5,13 @@
 // normalised query q^, alpha = exp(g), beta and v_i.  Each row is owned by an
 // 8-lane group of a warp; lane l of the group holds the dk/8 entries at key
 // channels {4l + 32j + e : j < dk/32, e < 4}, so that one float4 access per
-// j by the group covers 128 contiguous bytes of the row.
+// j by the group covers 128 contiguous bytes of the row.  A lane keeps its
+// entries as float2 pairs (channels 4l+32j+{0,1} and 4l+32j+{2,3}) and does
+// the element-wise work with the paired fp32 instructions of sm_100
+// (fma.rn.f32x2 and friends): each half is an ordinary round-to-nearest fp32
+// operation, at half the instruction count.
 //
-// All arithmetic uses explicit round-to-nearest intrinsics in one fixed order,
+// All arithmetic uses explicit round-to-nearest operations in one fixed order,
 // so every kernel that calls these functions produces the same bits for the
 // same token: replaying a record equals the decode step, bit for bit.
 #pragma once
@@ -74,51 +78,90 @@ __device__ __forceinline__ float group_sum(float x) {
     return x;
 }
 
-// ------------------------------------------------------------------ per-token coefficients
+// ------------------------------------------------------------------ lane vectors
 
+// A lane's dk/8 entries as dk/16 float2 pairs: v[2j] = channels 4l+32j+{0,1},
+// v[2j+1] = channels 4l+32j+{2,3}.
 template <int DK>
-struct TokenCoeffs {
-    static constexpr int E = DK / kLanesPerRow;  // entries per lane
-    float kh[E];      // normalised key at this lane's channels
-    float qh[E];      // normalised query at this lane's channels
-    float alpha[E];   // exp(g) at this lane's channels
-    float beta;       // sigmoid(b)
-    float kq;         // k^ . q^ over all dk channels
+struct LaneVec {
+    static constexpr int P = DK / 16;
+    float2 v[P];
 };
 
-// Channel index of entry e of lane l.
-template <int DK>
-__device__ __forceinline__ int lane_channel(int l, int e) {
-    return 4 * l + 32 * (e >> 2) + (e & 3);
+__device__ __forceinline__ void split4(float4 t, float2 &lo, float2 &hi) {
+    lo = make_float2(t.x, t.y);
+    hi = make_float2(t.z, t.w);
 }
 
 // Loads this lane's entries of a dk-vector of element type T.
 template <int DK, typename T>
-__device__ __forceinline__ void load_lane_vec(const T *p, int l, float (&x)[DK / kLanesPerRow]) {
+__device__ __forceinline__ void load_lane_vec(const T *p, int l, LaneVec<DK> &x) {
 #pragma unroll
-    for (int j = 0; j < DK / 32; ++j) {
-        float4 t = Elem<T>::load4(p + 4 * l + 32 * j);
-        x[4 * j + 0] = t.x;
-        x[4 * j + 1] = t.y;
-        x[4 * j + 2] = t.z;
-        x[4 * j + 3] = t.w;
-    }
+    for (int j = 0; j < DK / 32; ++j) split4(Elem<T>::load4(p + 4 * l + 32 * j), x.v[2 * j], x.v[2 * j + 1]);
 }
+
+// Stores this lane's entries (fp32) to global or shared memory.
+template <int DK>
+__device__ __forceinline__ void store_lane_vec(float *p, int l, const LaneVec<DK> &x) {
+#pragma unroll
+    for (int j = 0; j < DK / 32; ++j)
+        *reinterpret_cast<float4 *>(p + 4 * l + 32 * j) =
+            make_float4(x.v[2 * j].x, x.v[2 * j].y, x.v[2 * j + 1].x, x.v[2 * j + 1].y);
+}
+
+// Loads this lane's entries from fp32 shared memory.
+template <int DK>
+__device__ __forceinline__ void load_lane_vec_smem(const float *p, int l, LaneVec<DK> &x) {
+#pragma unroll
+    for (int j = 0; j < DK / 32; ++j)
+        split4(*reinterpret_cast<const float4 *>(p + 4 * l + 32 * j), x.v[2 * j], x.v[2 * j + 1]);
+}
+
+// Partial dot product of the lane's entries in a fixed association order:
+// two paired accumulators (channels {0,1} and {2,3} of each float4 slot) run
+// over the slots j in order, then are folded as ((a.x + b.x) + (a.y + b.y)).
+template <int DK>
+__device__ __forceinline__ float lane_dot(const LaneVec<DK> &s, const LaneVec<DK> &w) {
+    float2 a = __fmul2_rn(s.v[0], w.v[0]);
+    float2 b = __fmul2_rn(s.v[1], w.v[1]);
+#pragma unroll
+    for (int j = 1; j < DK / 32; ++j) {
+        a = __ffma2_rn(s.v[2 * j], w.v[2 * j], a);
+        b = __ffma2_rn(s.v[2 * j + 1], w.v[2 * j + 1], b);
+    }
+    const float2 t = __fadd2_rn(a, b);
+    return __fadd_rn(t.x, t.y);
+}
+
+// ------------------------------------------------------------------ per-token coefficients
+
+template <int DK>
+struct TokenCoeffs {
+    LaneVec<DK> kh;     // normalised key at this lane's channels
+    LaneVec<DK> qh;     // normalised query at this lane's channels
+    LaneVec<DK> alpha;  // exp(g) at this lane's channels
+    float beta;         // sigmoid(b)
+    float kq;           // k^ . q^ over all dk channels
+};
 
 // x^ = x * rsqrt(sum x^2 + eps) over the group's dk entries.
 template <int DK>
-__device__ __forceinline__ void l2norm_lane(float (&x)[DK / kLanesPerRow], float eps) {
-    float ss = 0.f;
-#pragma unroll
-    for (int e = 0; e < DK / kLanesPerRow; ++e) ss = __fmaf_rn(x[e], x[e], ss);
-    ss = group_sum(ss);
+__device__ __forceinline__ void l2norm_lane(LaneVec<DK> &x, float eps) {
+    const float ss = group_sum(lane_dot<DK>(x, x));
     const float inv = rsqrtf(__fadd_rn(ss, eps));
+    const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-    for (int e = 0; e < DK / kLanesPerRow; ++e) x[e] = __fmul_rn(x[e], inv);
+    for (int i = 0; i < DK / 16; ++i) x.v[i] = __fmul2_rn(x.v[i], inv2);
 }
 
 __device__ __forceinline__ float sigmoid_f(float b) {
     return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-b)));
+}
+
+template <int DK>
+__device__ __forceinline__ void exp_lane(LaneVec<DK> &x) {
+#pragma unroll
+    for (int i = 0; i < DK / 16; ++i) x.v[i] = make_float2(expf(x.v[i].x), expf(x.v[i].y));
 }
 
 // Q/K L2Norm, gate and beta processing for one token (decode and verify).
@@ -130,13 +173,9 @@ __device__ __forceinline__ void make_coeffs(TokenCoeffs<DK> &tc, const T *q, con
     load_lane_vec<DK, float>(g, l, tc.alpha);
     l2norm_lane<DK>(tc.kh, eps);
     l2norm_lane<DK>(tc.qh, eps);
-#pragma unroll
-    for (int e = 0; e < DK / kLanesPerRow; ++e) tc.alpha[e] = expf(tc.alpha[e]);
+    exp_lane<DK>(tc.alpha);
     tc.beta = sigmoid_f(b);
-    float kq = 0.f;
-#pragma unroll
-    for (int e = 0; e < DK / kLanesPerRow; ++e) kq = __fmaf_rn(tc.kh[e], tc.qh[e], kq);
-    tc.kq = group_sum(kq);
+    tc.kq = group_sum(lane_dot<DK>(tc.kh, tc.qh));
 }
 
 // The same coefficients rebuilt from a ReplaySSM record (no query needed).
@@ -145,51 +184,27 @@ __device__ __forceinline__ void coeffs_from_record(TokenCoeffs<DK> &tc, const fl
                                                    const float *g, float beta, int l) {
     load_lane_vec<DK, float>(k_hat, l, tc.kh);
     load_lane_vec<DK, float>(g, l, tc.alpha);
-#pragma unroll
-    for (int e = 0; e < DK / kLanesPerRow; ++e) tc.alpha[e] = expf(tc.alpha[e]);
+    exp_lane<DK>(tc.alpha);
     tc.beta = beta;
 }
 
 // ------------------------------------------------------------------ one row, one token
 
-// Partial dot product of the lane's entries in a fixed association order:
-// a 4-term FMA chain per float4 slot, then the slots summed pairwise.
-template <int DK>
-__device__ __forceinline__ float lane_dot(const float (&s)[DK / kLanesPerRow],
-                                          const float (&w)[DK / kLanesPerRow]) {
-    constexpr int J = DK / 32;
-    float p[J];
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-        float a = __fmul_rn(s[4 * j], w[4 * j]);
-        a = __fmaf_rn(s[4 * j + 1], w[4 * j + 1], a);
-        a = __fmaf_rn(s[4 * j + 2], w[4 * j + 2], a);
-        a = __fmaf_rn(s[4 * j + 3], w[4 * j + 3], a);
-        p[j] = a;
-    }
-    if constexpr (J == 1) {
-        return p[0];
-    } else if constexpr (J == 2) {
-        return __fadd_rn(p[0], p[1]);
-    } else {
-        return __fadd_rn(__fadd_rn(p[0], p[1]), __fadd_rn(p[2], p[3]));
-    }
-}
-
 // Decay, delta rule and outer-product update of one state row (in place).
 // Returns c = s'.q^ (the pre-update query dot, group-reduced) when WANT_OUT,
 // and writes u to *u_out.
 template <int DK, bool WANT_OUT>
-__device__ __forceinline__ float row_update(float (&s)[DK / kLanesPerRow], const TokenCoeffs<DK> &tc,
-                                            float v_i, float *u_out) {
+__device__ __forceinline__ float row_update(LaneVec<DK> &s, const TokenCoeffs<DK> &tc, float v_i,
+                                            float *u_out) {
 #pragma unroll
-    for (int e = 0; e < DK / kLanesPerRow; ++e) s[e] = __fmul_rn(s[e], tc.alpha[e]);
+    for (int i = 0; i < DK / 16; ++i) s.v[i] = __fmul2_rn(s.v[i], tc.alpha.v[i]);
     const float r = group_sum(lane_dot<DK>(s, tc.kh));
     float c = 0.f;
     if constexpr (WANT_OUT) c = group_sum(lane_dot<DK>(s, tc.qh));
     const float u = __fmul_rn(tc.beta, __fsub_rn(v_i, r));
+    const float2 u2 = make_float2(u, u);
 #pragma unroll
-    for (int e = 0; e < DK / kLanesPerRow; ++e) s[e] = __fmaf_rn(u, tc.kh[e], s[e]);
+    for (int i = 0; i < DK / 16; ++i) s.v[i] = __ffma2_rn(u2, tc.kh.v[i], s.v[i]);
     *u_out = u;
     return c;
 }
@@ -201,22 +216,16 @@ __device__ __forceinline__ float row_output(float c, float u, float kq, float sc
 
 // State row io: this lane's float4 slots of a row that starts at `row`.
 template <int DK>
-__device__ __forceinline__ void load_row(const float *row, int l, float (&s)[DK / kLanesPerRow]) {
+__device__ __forceinline__ void load_row(const float *row, int l, LaneVec<DK> &s) {
 #pragma unroll
-    for (int j = 0; j < DK / 32; ++j) {
-        float4 t = ld_state(row + 4 * l + 32 * j);
-        s[4 * j + 0] = t.x;
-        s[4 * j + 1] = t.y;
-        s[4 * j + 2] = t.z;
-        s[4 * j + 3] = t.w;
-    }
+    for (int j = 0; j < DK / 32; ++j) split4(ld_state(row + 4 * l + 32 * j), s.v[2 * j], s.v[2 * j + 1]);
 }
 
 template <int DK>
-__device__ __forceinline__ void store_row(float *row, int l, const float (&s)[DK / kLanesPerRow]) {
+__device__ __forceinline__ void store_row(float *row, int l, const LaneVec<DK> &s) {
 #pragma unroll
     for (int j = 0; j < DK / 32; ++j)
-        st_state(row + 4 * l + 32 * j, make_float4(s[4 * j], s[4 * j + 1], s[4 * j + 2], s[4 * j + 3]));
+        st_state(row + 4 * l + 32 * j, make_float4(s.v[2 * j].x, s.v[2 * j].y, s.v[2 * j + 1].x, s.v[2 * j + 1].y));
 }
 
 }  // namespace kda

@@ -38,23 +38,6 @@ struct SpecSmem {
     float v[kMaxDraft][ROWS];
 };
 
-template <int DK>
-__device__ __forceinline__ void put_lane_vec(float *dst, int l, const float (&x)[DK / kLanesPerRow]) {
-#pragma unroll
-    for (int j = 0; j < DK / 32; ++j)
-        *reinterpret_cast<float4 *>(dst + 4 * l + 32 * j) =
-            make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
-}
-
-template <int DK>
-__device__ __forceinline__ void get_lane_vec(const float *src, int l, float (&x)[DK / kLanesPerRow]) {
-#pragma unroll
-    for (int j = 0; j < DK / 32; ++j) {
-        const float4 t = *reinterpret_cast<const float4 *>(src + 4 * l + 32 * j);
-        x[4 * j] = t.x; x[4 * j + 1] = t.y; x[4 * j + 2] = t.z; x[4 * j + 3] = t.w;
-    }
-}
-
 template <int DK, typename T, int R>
 __global__ void __launch_bounds__(kSpecWarps * 32) verify_kernel(const VerifyParams p) {
     constexpr int ROWS = kRowStride * R;
@@ -75,7 +58,7 @@ __global__ void __launch_bounds__(kSpecWarps * 32) verify_kernel(const VerifyPar
     if (slot >= 0 && !valid && blk == 0 && threadIdx.x == 0 && p.err_flag)
         atomicOr(p.err_flag, KDA_DEVERR_SLOT);
 
-    float s[R][DK / kLanesPerRow];
+    LaneVec<DK> s[R];
     if (valid) {
         const float *S = p.pool + ((int64_t)slot * p.H + h) * (int64_t)p.dv * DK;
 #pragma unroll
@@ -95,9 +78,9 @@ __global__ void __launch_bounds__(kSpecWarps * 32) verify_kernel(const VerifyPar
         make_coeffs<DK, T>(tc, static_cast<const T *>(p.q) + tk * DK,
                            static_cast<const T *>(p.k) + tk * DK, p.g + tk * DK, bb, p.eps, l);
         if (mine) {
-            put_lane_vec<DK>(sm.kh[j], l, tc.kh);
-            put_lane_vec<DK>(sm.qh[j], l, tc.qh);
-            put_lane_vec<DK>(sm.al[j], l, tc.alpha);
+            store_lane_vec<DK>(sm.kh[j], l, tc.kh);
+            store_lane_vec<DK>(sm.qh[j], l, tc.qh);
+            store_lane_vec<DK>(sm.al[j], l, tc.alpha);
             if (l == 0) {
                 sm.beta[j] = tc.beta;
                 sm.kq[j] = tc.kq;
@@ -106,7 +89,7 @@ __global__ void __launch_bounds__(kSpecWarps * 32) verify_kernel(const VerifyPar
                 float *kr = p.rec_k_hat + tk * DK;
                 float *gr = p.rec_g + tk * DK;
                 const float *gi = p.g + tk * DK;
-                put_lane_vec<DK>(kr, l, tc.kh);
+                store_lane_vec<DK>(kr, l, tc.kh);
 #pragma unroll
                 for (int jj = 0; jj < DK / 32; ++jj)
                     *reinterpret_cast<float4 *>(gr + 4 * l + 32 * jj) =
@@ -131,9 +114,9 @@ __global__ void __launch_bounds__(kSpecWarps * 32) verify_kernel(const VerifyPar
         const int64_t tk = ((int64_t)n * p.D + j) * p.H + h;
         T *orow = static_cast<T *>(p.out) + tk * p.dv;
         TokenCoeffs<DK> tc;
-        get_lane_vec<DK>(sm.kh[j], l, tc.kh);
-        get_lane_vec<DK>(sm.qh[j], l, tc.qh);
-        get_lane_vec<DK>(sm.al[j], l, tc.alpha);
+        load_lane_vec_smem<DK>(sm.kh[j], l, tc.kh);
+        load_lane_vec_smem<DK>(sm.qh[j], l, tc.qh);
+        load_lane_vec_smem<DK>(sm.al[j], l, tc.alpha);
         tc.beta = sm.beta[j];
         tc.kq = sm.kq[j];
 #pragma unroll
@@ -180,7 +163,7 @@ __global__ void __launch_bounds__(kSpecWarps * 32) replay_kernel(const ReplayPar
     if (a == 0) return;  // nothing accepted: no memory access at all
 
     float *S = p.pool + ((int64_t)slot * p.H + h) * (int64_t)p.dv * DK;
-    float s[R][DK / kLanesPerRow];
+    LaneVec<DK> s[R];
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) load_row<DK>(S + (int64_t)(row0 + rr * kRowStride) * DK, l, s[rr]);
 
@@ -189,8 +172,8 @@ __global__ void __launch_bounds__(kSpecWarps * 32) replay_kernel(const ReplayPar
         const int64_t tk = ((int64_t)n * p.D + gid) * p.H + h;
         TokenCoeffs<DK> tc;
         coeffs_from_record<DK>(tc, p.rec_k_hat + tk * DK, p.rec_g + tk * DK, __ldg(p.rec_beta + tk), l);
-        put_lane_vec<DK>(sm.kh[gid], l, tc.kh);
-        put_lane_vec<DK>(sm.al[gid], l, tc.alpha);
+        store_lane_vec<DK>(sm.kh[gid], l, tc.kh);
+        store_lane_vec<DK>(sm.al[gid], l, tc.alpha);
         if (l == 0) sm.beta[gid] = tc.beta;
     }
     for (int idx = threadIdx.x; idx < a * ROWS; idx += kSpecWarps * 32) {
@@ -202,8 +185,8 @@ __global__ void __launch_bounds__(kSpecWarps * 32) replay_kernel(const ReplayPar
 
     for (int j = 0; j < a; ++j) {
         TokenCoeffs<DK> tc;
-        get_lane_vec<DK>(sm.kh[j], l, tc.kh);
-        get_lane_vec<DK>(sm.al[j], l, tc.alpha);
+        load_lane_vec_smem<DK>(sm.kh[j], l, tc.kh);
+        load_lane_vec_smem<DK>(sm.al[j], l, tc.alpha);
         tc.beta = sm.beta[j];
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
