@@ -215,23 +215,29 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
     const float span = fmaxf(gmax - ref, ref - gmin);
     reinterpret_cast<float *>(img + IMG_EGC)[c] = expf(gC);
     const bool unsafe = __syncthreads_or(span > kSpanLimit) != 0;
-    // pass 2: 16 tokens at a time, all of their loads issued before any use
+    // pass 2: 16 tokens at a time; the next block's loads are in flight while
+    // the current block computes
     {
         const float eref = expf(ref);
         const float egcref = expf(gC - ref);
         float acc = 0.f;
-#pragma unroll 1
-        for (int r0 = 0; r0 < C; r0 += 16) {
-            float kb[16], qb[16], vb[16], gb[16];
+        float kb[16], qb[16], vb[16], gb[16];
+        auto load_block = [&](int r0, float (&kk)[16], float (&qq)[16], float (&vv)[16], float (&gg)[16]) {
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
                 const bool ok_r = r0 + rr < L;
                 const int64_t off = (t0 + r0 + rr) * tok_stride + hoff + c;
-                kb[rr] = ok_r ? Elem<T>::load1(k + off) : 0.f;
-                qb[rr] = ok_r ? Elem<T>::load1(q + off) : 0.f;
-                vb[rr] = ok_r ? Elem<T>::load1(v + off) : 0.f;
-                gb[rr] = ok_r ? __ldg(gptr + off) : 0.f;
+                kk[rr] = ok_r ? Elem<T>::load1(k + off) : 0.f;
+                qq[rr] = ok_r ? Elem<T>::load1(q + off) : 0.f;
+                vv[rr] = ok_r ? Elem<T>::load1(v + off) : 0.f;
+                gg[rr] = ok_r ? __ldg(gptr + off) : 0.f;
             }
+        };
+        load_block(0, kb, qb, vb, gb);
+#pragma unroll 1
+        for (int r0 = 0; r0 < C; r0 += 16) {
+            float nk[16], nq[16], nv[16], ng[16];
+            if (r0 + 16 < C) load_block(r0 + 16, nk, nq, nv, ng);
             float bkt[16], bvt[16];
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
@@ -269,6 +275,13 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
             }
             tc::st16(tc::lane_addr(tm, warp, PT_BKT + r0), bkt);
             tc::st16(tc::lane_addr(tm, warp, PT_BVT + r0), bvt);
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                kb[rr] = nk[rr];
+                qb[rr] = nq[rr];
+                vb[rr] = nv[rr];
+                gb[rr] = ng[rr];
+            }
         }
     }
     tc::wait_st();

@@ -200,19 +200,34 @@ __global__ void __launch_bounds__(kSpecWarps * 32) replay_kernel(const ReplayPar
 
 template <int DK, typename T>
 static cudaError_t launch_verify_t(const VerifyParams &p, cudaStream_t st) {
-    constexpr int R = 2;  // 32 rows x dk fp32 held in registers per CTA
-    const int64_t grid = (int64_t)p.batch * p.H * (p.dv / (kRowStride * R));
-    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    verify_kernel<DK, T, R><<<(unsigned)grid, kSpecWarps * 32, 0, st>>>(p);
+    // 64 state rows per CTA where dv allows (measured faster than 32 or 16:
+    // the per-token coefficients are computed once per CTA, so larger row
+    // blocks amortise them), else 32.
+    if (p.dv % (kRowStride * 4) == 0) {
+        const int64_t grid = (int64_t)p.batch * p.H * (p.dv / (kRowStride * 4));
+        if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        verify_kernel<DK, T, 4><<<(unsigned)grid, kSpecWarps * 32, 0, st>>>(p);
+    } else {
+        const int64_t grid = (int64_t)p.batch * p.H * (p.dv / (kRowStride * 2));
+        if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        verify_kernel<DK, T, 2><<<(unsigned)grid, kSpecWarps * 32, 0, st>>>(p);
+    }
     return cudaGetLastError();
 }
 
 template <int DK, typename T>
 static cudaError_t launch_replay_t(const ReplayParams &p, cudaStream_t st) {
-    constexpr int R = 2;
-    const int64_t grid = (int64_t)p.batch * p.H * (p.dv / (kRowStride * R));
-    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    replay_kernel<DK, T, R><<<(unsigned)grid, kSpecWarps * 32, 0, st>>>(p);
+    // 64 rows per CTA where dv allows (each lane keeps 4 rows, more bytes in
+    // flight), else 32
+    if (p.dv % (kRowStride * 4) == 0) {
+        const int64_t grid = (int64_t)p.batch * p.H * (p.dv / (kRowStride * 4));
+        if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        replay_kernel<DK, T, 4><<<(unsigned)grid, kSpecWarps * 32, 0, st>>>(p);
+    } else {
+        const int64_t grid = (int64_t)p.batch * p.H * (p.dv / (kRowStride * 2));
+        if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        replay_kernel<DK, T, 2><<<(unsigned)grid, kSpecWarps * 32, 0, st>>>(p);
+    }
     return cudaGetLastError();
 }
 
