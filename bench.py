@@ -263,7 +263,7 @@ def run_decode(args, world, rank, kda, peaks, sampler):
     traffic = ncu_traffic("decode_kernel", digest)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": traffic, "kernel": "kda::decode_kernel<128,bf16,2>",
+                "traffic": traffic, "kernel": "kda::decode_kernel<128,bf16,4>",
                 "algorithmic_bytes_per_launch": DECODE_BYTES_PER_TH * units,
                 "peak_source": f"{peaks['source']} hbm_gbs (copy)",
                 "avg_kernel_us": round(avg_kernel_s * 1e6, 2)}
