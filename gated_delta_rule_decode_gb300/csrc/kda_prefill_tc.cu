@@ -102,6 +102,11 @@ __device__ inline int find_seq(const int32_t *plan, int n, int32_t c) {
 constexpr int PT_BKT = 0, PT_BVT = 64, PT_G = 128, PT_WT = 128, PT_UPT = 192;
 constexpr uint32_t PT_COLS = 256;
 
+// 8 warps: thread (warp w, lane) owns key channel c = 32 (w & 3) + lane, which
+// is also its TMEM lane and its row of the value-side tiles, for the token
+// half 32 (w >> 2) .. 32 (w >> 2) + 31.
+constexpr int kPrepThreads = 256;
+
 // Scratch of the UT inverse, laid over the [K+; Q+] tile once the A/P
 // product that reads it has completed.
 struct InvScratch {
@@ -119,6 +124,10 @@ struct PrepSmem {
         unsigned char bufT[64 * 64 * 4];     // T         (B of the WY products)
     };
     float invk[C], invq[C], beta[C];
+    float nrm[2][2 * C];  // sums of squares over each channel half: rows k_0..k_63, q_0..q_63
+    float ref[D];         // gamma at token 31
+    float gC[D];          // gamma at the chunk's last token
+    float egcref[D];      // e^{gamma_C - ref}
     float xs[3][16][17];  // off-diagonal partial products of the UT inverse
     uint64_t bar;
     uint32_t tmem_base;
@@ -127,7 +136,7 @@ constexpr size_t kPrepSmem = sizeof(PrepSmem) + 1024;
 static_assert(sizeof(InvScratch) <= 128 * 128 * 4, "inverse scratch must fit the [K+; Q+] tile");
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillParams p) {
     extern __shared__ unsigned char smem_raw[];
     PrepSmem &sm =
         *reinterpret_cast<PrepSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -142,7 +151,9 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
     if (slot < 0 || (int64_t)slot >= p.num_slots) return;  // the chain writes zeros
     const int64_t t0 = (int64_t)p.cu_seqlens[s] + (int64_t)(chunk - plan[s]) * C;
     const int L = (int)((int64_t)p.cu_seqlens[s + 1] - t0 < C ? (int64_t)p.cu_seqlens[s + 1] - t0 : C);
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = ((warp & 3) << 5) | lane;  // key channel = TMEM lane
+    const int rb = 32 * (warp >> 2);          // first token of this thread's half
     const T *__restrict__ q = static_cast<const T *>(p.q);
     const T *__restrict__ k = static_cast<const T *>(p.k);
     const T *__restrict__ v = static_cast<const T *>(p.v);
@@ -158,75 +169,91 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
         fence_barrier_init();
     }
 
-    // This channel's 64 gates are requested first so that their latency
-    // overlaps the row loads of the norms below (thread = key channel c).
-    const int c = tid;
-    float gall[C];
+    // this channel's gates over its token half, in flight during the norms
+    float gh[32];
 #pragma unroll
-    for (int r = 0; r < C; ++r) gall[r] = (r < L) ? __ldg(gptr + (t0 + r) * tok_stride + hoff + c) : 0.f;
+    for (int r = 0; r < 32; ++r) gh[r] = (rb + r < L) ? __ldg(gptr + (t0 + rb + r) * tok_stride + hoff + c) : 0.f;
 
-    // ---- 1a. inverse norms (thread = token row) and beta
+    // ---- 1a. sums of squares: thread = (row of k or q, half of the channels);
+    // the loop is unrolled so that the row is in flight at once
     {
-        const int r = tid & 63;
-        const bool isq = tid >= 64;
-        float inv = 0.f;
+        const int row = tid & (2 * C - 1), ch = tid >> 7;
+        const int r = row & (C - 1);
+        float ss = 0.f;
         if (r < L) {
-            const T *row = (isq ? q : k) + (t0 + r) * tok_stride + hoff;
-            float ss = 0.f;
-#pragma unroll 4
-            for (int j = 0; j < D; j += 4) {
-                const float4 x = Elem<T>::load4(row + j);
+            const T *src = (row >= C ? q : k) + (t0 + r) * tok_stride + hoff + 64 * ch;
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+                const float4 x = Elem<T>::load4(src + j);
                 ss = fmaf(x.x, x.x, ss);
                 ss = fmaf(x.y, x.y, ss);
                 ss = fmaf(x.z, x.z, ss);
                 ss = fmaf(x.w, x.w, ss);
             }
-            inv = rsqrtf(ss + p.eps);
         }
-        if (isq) {
+        sm.nrm[ch][row] = ss;
+    }
+    // ---- 1b. gamma (thread = key channel c): the first half's running sum
+    // ends at ref = gamma_31; the second half continues it from there.  Rows
+    // past the chunk's end repeat gamma_C.
+    float acc = 0.f, gmin = 0.f, gmax = 0.f, gC = 0.f;
+    if (rb == 0) {
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            acc += gh[r];
+            if (r == L - 1) gC = acc;
+            gmin = r == 0 ? acc : fminf(gmin, acc);
+            gmax = r == 0 ? acc : fmaxf(gmax, acc);
+        }
+        sm.ref[c] = acc;
+        if (L <= 32) sm.gC[c] = gC;
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (tid < 2 * C) {
+        const int r = tid & (C - 1);
+        const float inv = (r < L) ? rsqrtf(sm.nrm[0][tid] + sm.nrm[1][tid] + p.eps) : 0.f;
+        if (tid >= C) {
             sm.invq[r] = inv;
         } else {
             sm.invk[r] = inv;
             sm.beta[r] = (r < L) ? sigmoid_f(Elem<T>::load1(bb + (t0 + r) * H + h)) : 0.f;
         }
     }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tm = sm.tmem_base;
-    uint32_t phase = 0;
-
-    // ---- 1b. thread = key channel c (and value row i = c)
-    // pass 1 over the gates: ref = gamma at token 31, gamma_C, and the range
-    // of gamma (rows past the chunk's end repeat gamma_C).  (The loops of this
-    // kernel stay compact: every CTA runs them once, so code size decides.)
-    float ref = 0.f, gC = 0.f, gmin = 0.f, gmax = 0.f;
-    {
-        float acc = 0.f;
+    const float ref = sm.ref[c];
+    if (rb == 32) {
+        acc = ref;
 #pragma unroll
-        for (int r = 0; r < C; ++r) {
-            acc += gall[r];
-            if (r == 31) ref = acc;
-            if (r == L - 1) gC = acc;
+        for (int r = 0; r < 32; ++r) {
+            acc += gh[r];
+            if (32 + r == L - 1) gC = acc;
             gmin = r == 0 ? acc : fminf(gmin, acc);
             gmax = r == 0 ? acc : fmaxf(gmax, acc);
         }
+        if (L > 32) sm.gC[c] = gC;
     }
     const float span = fmaxf(gmax - ref, ref - gmin);
-    reinterpret_cast<float *>(img + IMG_EGC)[c] = expf(gC);
     const bool unsafe = __syncthreads_or(span > kSpanLimit) != 0;
-    // pass 2: 16 tokens at a time; the next block's loads are in flight while
-    // the current block computes
+    gC = sm.gC[c];
+    if (rb == 0) {
+        reinterpret_cast<float *>(img + IMG_EGC)[c] = expf(gC);
+        sm.egcref[c] = expf(gC - ref);
+    }
+    const uint32_t tm = sm.tmem_base;
+    uint32_t phase = 0;
+
+    // ---- 2. this thread's 32 tokens, 8 at a time; the next block's loads are
+    // in flight while the current block computes
     {
         const float eref = expf(ref);
-        const float egcref = expf(gC - ref);
-        float acc = 0.f;
-        float kb[16], qb[16], vb[16], gb[16];
-        auto load_block = [&](int r0, float (&kk)[16], float (&qq)[16], float (&vv)[16], float (&gg)[16]) {
+        acc = rb == 0 ? 0.f : ref;
+        float kb[8], qb[8], vb[8], gb[8];
+        auto load_block = [&](int r0, float (&kk)[8], float (&qq)[8], float (&vv)[8], float (&gg)[8]) {
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) {
-                const bool ok_r = r0 + rr < L;
-                const int64_t off = (t0 + r0 + rr) * tok_stride + hoff + c;
+            for (int rr = 0; rr < 8; ++rr) {
+                const bool ok_r = rb + r0 + rr < L;
+                const int64_t off = (t0 + rb + r0 + rr) * tok_stride + hoff + c;
                 kk[rr] = ok_r ? Elem<T>::load1(k + off) : 0.f;
                 qq[rr] = ok_r ? Elem<T>::load1(q + off) : 0.f;
                 vv[rr] = ok_r ? Elem<T>::load1(v + off) : 0.f;
@@ -235,19 +262,19 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
         };
         load_block(0, kb, qb, vb, gb);
 #pragma unroll 1
-        for (int r0 = 0; r0 < C; r0 += 16) {
-            float nk[16], nq[16], nv[16], ng[16];
-            if (r0 + 16 < C) load_block(r0 + 16, nk, nq, nv, ng);
-            float bkt[16], bvt[16];
+        for (int r0 = 0; r0 < 32; r0 += 8) {
+            float nk[8], nq[8], nv[8], ng[8];
+            if (r0 + 8 < 32) load_block(r0 + 8, nk, nq, nv, ng);
+            float bkt[8], bvt[8];
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) {
-                const int r = r0 + rr;
+            for (int rr = 0; rr < 8; ++rr) {
+                const int r = rb + r0 + rr;
                 const bool valid = r < L;
                 acc += gb[rr];
                 const float gam = acc;
                 const float kx = kb[rr] * sm.invk[r];
                 const float qx = qb[rr] * sm.invq[r];
-                float ktil, qtil, khat_end;
+                float ktil, qtil;
                 if (!unsafe) {
                     const float E = __expf(gam - ref);
                     const float Ei = __expf(ref - gam);
@@ -257,7 +284,6 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
                     st_sw(sm.bufKM, 64, r, c, kx * Ei);
                     ktil = kp * eref;
                     qtil = qp * eref;
-                    khat_end = kx * Ei * egcref;
                 } else {
                     // plain [64][128] copies of k^, q^ and gamma for the exact path
                     reinterpret_cast<float *>(sm.bufKQ)[r * D + c] = kx;
@@ -266,17 +292,16 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
                     const float eg = expf(gam);
                     ktil = kx * eg;
                     qtil = qx * eg;
-                    khat_end = kx * expf(gC - gam);
+                    st_sw(img + IMG_KT, 128, c, r, valid ? kx * expf(gC - gam) : 0.f);
                 }
                 st_sw(img + IMG_BW, 128, 64 + r, c, qtil);  // Q~ rows of [W; Q~]
-                st_sw(img + IMG_KT, 128, c, r, valid ? khat_end : 0.f);
                 bkt[rr] = sm.beta[r] * ktil;
                 bvt[rr] = sm.beta[r] * vb[rr];
             }
-            tc::st16(tc::lane_addr(tm, warp, PT_BKT + r0), bkt);
-            tc::st16(tc::lane_addr(tm, warp, PT_BVT + r0), bvt);
+            tc::st8(tc::lane_addr(tm, warp, PT_BKT + rb + r0), bkt);
+            tc::st8(tc::lane_addr(tm, warp, PT_BVT + rb + r0), bvt);
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) {
+            for (int rr = 0; rr < 8; ++rr) {
                 kb[rr] = nk[rr];
                 qb[rr] = nq[rr];
                 vb[rr] = nv[rr];
@@ -288,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
     sync_for_mma();
 
     bool ok = true;
-    // ---- 2. A and P
+    // ---- 3. A and P
     if (!unsafe) {
         if (tid == 0) {
             constexpr uint32_t id = tc::idesc_tf32(128, 64);
@@ -301,23 +326,35 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
         }
         ok = wait_mma(&sm.bar, phase, p.err_flag);
         if (ok) {
-            // lanes 0..63: rows of A'; lanes 64..127: rows of P
-            const int r = tid & 63;
+            // the K^^T image tile, transposed out of K- (K^ = K- e^{gamma_C - ref})
+            // now that its product has completed: warp w writes rows
+            // 16 w .. 16 w + 15 of both 32-token halves, one token per lane, so
+            // every store is one 128-byte line
+#pragma unroll 4
+            for (int it = 0; it < 32; ++it) {
+                const int cc = 16 * warp + (it >> 1);
+                const int r = 32 * (it & 1) + lane;
+                const float km = *reinterpret_cast<const float *>(sm.bufKM + tc::sw128_off(r, cc, 64));
+                st_sw(img + IMG_KT, 128, cc, r, r < L ? km * sm.egcref[cc] : 0.f);
+            }
+            // G rows (TMEM lanes): 0..63 are A', 64..127 are P; warp w takes
+            // columns 32 (w >> 2) .. 32 (w >> 2) + 31
+            const int grow = c, r = grow & (C - 1), j0 = rb;
             float g16[16];
 #pragma unroll
-            for (int j0 = 0; j0 < C; j0 += 16) {
-                tc::ld16(tc::lane_addr(tm, warp, PT_G + j0), g16);
+            for (int jb = 0; jb < 32; jb += 16) {
+                tc::ld16(tc::lane_addr(tm, warp, PT_G + j0 + jb), g16);
                 tc::wait_ld();
-                if (tid < 64) {
+                if (grow < C) {
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
-                        const int j = j0 + jj;
+                        const int j = j0 + jb + jj;
                         sm.inv.As[r][j] = (j < r) ? sm.beta[r] * g16[jj] : 0.f;
                     }
                 } else {
 #pragma unroll
                     for (int jj = 0; jj < 16; jj += 4) {
-                        const int j = j0 + jj;
+                        const int j = j0 + jb + jj;
                         *reinterpret_cast<float4 *>(img + IMG_P + tc::sw128_off(r, j, 64)) =
                             make_float4(j <= r ? g16[jj] : 0.f, j + 1 <= r ? g16[jj + 1] : 0.f,
                                         j + 2 <= r ? g16[jj + 2] : 0.f, j + 3 <= r ? g16[jj + 3] : 0.f);
@@ -330,10 +367,10 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
         const float *kh = reinterpret_cast<const float *>(sm.bufKQ);
         const float *qh = kh + C * D;
         const float *gm = reinterpret_cast<const float *>(sm.bufKM);
-        float areg[C * C / kThreads];
+        float areg[C * C / kPrepThreads];
 #pragma unroll 1
-        for (int it = 0; it < C * C / kThreads; ++it) {
-            const int idx = tid + it * kThreads;
+        for (int it = 0; it < C * C / kPrepThreads; ++it) {
+            const int idx = tid + it * kPrepThreads;
             const int r = idx / C, j = idx % C;
             float a = 0.f, pp = 0.f;
             if (j <= r) {
@@ -348,15 +385,15 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
         }
         __syncthreads();
 #pragma unroll
-        for (int it = 0; it < C * C / kThreads; ++it) {
-            const int idx = tid + it * kThreads;
+        for (int it = 0; it < C * C / kPrepThreads; ++it) {
+            const int idx = tid + it * kPrepThreads;
             sm.inv.As[idx / C][idx % C] = areg[it];
         }
     }
     __syncthreads();
 
     if (ok) {
-        // ---- 2c. T = (I + A)^-1 (unit lower triangular), blocked by 16:
+        // ---- 4. T = (I + A)^-1 (unit lower triangular), blocked by 16:
         // the four diagonal blocks by forward substitution (one column per
         // thread, in registers), then the blocks below the diagonal in order of
         // distance d: X = sum_{K=J}^{I-1} A_IK T_KJ, T_IJ = -T_II X.
@@ -365,17 +402,17 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
             float col[16];
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
-                float acc = (r == jj) ? 1.f : 0.f;
+                float acc2 = (r == jj) ? 1.f : 0.f;
 #pragma unroll
                 for (int m = 0; m < r; ++m)
-                    if (m >= jj) acc = fmaf(-sm.inv.As[o + r][o + m], col[m], acc);
-                col[r] = (r >= jj) ? acc : 0.f;
+                    if (m >= jj) acc2 = fmaf(-sm.inv.As[o + r][o + m], col[m], acc2);
+                col[r] = (r >= jj) ? acc2 : 0.f;
             }
 #pragma unroll
             for (int r = 0; r < 16; ++r) sm.inv.Ts[o + r][o + jj] = col[r];
         } else {
             // zero the blocks above the diagonal
-            for (int idx = tid - C; idx < C * C; idx += kThreads - C) {
+            for (int idx = tid - C; idx < C * C; idx += kPrepThreads - C) {
                 const int r = idx / C, j = idx % C;
                 if ((j >> 4) > (r >> 4)) sm.inv.Ts[r][j] = 0.f;
             }
@@ -385,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
         for (int d = 1; d < 4; ++d) {
             const int nb = 4 - d;
 #pragma unroll 1
-            for (int idx = tid; idx < nb * 256; idx += kThreads) {
+            for (int idx = tid; idx < nb * 256; idx += kPrepThreads) {
                 const int J = idx >> 8, I = J + d, r = (idx >> 4) & 15, jj = idx & 15;
                 float x0 = 0.f, x1 = 0.f;
 #pragma unroll 1
@@ -400,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
             }
             __syncthreads();
 #pragma unroll 1
-            for (int idx = tid; idx < nb * 256; idx += kThreads) {
+            for (int idx = tid; idx < nb * 256; idx += kPrepThreads) {
                 const int J = idx >> 8, I = J + d, r = (idx >> 4) & 15, jj = idx & 15;
                 float t = 0.f;
 #pragma unroll
@@ -410,14 +447,14 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
             }
             __syncthreads();
         }
-        for (int idx = tid; idx < C * C / 4; idx += kThreads) {
+        for (int idx = tid; idx < C * C / 4; idx += kPrepThreads) {
             const int r = idx / (C / 4), j = (idx % (C / 4)) * 4;
             *reinterpret_cast<float4 *>(sm.bufT + tc::sw128_off(r, j, 64)) =
                 make_float4(sm.inv.Ts[r][j], sm.inv.Ts[r][j + 1], sm.inv.Ts[r][j + 2], sm.inv.Ts[r][j + 3]);
         }
         sync_for_mma();
 
-        // ---- 3. W^T = (beta K~)^T T^T and U'^T = (beta V)^T T^T
+        // ---- 5. W^T = (beta K~)^T T^T and U'^T = (beta V)^T T^T
         if (tid == 0) {
             constexpr uint32_t id = tc::idesc_tf32(128, 64);
             const uint32_t b0 = tc::smem_u32(sm.bufT);
@@ -431,19 +468,20 @@ __global__ void __launch_bounds__(kThreads, 2) prep_tc_kernel(const PrefillParam
         }
         ok = wait_mma(&sm.bar, phase, p.err_flag);
         if (ok) {
+            // lane c: W[r][c] and U'^T[c][r] for this thread's token half
             float w16[16];
-            float *upt = reinterpret_cast<float *>(img + IMG_UPT) + (size_t)tid * C;
+            float *upt = reinterpret_cast<float *>(img + IMG_UPT) + (size_t)c * C;
 #pragma unroll
-            for (int r0 = 0; r0 < C; r0 += 16) {
-                tc::ld16(tc::lane_addr(tm, warp, PT_WT + r0), w16);  // lane c: W[r][c]
+            for (int r0 = 0; r0 < 32; r0 += 16) {
+                tc::ld16(tc::lane_addr(tm, warp, PT_WT + rb + r0), w16);
                 tc::wait_ld();
 #pragma unroll
-                for (int rr = 0; rr < 16; ++rr) st_sw(img + IMG_BW, 128, r0 + rr, c, w16[rr]);
-                tc::ld16(tc::lane_addr(tm, warp, PT_UPT + r0), w16);  // lane i: U'^T[i][r]
+                for (int rr = 0; rr < 16; ++rr) st_sw(img + IMG_BW, 128, rb + r0 + rr, c, w16[rr]);
+                tc::ld16(tc::lane_addr(tm, warp, PT_UPT + rb + r0), w16);
                 tc::wait_ld();
 #pragma unroll
                 for (int rr = 0; rr < 16; rr += 4)
-                    *reinterpret_cast<float4 *>(upt + r0 + rr) =
+                    *reinterpret_cast<float4 *>(upt + rb + r0 + rr) =
                         make_float4(w16[rr], w16[rr + 1], w16[rr + 2], w16[rr + 3]);
             }
         }
@@ -735,7 +773,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     const int64_t mc = max_chunks(p.num_seqs, p.total_tokens);
     if (mc > 0) {
-        prep_tc_kernel<__nv_bfloat16><<<dim3((unsigned)mc, (unsigned)p.H), kThreads, kPrepSmem, st>>>(p);
+        prep_tc_kernel<__nv_bfloat16><<<dim3((unsigned)mc, (unsigned)p.H), kPrepThreads, kPrepSmem, st>>>(p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
