@@ -72,6 +72,10 @@ struct PrefillParams {
 // Each launcher returns cudaSuccess or the launch error.
 cudaError_t launch_decode(const DecodeParams &p, int dk, int dtype, cudaStream_t s);
 cudaError_t launch_verify(const VerifyParams &p, int dk, int dtype, cudaStream_t s);
+// Tensor-core row phase of verify (bf16, dk = dv = 128, D <= 8): whether it
+// applies to these parameters, and its launcher.
+bool verify_tc_supported(const VerifyParams &p, int dk, int dtype);
+cudaError_t launch_verify_tc(const VerifyParams &p, cudaStream_t st);
 cudaError_t launch_replay(const ReplayParams &p, int dk, int dtype, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams &p, int dtype, cudaStream_t s);
 size_t prefill_workspace_bytes(int H, int dk, int dv, int dtype, int32_t num_seqs, int64_t total_tokens);

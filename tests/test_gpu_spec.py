@@ -138,23 +138,26 @@ def test_verify_many_items_per_cta(D):
     assert torch.equal(rec["g"].cpu(), x.g)
 
 
-@pytest.mark.parametrize("g_mean,D", [(-8.0, 16), (-3.0, 7), (6.0, 16), (3.0, 9)])
-def test_verify_decay_range(g_mean, D):
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("g_mean,D", [(-8.0, 16), (-8.0, 8), (-3.0, 7), (6.0, 16), (6.0, 5), (3.0, 9)])
+def test_verify_decay_range(dtype, g_mean, D):
     """Near-total decay (alpha ~ 3e-4 per token: the window's decay products
     underflow), strong, negligible and typical decay, over windows that take
-    both register-array sizes."""
+    each verify path (bf16 windows of up to 8 tokens at dk = dv = 128 use the
+    tensor-core row phase)."""
     kda = _kda()
     B, H, dk, dv, NS = 4, 2, 128, 128, 6
-    x = inputs.verify_inputs(B, D, H, dk, dv, dtype="f32", num_slots=NS, seed=31 + D,
+    x = inputs.verify_inputs(B, D, H, dk, dv, dtype=dtype, num_slots=NS, seed=31 + D,
                              g_mean=g_mean)
     out, _ = kda.verify_record(x.q.cuda(), x.k.cuda(), x.v.cuda(), x.g.cuda(),
                                x.b.cuda(), x.slot_ids.cuda(), x.pool.cuda())
     torch.cuda.synchronize()
-    assert torch.isfinite(out).all()
+    assert torch.isfinite(out.float()).all()
     o_ref, _, e = oracle.verify(x.q, x.k, x.v, x.g, x.b, x.slot_ids, x.pool)
     assert e == 0
-    atol, rtol = tol_for(torch.float32)
-    assert_close(to_np64(out), o_ref, atol, rtol, "verify outputs")
+    dt = inputs.torch_dtype(dtype)
+    atol, rtol = tol_for(dt)
+    assert_close(to_np64(out), round_to(o_ref, dt), atol, rtol, "verify outputs")
 
 
 def test_replay_rejects_bad_accepted_length_and_slot():
