@@ -18,11 +18,12 @@
 //   the state and writes, per (chunk, head), an operand image that the chain
 //   kernel copies into shared memory with one bulk copy:
 //     [W; Q~] (128 x 128), P (64 x 64), K^^T (128 x 64) as K-major 128B-swizzled
-//     tf32 tiles, e^{gamma_C} (128) and U'^T (128 x 64, plain fp32).
-// chain_tc_kernel  one CTA per (sequence, head) walks the chunks in order.
-//   The fp32 state never leaves tensor memory: it is the A operand of
-//   D1 = S [W; Q~]^T and the accumulator of S += U^T K^.  The operand image of
-//   chunk c+1 is in flight (bulk copy, double-buffered) while chunk c computes.
+//     tf32 tiles, e^{gamma_C} (128) and U' (64 x 128, plain fp32).
+// chain_tc_kernel  one CTA per (sequence, head, block of 32 value rows) walks
+//   the chunks in order; rows of the state are independent, so four CTAs
+//   share a head.  The rows sit on the N side of the products and the state
+//   block is a swizzled tile in shared memory (the B operand).  The operand
+//   images of the next chunk are in flight (bulk copies) while a chunk computes.
 //
 // Decay factors in the A/P product: with ref = gamma at token 31 of the chunk,
 // K+ = k^ e^{gamma-ref}, Q+ = q^ e^{gamma-ref}, K- = k^ e^{ref-gamma}, so that
@@ -51,8 +52,8 @@ constexpr uint32_t IMG_P = IMG_BW + 128 * 128 * 4;     // P        64 rows x K 6
 constexpr uint32_t IMG_KT = IMG_P + 64 * 64 * 4;       // K^^T     128 rows x K 64
 constexpr uint32_t IMG_TILES = IMG_KT + 128 * 64 * 4;  // = 112 KiB, one bulk copy
 constexpr uint32_t IMG_EGC = IMG_TILES;                // e^{gamma_C}, 128 fp32
-constexpr uint32_t IMG_UPT = IMG_EGC + 1024;           // U'^T plain [128][64] fp32
-constexpr uint32_t IMG_BYTES = IMG_UPT + 128 * 64 * 4;
+constexpr uint32_t IMG_UP = IMG_EGC + 1024;            // U' plain [64 tokens][128 value rows] fp32
+constexpr uint32_t IMG_BYTES = IMG_UP + 64 * 128 * 4;
 
 __host__ __device__ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -468,9 +469,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         }
         ok = wait_mma(&sm.bar, phase, p.err_flag);
         if (ok) {
-            // lane c: W[r][c] and U'^T[c][r] for this thread's token half
+            // lane c: W[r][c] and U'[r][c] for this thread's token half (a warp's
+            // stores of one token row are one 128-byte line)
             float w16[16];
-            float *upt = reinterpret_cast<float *>(img + IMG_UPT) + (size_t)c * C;
+            float *up = reinterpret_cast<float *>(img + IMG_UP);
 #pragma unroll
             for (int r0 = 0; r0 < 32; r0 += 16) {
                 tc::ld16(tc::lane_addr(tm, warp, PT_WT + rb + r0), w16);
@@ -480,9 +482,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                 tc::ld16(tc::lane_addr(tm, warp, PT_UPT + rb + r0), w16);
                 tc::wait_ld();
 #pragma unroll
-                for (int rr = 0; rr < 16; rr += 4)
-                    *reinterpret_cast<float4 *>(upt + rb + r0 + rr) =
-                        make_float4(w16[rr], w16[rr + 1], w16[rr + 2], w16[rr + 3]);
+                for (int rr = 0; rr < 16; ++rr) up[(rb + r0 + rr) * D + c] = w16[rr];
             }
         }
     }
@@ -494,17 +494,30 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
 
 // ================================================================== chain
 
-// TMEM columns of the chain kernel.  The state ping-pongs between two
-// regions: while D1 = S [W; Q~]^T reads the current one, the threads write the
-// decayed copy S diag(e^{gamma_C}) into the other, which then accumulates
-// U^T K^ and becomes the next chunk's state.
-constexpr int CT_S0 = 0, CT_S1 = 128, CT_D1 = 256, CT_UT = 384;
-constexpr uint32_t CT_COLS = 512;
+// One CTA per (sequence, head, block of NR value rows).  With the rows on the
+// N side, a chunk step is
+//   D1 = [W; Q~] Sb^T            M = 128 (token rows of W, then of Q~), N = NR, K = 128
+//   U = U' - D1[0:64]            thread = token r = TMEM lane r, into the swizzled U tile
+//   D1[64:128] += P U            A = P placed in rows 64..127 of a 128-row tile
+//   D3 = K^^T U                  M = 128 channels, N = NR, K = 64 tokens
+//   Sb <- Sb diag(e^{gamma_C}) + D3^T,   O = scale D1[64:128]
+// (the A operands come from the chunk's operand image; Sb and U are K-major
+// 128-byte-swizzled tiles in shared memory).
+constexpr int NR = 32;
+constexpr int kRowBlocks = D / NR;
+constexpr uint32_t CT_D1 = 0, CT_D3 = NR;
+constexpr uint32_t CT_COLS = 64;
+constexpr uint32_t kPKBytes = 2 * 8192 + 128 * 64 * 4 + D * 4;  // P, K^^T, e^{gamma_C}
 
 struct ChainSmem {
-    unsigned char stage[2][IMG_TILES];  // [W;Q~] | P | K^^T, double-buffered
+    unsigned char bw[2][128 * 128 * 4];  // [W; Q~], double-buffered
+    unsigned char p128[2][128 * 128];    // 2 token atoms of a 128-row tile; P in rows 64..127
+    unsigned char kt[2][128 * 128];      // K^^T: 2 token atoms of 128 channel rows
+    unsigned char sb[4][NR * 128];       // state block: 4 channel atoms of NR rows
+    unsigned char ub[2][NR * 128];       // U block: 2 token atoms of NR rows
     float egc[2][D];
-    uint64_t full[2];
+    uint64_t full_bw[2];
+    uint64_t full_pk;
     uint64_t mma;
     uint32_t tmem_base;
 };
@@ -518,15 +531,16 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
     const int32_t *plan = static_cast<const int32_t *>(p.workspace);
     const int n = p.num_seqs;
     if (plan[n + 1] == 0) return;
-    const int s = blockIdx.x, h = blockIdx.y, H = p.H;
+    const int s = blockIdx.x, h = blockIdx.y, i0 = blockIdx.z * NR, H = p.H;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int32_t cs = p.cu_seqlens[s], ce = p.cu_seqlens[s + 1];
     const int slot = p.slot_ids[s];
     T *out = static_cast<T *>(p.out);
-    const int64_t tok_stride = (int64_t)H * D, hoff = (int64_t)h * D;
+    const int64_t tok_stride = (int64_t)H * D, hoff = (int64_t)h * D + i0;
     if (slot < 0 || (int64_t)slot >= p.num_slots) {
-        for (int64_t t = cs; t < ce; ++t) Elem<T>::store1(out + t * tok_stride + hoff + tid, 0.f);
-        if (slot >= 0 && h == 0 && tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_SLOT);
+        for (int64_t t = cs; t < ce; ++t)
+            if (tid < NR) Elem<T>::store1(out + t * tok_stride + hoff + tid, 0.f);
+        if (slot >= 0 && h == 0 && blockIdx.z == 0 && tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_SLOT);
         return;
     }
     const int nchunks = plan[s + 1] - plan[s];
@@ -534,214 +548,189 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
     auto image = [&](int ci) {
         return ws + ((size_t)(plan[s] + ci) * H + h) * (size_t)IMG_BYTES;
     };
+    auto issue_bw = [&](int ci, int b) {
+        mbar_arrive_expect_tx(&sm.full_bw[b], 128 * 128 * 4);
+        bulk_g2s(sm.bw[b], image(ci) + IMG_BW, 128 * 128 * 4, &sm.full_bw[b]);
+    };
+    auto issue_pk = [&](int ci) {
+        mbar_arrive_expect_tx(&sm.full_pk, kPKBytes);
+        bulk_g2s(sm.p128[0] + 8192, image(ci) + IMG_P, 8192, &sm.full_pk);
+        bulk_g2s(sm.p128[1] + 8192, image(ci) + IMG_P + 8192, 8192, &sm.full_pk);
+        bulk_g2s(sm.kt, image(ci) + IMG_KT, 128 * 64 * 4, &sm.full_pk);
+        bulk_g2s(sm.egc[ci & 1], image(ci) + IMG_EGC, D * 4, &sm.full_pk);
+    };
 
     if (warp == 0) tc::tmem_alloc(&sm.tmem_base, CT_COLS);
     if (tid == 0) {
-        mbar_init(&sm.full[0], 1);
-        mbar_init(&sm.full[1], 1);
+        mbar_init(&sm.full_bw[0], 1);
+        mbar_init(&sm.full_bw[1], 1);
+        mbar_init(&sm.full_pk, 1);
         mbar_init(&sm.mma, 1);
         fence_barrier_init();
         if (nchunks > 0) {
-            mbar_arrive_expect_tx(&sm.full[0], IMG_TILES + D * 4);
-            bulk_g2s(sm.stage[0], image(0), IMG_TILES, &sm.full[0]);
-            bulk_g2s(sm.egc[0], image(0) + IMG_EGC, D * 4, &sm.full[0]);
+            issue_bw(0, 0);
+            issue_pk(0);
         }
     }
+    // rows 0..63 of the P tile only feed discarded accumulator lanes; zeroed
+    // once so that they hold finite values
+    for (int idx = tid; idx < 2 * 8192 / 16; idx += kThreads)
+        *reinterpret_cast<uint4 *>(sm.p128[idx >> 9] + (idx & 511) * 16) = make_uint4(0, 0, 0, 0);
+    // initial state block (rows i0 .. i0 + NR) into the swizzled tile
+    float *Sg = p.pool + ((int64_t)slot * H + h) * (int64_t)D * D + (int64_t)i0 * D;
+    for (int idx = tid; idx < NR * (D / 4); idx += kThreads) {
+        const int i = idx / (D / 4), c4 = (idx % (D / 4)) * 4;
+        const float4 x = p.init_from_pool ? *reinterpret_cast<const float4 *>(Sg + (int64_t)i * D + c4)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(&sm.sb[0][0] + tc::sw128_off(i, c4, NR)) = x;
+    }
+    fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tm = sm.tmem_base;
-    float *Sg = p.pool + ((int64_t)slot * H + h) * (int64_t)D * D;
-    {
-        float vv[16];
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 16) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) vv[j] = p.init_from_pool ? Sg[(int64_t)tid * D + c0 + j] : 0.f;
-            tc::st16(tc::lane_addr(tm, warp, CT_S0 + c0), vv);
-        }
-        tc::wait_st();
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
 
     uint32_t mphase = 0;
     bool ok = true;
-    // this thread's row of U'^T (value row i = tid): the next chunk's row is
-    // loaded into registers while the current chunk computes
-    float upt[C];
-    auto load_upt = [&](int ci, float (&dst)[C]) {
-        const float4 *src = reinterpret_cast<const float4 *>(image(ci) + IMG_UPT) + (size_t)tid * (C / 4);
+    int last_bw[2] = {nchunks > 0 ? 0 : -1, -1}, last_pk = nchunks > 0 ? 0 : -1;
+    // this token thread's U' values for the block (threads 0..63), the next
+    // chunk's in flight while the current one computes
+    float upc[NR], upn[NR];
+    auto load_up = [&](int ci, float (&dst)[NR]) {
+        const float4 *src = reinterpret_cast<const float4 *>(image(ci) + IMG_UP) + ((size_t)tid * D + i0) / 4;
 #pragma unroll
-        for (int j = 0; j < C / 4; ++j) {
+        for (int j = 0; j < NR / 4; ++j) {
             const float4 x = __ldg(src + j);
             dst[4 * j] = x.x; dst[4 * j + 1] = x.y; dst[4 * j + 2] = x.z; dst[4 * j + 3] = x.w;
         }
     };
-    if (nchunks > 0) load_upt(0, upt);
+    if (tid < C && nchunks > 0) load_up(0, upc);
+
     for (int ci = 0; ci < nchunks; ++ci) {
-        const int st = ci & 1;
+        const int b = ci & 1;
         const int64_t t0 = (int64_t)cs + (int64_t)ci * C;
         const int L = (int)((int64_t)ce - t0 < C ? (int64_t)ce - t0 : C);
-        // prefetch the next chunk's image into the other stage (its previous
-        // user, chunk ci-1, has finished all its MMAs and reads)
-        if (tid == 0 && ci + 1 < nchunks) {
-            mbar_arrive_expect_tx(&sm.full[st ^ 1], IMG_TILES + D * 4);
-            bulk_g2s(sm.stage[st ^ 1], image(ci + 1), IMG_TILES, &sm.full[st ^ 1]);
-            bulk_g2s(sm.egc[st ^ 1], image(ci + 1) + IMG_EGC, D * 4, &sm.full[st ^ 1]);
-        }
-        const bool landed = mbar_wait(&sm.full[st], (ci >> 1) & 1);
+        const bool landed = mbar_wait(&sm.full_bw[b], (ci >> 1) & 1);
         if (__syncthreads_and(landed) == 0) {
             if (tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
             ok = false;
             break;
         }
         tc::fence_after_sync();
-        const uint32_t sb = tc::smem_u32(sm.stage[st]);
-        const int s_cur = (ci & 1) ? CT_S1 : CT_S0;
-        const int s_nxt = (ci & 1) ? CT_S0 : CT_S1;
-
-        // ---- D1 = S [W; Q~]^T
+        // ---- D1 = [W; Q~] Sb^T
         if (tid == 0) {
-            constexpr uint32_t id = tc::idesc_tf32(128, 128);
+            constexpr uint32_t id = tc::idesc_tf32(128, NR);
+            const uint32_t a0 = tc::smem_u32(sm.bw[b]), b0 = tc::smem_u32(sm.sb);
 #pragma unroll
             for (int ks = 0; ks < D / 8; ++ks)
-                tc::mma_tf32_ts(tm + CT_D1, tm + s_cur + 8 * ks, tc::desc_tf32_kstep(sb + IMG_BW, 128, ks), id,
+                tc::mma_tf32_ss(tm + CT_D1, tc::desc_tf32_kstep(a0, 128, ks), tc::desc_tf32_kstep(b0, NR, ks), id,
                                 ks > 0);
             tc::commit(&sm.mma);
-        }
-        // the next chunk's U'^T rows start loading while MMA 1 runs
-        float upn[C];
-        if (ci + 1 < nchunks) load_upt(ci + 1, upn);
-        // meanwhile: S_next = S diag(e^{gamma_C}), first half of the columns
-        // (MMA 1 only reads S); the second half overlaps the P product below
-        {
-            float a[2][16];
-#pragma unroll
-            for (int quarter = 0; quarter < 2; ++quarter) {
-#pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2)
-                    tc::ld16(tc::lane_addr(tm, warp, s_cur + 32 * quarter + 16 * q2), a[q2]);
-                tc::wait_ld();
-#pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) a[q2][j] *= sm.egc[st][32 * quarter + 16 * q2 + j];
-                    tc::st16(tc::lane_addr(tm, warp, s_nxt + 32 * quarter + 16 * q2), a[q2]);
-                }
+            // the other [W; Q~] buffer's last product (chunk ci - 1) has completed
+            if (ci + 1 < nchunks) {
+                issue_bw(ci + 1, b ^ 1);
+                last_bw[b ^ 1] = ci + 1;
             }
         }
+        if (tid < C && ci + 1 < nchunks) load_up(ci + 1, upn);
         ok = wait_mma(&sm.mma, mphase, p.err_flag);
         if (!ok) break;
-        // U^T = U'^T - S W^T
-        {
-            float a[2][16];
+        // ---- U = U' - W Sb^T (thread = token r = TMEM lane r)
+        if (tid < C) {
+            float d[2][16];
+            tc::ld16(tc::lane_addr(tm, warp, CT_D1), d[0]);
+            tc::ld16(tc::lane_addr(tm, warp, CT_D1 + 16), d[1]);
+            tc::wait_ld();
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-#pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) tc::ld16(tc::lane_addr(tm, warp, CT_D1 + 32 * half + 16 * q2), a[q2]);
-                tc::wait_ld();
-#pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) a[q2][j] = upt[32 * half + 16 * q2 + j] - a[q2][j];
-                    tc::st16(tc::lane_addr(tm, warp, CT_UT + 32 * half + 16 * q2), a[q2]);
-                }
-            }
-            tc::wait_st();
+            for (int i = 0; i < NR; ++i) st_sw(&sm.ub[0][0], NR, i, tid, upc[i] - d[i >> 4][i & 15]);
         }
-        sync_for_mma();
-        // ---- O^T += U^T P^T (needs no state) while the rest of S is decayed
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        // ---- D1[64:128] += P U and D3 = K^^T U
+        const bool pk = mbar_wait(&sm.full_pk, ci & 1);
+        if (__syncthreads_and(pk) == 0) {
+            if (tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
+            ok = false;
+            break;
+        }
+        tc::fence_after_sync();
         if (tid == 0) {
-            constexpr uint32_t id64 = tc::idesc_tf32(128, 64);
+            constexpr uint32_t id = tc::idesc_tf32(128, NR);
+            const uint32_t ap = tc::smem_u32(sm.p128), ak = tc::smem_u32(sm.kt), b0 = tc::smem_u32(sm.ub);
 #pragma unroll
-            for (int ks = 0; ks < C / 8; ++ks)
-                tc::mma_tf32_ts(tm + CT_D1 + 64, tm + CT_UT + 8 * ks, tc::desc_tf32_kstep(sb + IMG_P, 64, ks), id64,
-                                1);
-        }
-        {
-            float a[2][16];
-#pragma unroll
-            for (int quarter = 2; quarter < 4; ++quarter) {
-#pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2)
-                    tc::ld16(tc::lane_addr(tm, warp, s_cur + 32 * quarter + 16 * q2), a[q2]);
-                tc::wait_ld();
-#pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) a[q2][j] *= sm.egc[st][32 * quarter + 16 * q2 + j];
-                    tc::st16(tc::lane_addr(tm, warp, s_nxt + 32 * quarter + 16 * q2), a[q2]);
-                }
+            for (int ks = 0; ks < C / 8; ++ks) {
+                const uint64_t bd = tc::desc_tf32_kstep(b0, NR, ks);
+                tc::mma_tf32_ss(tm + CT_D1, tc::desc_tf32_kstep(ap, 128, ks), bd, id, 1);
+                tc::mma_tf32_ss(tm + CT_D3, tc::desc_tf32_kstep(ak, 128, ks), bd, id, ks > 0);
             }
-            tc::wait_st();
-        }
-        sync_for_mma();
-        // ---- S_next += U^T K^
-        if (tid == 0) {
-            constexpr uint32_t id128 = tc::idesc_tf32(128, 128);
-#pragma unroll
-            for (int ks = 0; ks < C / 8; ++ks)
-                tc::mma_tf32_ts(tm + s_nxt, tm + CT_UT + 8 * ks, tc::desc_tf32_kstep(sb + IMG_KT, 128, ks), id128,
-                                1);
             tc::commit(&sm.mma);
         }
         ok = wait_mma(&sm.mma, mphase, p.err_flag);
         if (!ok) break;
-        // O^T (lane = value row i, column = token r) goes out through the
-        // stage buffer this chunk no longer needs: transposed to [r][i] in
-        // shared memory, then written with 16-byte stores per token row
+        // P and K^^T are free, and the other e^{gamma_C} slot was last read by
+        // chunk ci - 1: bring in the next chunk's
+        if (tid == 0 && ci + 1 < nchunks) {
+            issue_pk(ci + 1);
+            last_pk = ci + 1;
+        }
+        // ---- Sb <- Sb diag(e^{gamma_C}) + D3^T (thread = channel c = TMEM
+        // lane c); token threads 64..127 also write O = scale D1[64:128]
         {
-            T *ot = reinterpret_cast<T *>(sm.stage[st]);  // [C][D]
-            const float scale = p.scale;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float o[2][16];
-#pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2) tc::ld16(tc::lane_addr(tm, warp, CT_D1 + 64 + 32 * half + 16 * q2), o[q2]);
-                tc::wait_ld();
-#pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2)
-#pragma unroll
-                    for (int rr = 0; rr < 16; ++rr)
-                        Elem<T>::store1(ot + (32 * half + 16 * q2 + rr) * D + tid, scale * o[q2][rr]);
+            float d[2][16];
+            tc::ld16(tc::lane_addr(tm, warp, CT_D3), d[0]);
+            tc::ld16(tc::lane_addr(tm, warp, CT_D3 + 16), d[1]);
+            float o[2][16];
+            if (tid >= C) {  // warp-uniform
+                tc::ld16(tc::lane_addr(tm, warp, CT_D1), o[0]);
+                tc::ld16(tc::lane_addr(tm, warp, CT_D1 + 16), o[1]);
             }
-            __syncthreads();
-            constexpr int V = 16 / sizeof(T);  // elements per 16-byte vector
-            for (int idx = tid; idx < C * D / V; idx += kThreads) {
-                const int r = idx / (D / V), i0 = (idx % (D / V)) * V;
-                if (r < L)
-                    *reinterpret_cast<uint4 *>(out + (t0 + r) * tok_stride + hoff + i0) =
-                        *reinterpret_cast<const uint4 *>(ot + r * D + i0);
+            tc::wait_ld();
+            const float e = sm.egc[b][tid];
+#pragma unroll
+            for (int i = 0; i < NR; ++i) {
+                float *sp = reinterpret_cast<float *>(&sm.sb[0][0] + tc::sw128_off(i, tid, NR));
+                *sp = fmaf(*sp, e, d[i >> 4][i & 15]);
+            }
+            if (tid >= C && tid - C < L) {
+                T *dst = out + (t0 + tid - C) * tok_stride + hoff;
+                constexpr int V = 16 / sizeof(T);  // elements per 16-byte store
+#pragma unroll
+                for (int v0 = 0; v0 < NR; v0 += V) {
+                    alignas(16) T pack[V];
+#pragma unroll
+                    for (int e2 = 0; e2 < V; ++e2) {
+                        float tmp = p.scale * o[(v0 + e2) >> 4][(v0 + e2) & 15];
+                        Elem<T>::store1(&pack[e2], tmp);
+                    }
+                    *reinterpret_cast<uint4 *>(dst + v0) = *reinterpret_cast<const uint4 *>(pack);
+                }
             }
         }
+        if (tid < C) {
 #pragma unroll
-        for (int j = 0; j < C; ++j) upt[j] = upn[j];
-        fence_proxy_async_smem();  // this stage's e^{gamma_C} reads before its next bulk refill
+            for (int j = 0; j < NR; ++j) upc[j] = upn[j];
+        }
+        fence_proxy_async_smem();  // Sb writes before the next product; e^{gamma_C} reads before its refill
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
     }
 
     if (ok) {
-        float s16[16];
-        const int s_fin = (nchunks & 1) ? CT_S1 : CT_S0;
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 16) {
-            tc::ld16(tc::lane_addr(tm, warp, s_fin + c0), s16);
-            tc::wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; j += 4)
-                *reinterpret_cast<float4 *>(Sg + (int64_t)tid * D + c0 + j) =
-                    make_float4(s16[j], s16[j + 1], s16[j + 2], s16[j + 3]);
+        for (int idx = tid; idx < NR * (D / 4); idx += kThreads) {
+            const int i = idx / (D / 4), c4 = (idx % (D / 4)) * 4;
+            *reinterpret_cast<float4 *>(Sg + (int64_t)i * D + c4) =
+                *reinterpret_cast<const float4 *>(&sm.sb[0][0] + tc::sw128_off(i, c4, NR));
         }
-    } else {
-        // bounded waits so that no MMA or bulk copy is still writing when the
-        // CTA releases its memory
-        mbar_wait(&sm.mma, (mphase ^ 1) & 1);
-        mbar_wait(&sm.full[0], 0);
-        mbar_wait(&sm.full[1], 0);
+    } else if (tid == 0) {
+        // bounded waits so that no product or bulk copy is still writing when
+        // the CTA releases its memory
+        mbar_wait(&sm.mma, mphase & 1);
+        for (int bb = 0; bb < 2; ++bb)
+            if (last_bw[bb] >= 0) mbar_wait(&sm.full_bw[bb], (last_bw[bb] >> 1) & 1);
+        if (last_pk >= 0) mbar_wait(&sm.full_pk, last_pk & 1);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -777,7 +766,8 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    chain_tc_kernel<__nv_bfloat16><<<dim3((unsigned)p.num_seqs, (unsigned)p.H), kThreads, kChainSmem, st>>>(p);
+    chain_tc_kernel<__nv_bfloat16>
+        <<<dim3((unsigned)p.num_seqs, (unsigned)p.H, (unsigned)kRowBlocks), kThreads, kChainSmem, st>>>(p);
     return cudaGetLastError();
 }
 
