@@ -67,6 +67,11 @@ __device__ __forceinline__ void bulk_s2g(void *dst_gmem, const void *src_smem, u
                  : "memory");
 }
 
+// Hint: bring `bytes` (a multiple of 16) at a 16-byte aligned global address into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src_gmem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Waits until the committed bulk stores have finished READING shared memory.

@@ -498,15 +498,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
 // N side, a chunk step is
 //   D1 = [W; Q~] Sb^T            M = 128 (token rows of W, then of Q~), N = NR, K = 128
 //   U = U' - D1[0:64]            thread = token r = TMEM lane r, into the swizzled U tile
-//   D1[64:128] += P U            A = P placed in rows 64..127 of a 128-row tile
 //   D3 = K^^T U                  M = 128 channels, N = NR, K = 64 tokens
+//   D1[64:128] += P U            A = P placed in rows 64..127 of a 128-row tile
 //   Sb <- Sb diag(e^{gamma_C}) + D3^T,   O = scale D1[64:128]
 // (the A operands come from the chunk's operand image; Sb and U are K-major
-// 128-byte-swizzled tiles in shared memory).
+// 128-byte-swizzled tiles in shared memory).  Only D1 -> U -> D3 -> Sb is on
+// the serial path: P U has its own completion barrier and D1 alternates
+// between two TMEM regions, so a chunk's output is written while the next
+// chunk's first product runs.
 constexpr int NR = 32;
 constexpr int kRowBlocks = D / NR;
-constexpr uint32_t CT_D1 = 0, CT_D3 = NR;
-constexpr uint32_t CT_COLS = 64;
+constexpr uint32_t CT_D1 = 0, CT_D3 = 2 * NR;  // D1 ping-pongs between columns 0 and NR
+constexpr uint32_t CT_COLS = 128;
 constexpr uint32_t kPKBytes = 2 * 8192 + 128 * 64 * 4 + D * 4;  // P, K^^T, e^{gamma_C}
 
 struct ChainSmem {
@@ -518,7 +521,7 @@ struct ChainSmem {
     float egc[2][D];
     uint64_t full_bw[2];
     uint64_t full_pk;
-    uint64_t mma;
+    uint64_t mma1, mma2, mma3;  // [W; Q~] Sb^T, P U, K^^T U done
     uint32_t tmem_base;
 };
 constexpr size_t kChainSmem = sizeof(ChainSmem) + 1024;
@@ -565,7 +568,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
         mbar_init(&sm.full_bw[0], 1);
         mbar_init(&sm.full_bw[1], 1);
         mbar_init(&sm.full_pk, 1);
-        mbar_init(&sm.mma, 1);
+        mbar_init(&sm.mma1, 1);
+        mbar_init(&sm.mma2, 1);
+        mbar_init(&sm.mma3, 1);
         fence_barrier_init();
         if (nchunks > 0) {
             issue_bw(0, 0);
@@ -590,9 +595,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
     tc::fence_after_sync();
     const uint32_t tm = sm.tmem_base;
 
-    uint32_t mphase = 0;
+    uint32_t ph1 = 0, ph2 = 0, ph3 = 0;
     bool ok = true;
-    int last_bw[2] = {nchunks > 0 ? 0 : -1, -1}, last_pk = nchunks > 0 ? 0 : -1;
+    int last_bw0 = nchunks > 0 ? 0 : -1, last_bw1 = -1, last_pk = nchunks > 0 ? 0 : -1;
     // this token thread's U' values for the block (threads 0..63), the next
     // chunk's in flight while the current one computes
     float upc[NR], upn[NR];
@@ -604,12 +609,32 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
             dst[4 * j] = x.x; dst[4 * j + 1] = x.y; dst[4 * j + 2] = x.z; dst[4 * j + 3] = x.w;
         }
     };
+    // O = scale D1[64:128] of chunk cj from the D1 region at column col
+    // (token threads 64..127; warp-uniform)
+    auto write_output = [&](int cj, uint32_t col) {
+        const int64_t tj = (int64_t)cs + (int64_t)cj * C;
+        const int Lj = (int)((int64_t)ce - tj < C ? (int64_t)ce - tj : C);
+        float o[2][16];
+        tc::ld16(tc::lane_addr(tm, warp, col), o[0]);
+        tc::ld16(tc::lane_addr(tm, warp, col + 16), o[1]);
+        tc::wait_ld();
+        if (tid - C < Lj) {
+            T *dst = out + (tj + tid - C) * tok_stride + hoff;
+            constexpr int V = 16 / sizeof(T);  // elements per 16-byte store
+#pragma unroll
+            for (int v0 = 0; v0 < NR; v0 += V) {
+                alignas(16) T pack[V];
+#pragma unroll
+                for (int e2 = 0; e2 < V; ++e2) Elem<T>::store1(&pack[e2], p.scale * o[(v0 + e2) >> 4][(v0 + e2) & 15]);
+                *reinterpret_cast<uint4 *>(dst + v0) = *reinterpret_cast<const uint4 *>(pack);
+            }
+        }
+    };
     if (tid < C && nchunks > 0) load_up(0, upc);
 
     for (int ci = 0; ci < nchunks; ++ci) {
         const int b = ci & 1;
-        const int64_t t0 = (int64_t)cs + (int64_t)ci * C;
-        const int L = (int)((int64_t)ce - t0 < C ? (int64_t)ce - t0 : C);
+        const uint32_t d1 = CT_D1 + b * NR;
         const bool landed = mbar_wait(&sm.full_bw[b], (ci >> 1) & 1);
         if (__syncthreads_and(landed) == 0) {
             if (tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
@@ -623,23 +648,27 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
             const uint32_t a0 = tc::smem_u32(sm.bw[b]), b0 = tc::smem_u32(sm.sb);
 #pragma unroll
             for (int ks = 0; ks < D / 8; ++ks)
-                tc::mma_tf32_ss(tm + CT_D1, tc::desc_tf32_kstep(a0, 128, ks), tc::desc_tf32_kstep(b0, NR, ks), id,
+                tc::mma_tf32_ss(tm + d1, tc::desc_tf32_kstep(a0, 128, ks), tc::desc_tf32_kstep(b0, NR, ks), id,
                                 ks > 0);
-            tc::commit(&sm.mma);
+            tc::commit(&sm.mma1);
             // the other [W; Q~] buffer's last product (chunk ci - 1) has completed
             if (ci + 1 < nchunks) {
                 issue_bw(ci + 1, b ^ 1);
-                last_bw[b ^ 1] = ci + 1;
+                if (b) last_bw0 = ci + 1; else last_bw1 = ci + 1;
+                // the next chunk's P, K^^T and e^{gamma_C} towards L2 ahead of their copy
+                bulk_prefetch_l2(image(ci + 1) + IMG_P, IMG_EGC + D * 4 - IMG_P);
             }
         }
+        // the previous chunk's output goes out while this chunk's first product runs
+        if (ci > 0 && tid >= C) write_output(ci - 1, CT_D1 + (b ^ 1) * NR);
         if (tid < C && ci + 1 < nchunks) load_up(ci + 1, upn);
-        ok = wait_mma(&sm.mma, mphase, p.err_flag);
+        ok = wait_mma(&sm.mma1, ph1, p.err_flag);
         if (!ok) break;
         // ---- U = U' - W Sb^T (thread = token r = TMEM lane r)
         if (tid < C) {
             float d[2][16];
-            tc::ld16(tc::lane_addr(tm, warp, CT_D1), d[0]);
-            tc::ld16(tc::lane_addr(tm, warp, CT_D1 + 16), d[1]);
+            tc::ld16(tc::lane_addr(tm, warp, d1), d[0]);
+            tc::ld16(tc::lane_addr(tm, warp, d1 + 16), d[1]);
             tc::wait_ld();
 #pragma unroll
             for (int i = 0; i < NR; ++i) st_sw(&sm.ub[0][0], NR, i, tid, upc[i] - d[i >> 4][i & 15]);
@@ -648,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
-        // ---- D1[64:128] += P U and D3 = K^^T U
+        // ---- D3 = K^^T U (serial path), then D1[64:128] += P U
         const bool pk = mbar_wait(&sm.full_pk, ci & 1);
         if (__syncthreads_and(pk) == 0) {
             if (tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
@@ -660,32 +689,22 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
             constexpr uint32_t id = tc::idesc_tf32(128, NR);
             const uint32_t ap = tc::smem_u32(sm.p128), ak = tc::smem_u32(sm.kt), b0 = tc::smem_u32(sm.ub);
 #pragma unroll
-            for (int ks = 0; ks < C / 8; ++ks) {
-                const uint64_t bd = tc::desc_tf32_kstep(b0, NR, ks);
-                tc::mma_tf32_ss(tm + CT_D1, tc::desc_tf32_kstep(ap, 128, ks), bd, id, 1);
-                tc::mma_tf32_ss(tm + CT_D3, tc::desc_tf32_kstep(ak, 128, ks), bd, id, ks > 0);
-            }
-            tc::commit(&sm.mma);
+            for (int ks = 0; ks < C / 8; ++ks)
+                tc::mma_tf32_ss(tm + CT_D3, tc::desc_tf32_kstep(ak, 128, ks), tc::desc_tf32_kstep(b0, NR, ks), id,
+                                ks > 0);
+            tc::commit(&sm.mma3);
+#pragma unroll
+            for (int ks = 0; ks < C / 8; ++ks)
+                tc::mma_tf32_ss(tm + d1, tc::desc_tf32_kstep(ap, 128, ks), tc::desc_tf32_kstep(b0, NR, ks), id, 1);
+            tc::commit(&sm.mma2);
         }
-        ok = wait_mma(&sm.mma, mphase, p.err_flag);
+        ok = wait_mma(&sm.mma3, ph3, p.err_flag);
         if (!ok) break;
-        // P and K^^T are free, and the other e^{gamma_C} slot was last read by
-        // chunk ci - 1: bring in the next chunk's
-        if (tid == 0 && ci + 1 < nchunks) {
-            issue_pk(ci + 1);
-            last_pk = ci + 1;
-        }
-        // ---- Sb <- Sb diag(e^{gamma_C}) + D3^T (thread = channel c = TMEM
-        // lane c); token threads 64..127 also write O = scale D1[64:128]
+        // ---- Sb <- Sb diag(e^{gamma_C}) + D3^T (thread = channel c = TMEM lane c)
         {
             float d[2][16];
             tc::ld16(tc::lane_addr(tm, warp, CT_D3), d[0]);
             tc::ld16(tc::lane_addr(tm, warp, CT_D3 + 16), d[1]);
-            float o[2][16];
-            if (tid >= C) {  // warp-uniform
-                tc::ld16(tc::lane_addr(tm, warp, CT_D1), o[0]);
-                tc::ld16(tc::lane_addr(tm, warp, CT_D1 + 16), o[1]);
-            }
             tc::wait_ld();
             const float e = sm.egc[b][tid];
 #pragma unroll
@@ -693,30 +712,25 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
                 float *sp = reinterpret_cast<float *>(&sm.sb[0][0] + tc::sw128_off(i, tid, NR));
                 *sp = fmaf(*sp, e, d[i >> 4][i & 15]);
             }
-            if (tid >= C && tid - C < L) {
-                T *dst = out + (t0 + tid - C) * tok_stride + hoff;
-                constexpr int V = 16 / sizeof(T);  // elements per 16-byte store
-#pragma unroll
-                for (int v0 = 0; v0 < NR; v0 += V) {
-                    alignas(16) T pack[V];
-#pragma unroll
-                    for (int e2 = 0; e2 < V; ++e2) {
-                        float tmp = p.scale * o[(v0 + e2) >> 4][(v0 + e2) & 15];
-                        Elem<T>::store1(&pack[e2], tmp);
-                    }
-                    *reinterpret_cast<uint4 *>(dst + v0) = *reinterpret_cast<const uint4 *>(pack);
-                }
-            }
         }
         if (tid < C) {
 #pragma unroll
             for (int j = 0; j < NR; ++j) upc[j] = upn[j];
+        }
+        // P U is done (it ran during the update): P and K^^T are free, and the
+        // other e^{gamma_C} slot was last read by chunk ci - 1
+        ok = wait_mma(&sm.mma2, ph2, p.err_flag);
+        if (!ok) break;
+        if (tid == 0 && ci + 1 < nchunks) {
+            issue_pk(ci + 1);
+            last_pk = ci + 1;
         }
         fence_proxy_async_smem();  // Sb writes before the next product; e^{gamma_C} reads before its refill
         tc::fence_before_sync();
         __syncthreads();
         tc::fence_after_sync();
     }
+    if (ok && nchunks > 0 && tid >= C) write_output(nchunks - 1, CT_D1 + ((nchunks - 1) & 1) * NR);
 
     if (ok) {
         for (int idx = tid; idx < NR * (D / 4); idx += kThreads) {
@@ -727,9 +741,11 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
     } else if (tid == 0) {
         // bounded waits so that no product or bulk copy is still writing when
         // the CTA releases its memory
-        mbar_wait(&sm.mma, mphase & 1);
-        for (int bb = 0; bb < 2; ++bb)
-            if (last_bw[bb] >= 0) mbar_wait(&sm.full_bw[bb], (last_bw[bb] >> 1) & 1);
+        mbar_wait(&sm.mma1, ph1 & 1);
+        mbar_wait(&sm.mma2, ph2 & 1);
+        mbar_wait(&sm.mma3, ph3 & 1);
+        if (last_bw0 >= 0) mbar_wait(&sm.full_bw[0], (last_bw0 >> 1) & 1);
+        if (last_bw1 >= 0) mbar_wait(&sm.full_bw[1], (last_bw1 >> 1) & 1);
         if (last_pk >= 0) mbar_wait(&sm.full_pk, last_pk & 1);
     }
     tc::fence_before_sync();
