@@ -268,26 +268,43 @@ def run_decode(args, world, rank, kda, peaks, sampler):
                 "peak_source": f"{peaks['source']} hbm_gbs (copy)",
                 "avg_kernel_us": round(avg_kernel_s * 1e6, 2)}
 
-    # e2e: host buffers through the same C ABI entry point
+    # e2e: host buffers through the same C ABI entry point.  As in a serving
+    # loop, step i+1's inputs are uploaded and step i-1's outputs read back on
+    # copy streams while step i computes (two device buffer sets).
     pinned = {}
     for name in ("q", "k", "v", "g", "b"):
         pinned[name] = [getattr(bt, name).cpu().pin_memory() for bt in batches]
     pinned["slots"] = [s.cpu().pin_memory() for s in slot_sets]
-    dev_in = {n: torch.empty_like(getattr(batches[0], n)) for n in ("q", "k", "v", "g", "b")}
-    dev_slots = torch.empty_like(slot_sets[0])
-    host_out = torch.empty((B, H, w["dv"]), dtype=torch.bfloat16).pin_memory()
+    NB = 2
+    dev_in = [{n: torch.empty_like(getattr(batches[0], n)) for n in ("q", "k", "v", "g", "b")} for _ in range(NB)]
+    dev_slots = [torch.empty_like(slot_sets[0]) for _ in range(NB)]
+    dev_out = [torch.empty((B, H, w["dv"]), dtype=torch.bfloat16, device="cuda") for _ in range(NB)]
+    host_out = [torch.empty((B, H, w["dv"]), dtype=torch.bfloat16).pin_memory() for _ in range(NB)]
     h2d = sum(pinned[n][0].numel() * pinned[n][0].element_size() for n in ("q", "k", "v", "g", "b"))
     h2d += pinned["slots"][0].numel() * 4
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = host_out[0].numel() * host_out[0].element_size()
+    up_s, down_s = torch.cuda.Stream(), torch.cuda.Stream()
+    up_done = [torch.cuda.Event() for _ in range(NB)]
+    comp_done = [torch.cuda.Event() for _ in range(NB)]
+    down_done = [torch.cuda.Event() for _ in range(NB)]
 
     def e2e_step(i):
-        j = i % len(batches)
-        for n in ("q", "k", "v", "g", "b"):
-            dev_in[n].copy_(pinned[n][j], non_blocking=True)
-        dev_slots.copy_(pinned["slots"][i % len(slot_sets)], non_blocking=True)
-        kda.decode(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["b"],
-                   dev_slots, pool, outs)
-        host_out.copy_(outs, non_blocking=True)
+        j, bi = i % NB, i % len(batches)
+        up_s.wait_event(comp_done[j])  # buffer set j: step i - NB has consumed it
+        with torch.cuda.stream(up_s):
+            for n in ("q", "k", "v", "g", "b"):
+                dev_in[j][n].copy_(pinned[n][bi], non_blocking=True)
+            dev_slots[j].copy_(pinned["slots"][i % len(slot_sets)], non_blocking=True)
+        up_done[j].record(up_s)
+        stream.wait_event(up_done[j])
+        stream.wait_event(down_done[j])  # output buffer j has been read back
+        kda.decode(dev_in[j]["q"], dev_in[j]["k"], dev_in[j]["v"], dev_in[j]["g"], dev_in[j]["b"],
+                   dev_slots[j], pool, dev_out[j], stream=stream)
+        comp_done[j].record(stream)
+        down_s.wait_event(comp_done[j])
+        with torch.cuda.stream(down_s):
+            host_out[j].copy_(dev_out[j], non_blocking=True)
+        down_done[j].record(down_s)
 
     n_e2e = max(3, min(args.steps, 200))
     for i in range(3):
@@ -297,14 +314,43 @@ def run_decode(args, world, rank, kda, peaks, sampler):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    up_s.wait_event(e0)
     for i in range(n_e2e):
         e2e_step(i)
+    for j in range(NB):
+        stream.wait_event(down_done[j])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world)
     e2e_value = sum_over_ranks(units * n_e2e, world) / (e2e_ms * n_e2e / 1e3)
+
+    # the same steps with copy, kernel and read-back in order on one stream
+    def serial_step(i):
+        bi = i % len(batches)
+        for n in ("q", "k", "v", "g", "b"):
+            dev_in[0][n].copy_(pinned[n][bi], non_blocking=True)
+        dev_slots[0].copy_(pinned["slots"][i % len(slot_sets)], non_blocking=True)
+        kda.decode(dev_in[0]["q"], dev_in[0]["k"], dev_in[0]["v"], dev_in[0]["g"], dev_in[0]["b"],
+                   dev_slots[0], pool, dev_out[0], stream=stream)
+        host_out[0].copy_(dev_out[0], non_blocking=True)
+
+    for i in range(3):
+        serial_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0.record(stream)
+    for i in range(n_e2e):
+        serial_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    serial_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world)
+    serial_value = sum_over_ranks(units * n_e2e, world) / (serial_ms * n_e2e / 1e3)
     e2e = {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-           "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4), "steps": n_e2e}
+           "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4), "steps": n_e2e,
+           "copies": "pinned host buffers; uploads and read-backs on two copy streams, "
+                     "overlapping the neighbouring steps' kernels (two device buffer sets)",
+           "serial": {"value": round(serial_value, 1), "ms_per_step": round(serial_ms, 4),
+                      "copies": "upload, kernel and read-back in order on one stream"}}
     del pool
     return dict(value=value, ms_per_step=ms_per_step, roofline=roofline, e2e=e2e,
                 launches=args.steps, kernel_us=avg_kernel_s * 1e6)
