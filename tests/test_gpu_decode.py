@@ -132,3 +132,24 @@ def test_decode_full_size_sampled():
     touched = torch.zeros(NS, dtype=torch.bool, device="cuda")
     touched[x.slot_ids.long()] = True
     assert torch.equal(x.pool[~touched], pool_before[~touched])
+
+
+def test_decode_rows_per_cta_do_not_change_bits():
+    """The launcher picks 64, 32 or 16 state rows per CTA from the grid size;
+    the same tokens decoded as one large batch (64 rows per CTA) and as small
+    slices (fewer rows per CTA) give the same bits."""
+    kda = _kda()
+    B, H, dk, dv, NS = 192, 8, 128, 128, 256
+    x = inputs.decode_inputs(B, H, dk, dv, dtype="bf16", num_slots=NS, seed=23)
+    args = [t.cuda() for t in (x.q, x.k, x.v, x.g, x.b)]
+    slots = x.slot_ids.cuda()
+    p_big = x.pool.cuda()
+    o_big = kda.decode(*args, slots, p_big)
+    p_small = x.pool.cuda()
+    outs = []
+    for s0 in range(0, B, 3):
+        sl = slice(s0, min(s0 + 3, B))
+        outs.append(kda.decode(*[a[sl].contiguous() for a in args], slots[sl].contiguous(), p_small))
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat(outs), o_big)
+    assert torch.equal(p_small, p_big)
