@@ -178,10 +178,33 @@ __global__ void __launch_bounds__(kSpecWarps * 32) replay_kernel(const ReplayPar
         store_lane_vec<DK>(sm.al[gid], l, tc.alpha);
         if (l == 0) sm.beta[gid] = tc.beta;
     }
-    for (int idx = threadIdx.x; idx < a * ROWS; idx += kSpecWarps * 32) {
-        const int j = idx / ROWS, r = idx % ROWS;
-        const int64_t tk = ((int64_t)n * p.D + j) * p.H + h;
-        sm.v[j][r] = Elem<T>::load1(static_cast<const T *>(p.rec_v) + tk * p.dv + blk * ROWS + r);
+    // this tile's value records in 16-byte vectors, at most two per thread
+    // (D <= 16, 4-byte elements), all in flight at once
+    {
+        constexpr int E = 16 / sizeof(T);
+        constexpr int VPT = ROWS / E;  // vectors per token
+        const int total = a * VPT;
+        uint4 vbuf[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int idx = threadIdx.x + u * kSpecWarps * 32;
+            if (idx < total) {
+                const int j = idx / VPT, c = (idx % VPT) * E;
+                const int64_t tk = ((int64_t)n * p.D + j) * p.H + h;
+                vbuf[u] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const T *>(p.rec_v) + tk * p.dv +
+                                                                blk * ROWS + c));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int idx = threadIdx.x + u * kSpecWarps * 32;
+            if (idx < total) {
+                const int j = idx / VPT, c = (idx % VPT) * E;
+                const T *e = reinterpret_cast<const T *>(&vbuf[u]);
+#pragma unroll
+                for (int i = 0; i < E; ++i) sm.v[j][c + i] = Elem<T>::to_f(e[i]);
+            }
+        }
     }
     __syncthreads();
 
