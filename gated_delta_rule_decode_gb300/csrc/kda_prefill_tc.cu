@@ -129,7 +129,7 @@ struct PrepSmem {
     float ref[D];         // gamma at token 31
     float gC[D];          // gamma at the chunk's last token
     float egcref[D];      // e^{gamma_C - ref}
-    float xs[3][16][17];  // off-diagonal partial products of the UT inverse
+    float xs[32][33];     // partial products of the UT inverse
     uint64_t bar;
     uint32_t tmem_base;
 };
@@ -394,10 +394,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
     __syncthreads();
 
     if (ok) {
-        // ---- 4. T = (I + A)^-1 (unit lower triangular), blocked by 16:
-        // the four diagonal blocks by forward substitution (one column per
-        // thread, in registers), then the blocks below the diagonal in order of
-        // distance d: X = sum_{K=J}^{I-1} A_IK T_KJ, T_IJ = -T_II X.
+        // ---- 4. T = (I + A)^-1 (unit lower triangular) by doubling: the four
+        // 16 x 16 diagonal blocks by forward substitution (one column per
+        // thread, in registers); then the lower-left 16 x 16 block of each
+        // 32-row block as -T22 (A21 T11); then the lower-left 32 x 32 block of
+        // the whole matrix the same way.
+        float(*As)[C + 1] = sm.inv.As;
+        float(*Ts)[C + 1] = sm.inv.Ts;
         if (tid < C) {
             const int I = tid >> 4, jj = tid & 15, o = 16 * I;
             float col[16];
@@ -406,48 +409,63 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                 float acc2 = (r == jj) ? 1.f : 0.f;
 #pragma unroll
                 for (int m = 0; m < r; ++m)
-                    if (m >= jj) acc2 = fmaf(-sm.inv.As[o + r][o + m], col[m], acc2);
+                    if (m >= jj) acc2 = fmaf(-As[o + r][o + m], col[m], acc2);
                 col[r] = (r >= jj) ? acc2 : 0.f;
             }
 #pragma unroll
-            for (int r = 0; r < 16; ++r) sm.inv.Ts[o + r][o + jj] = col[r];
+            for (int r = 0; r < 16; ++r) Ts[o + r][o + jj] = col[r];
         } else {
             // zero the blocks above the diagonal
             for (int idx = tid - C; idx < C * C; idx += kPrepThreads - C) {
                 const int r = idx / C, j = idx % C;
-                if ((j >> 4) > (r >> 4)) sm.inv.Ts[r][j] = 0.f;
+                if ((j >> 4) > (r >> 4)) Ts[r][j] = 0.f;
             }
         }
         __syncthreads();
-#pragma unroll 1
-        for (int d = 1; d < 4; ++d) {
-            const int nb = 4 - d;
-#pragma unroll 1
-            for (int idx = tid; idx < nb * 256; idx += kPrepThreads) {
-                const int J = idx >> 8, I = J + d, r = (idx >> 4) & 15, jj = idx & 15;
-                float x0 = 0.f, x1 = 0.f;
-#pragma unroll 1
-                for (int K = J; K < I; ++K) {
+        // level 1: both 32-row blocks at once (o = 0, 32)
+        for (int idx = tid; idx < 2 * 256; idx += kPrepThreads) {
+            const int o = 32 * (idx >> 8), r = (idx >> 4) & 15, j = idx & 15;
+            float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-                    for (int kk = 0; kk < 16; kk += 2) {
-                        x0 = fmaf(sm.inv.As[16 * I + r][16 * K + kk], sm.inv.Ts[16 * K + kk][16 * J + jj], x0);
-                        x1 = fmaf(sm.inv.As[16 * I + r][16 * K + kk + 1], sm.inv.Ts[16 * K + kk + 1][16 * J + jj], x1);
-                    }
-                }
-                sm.xs[J][r][jj] = x0 + x1;
+            for (int k = 0; k < 16; k += 2) {
+                x0 = fmaf(As[o + 16 + r][o + k], Ts[o + k][o + j], x0);
+                x1 = fmaf(As[o + 16 + r][o + k + 1], Ts[o + k + 1][o + j], x1);
             }
-            __syncthreads();
-#pragma unroll 1
-            for (int idx = tid; idx < nb * 256; idx += kPrepThreads) {
-                const int J = idx >> 8, I = J + d, r = (idx >> 4) & 15, jj = idx & 15;
-                float t = 0.f;
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    if (m <= r) t = fmaf(sm.inv.Ts[16 * I + r][16 * I + m], sm.xs[J][m][jj], t);
-                sm.inv.Ts[16 * I + r][16 * J + jj] = -t;
-            }
-            __syncthreads();
+            sm.xs[(idx >> 8) * 16 + r][j] = x0 + x1;
         }
+        __syncthreads();
+        for (int idx = tid; idx < 2 * 256; idx += kPrepThreads) {
+            const int o = 32 * (idx >> 8), r = (idx >> 4) & 15, j = idx & 15;
+            float t = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m)
+                if (m <= r) t = fmaf(Ts[o + 16 + r][o + 16 + m], sm.xs[(idx >> 8) * 16 + m][j], t);
+            Ts[o + 16 + r][o + j] = -t;
+        }
+        __syncthreads();
+        // level 2: the 32 x 32 blocks
+        for (int idx = tid; idx < 32 * 32; idx += kPrepThreads) {
+            const int r = idx >> 5, j = idx & 31;
+            float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+                x0 = fmaf(As[32 + r][k], Ts[k][j], x0);
+                x1 = fmaf(As[32 + r][k + 1], Ts[k + 1][j], x1);
+            }
+            sm.xs[r][j] = x0 + x1;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < 32 * 32; idx += kPrepThreads) {
+            const int r = idx >> 5, j = idx & 31;
+            float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < 32; m += 2) {
+                if (m <= r) t0 = fmaf(Ts[32 + r][32 + m], sm.xs[m][j], t0);
+                if (m + 1 <= r) t1 = fmaf(Ts[32 + r][32 + m + 1], sm.xs[m + 1][j], t1);
+            }
+            Ts[32 + r][j] = -(t0 + t1);
+        }
+        __syncthreads();
         for (int idx = tid; idx < C * C / 4; idx += kPrepThreads) {
             const int r = idx / (C / 4), j = (idx % (C / 4)) * 4;
             *reinterpret_cast<float4 *>(sm.bufT + tc::sw128_off(r, j, 64)) =
