@@ -153,3 +153,60 @@ def test_decode_rows_per_cta_do_not_change_bits():
     torch.cuda.synchronize()
     assert torch.equal(torch.cat(outs), o_big)
     assert torch.equal(p_small, p_big)
+
+
+def test_decode_full_size_1024x64_pool16384_sampled():
+    """The long-context mix's decode batch: 1024 sequences x 64 heads over a
+    16384-slot pool (64 GiB of state, so slot offsets run far past 2^32
+    bytes).  Sampled sequences, including the highest slots, against the
+    oracle; untouched slots bit-exact on a sample."""
+    kda = _kda()
+    B, H, dk, dv, NS = 1024, 64, 128, 128, 16384
+    x = inputs.decode_inputs(B, H, dk, dv, dtype="bf16", num_slots=NS, seed=11, g_mean=3.0,
+                             pool_std=0.02, device="cuda")
+    order = torch.argsort(x.slot_ids.cpu())
+    sample_n = torch.cat([order[-3:], order[:2], torch.tensor([5, 500, 1000])]).unique()
+    sample_slots = x.slot_ids.cpu()[sample_n].long()
+    before = x.pool[sample_slots.cuda()].cpu()
+    touched = torch.zeros(NS, dtype=torch.bool)
+    touched[x.slot_ids.cpu().long()] = True
+    probe = torch.nonzero(~touched).flatten()[-4:]  # untouched slots near the top of the pool
+    probe_before = x.pool[probe.cuda()].cpu()
+    flag = err_flag()
+    out = kda.decode(x.q, x.k, x.v, x.g, x.b, x.slot_ids, x.pool, err_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    sn = sample_n
+    o_ref, p_ref, e = oracle.decode(x.q.cpu()[sn], x.k.cpu()[sn], x.v.cpu()[sn], x.g.cpu()[sn],
+                                    x.b.cpu()[sn], torch.arange(len(sn), dtype=torch.int32), before)
+    atol, rtol = tol_for(torch.bfloat16)
+    assert_close(to_np64(out.cpu()[sn]), round_to(o_ref, torch.bfloat16), atol, rtol, "outputs")
+    assert_close(to_np64(x.pool[sample_slots.cuda()].cpu()), p_ref, atol, rtol, "states")
+    assert torch.equal(x.pool[probe.cuda()].cpu(), probe_before)
+
+
+def test_decode_in_cuda_graph_equals_eager():
+    """Decode steps captured in a CUDA graph (as the long-context mix runs
+    them) give the same bits as the same calls issued eagerly."""
+    kda = _kda()
+    H, steps = 32, 16
+    x = inputs.decode_inputs(1, H, 128, 128, dtype="bf16", num_slots=1, seed=7, device="cuda",
+                             tokens=steps, zero_state=False)
+    slots = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pool_e = x.pool.clone()
+    out_e = torch.empty((steps, 1, H, 128), dtype=torch.bfloat16, device="cuda")
+    for t in range(steps):
+        kda.decode(x.q[t], x.k[t], x.v[t], x.g[t], x.b[t], slots, pool_e, out_e[t])
+    pool_g = x.pool.clone()
+    out_g = torch.empty_like(out_e)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        for t in range(steps):
+            kda.decode(x.q[t], x.k[t], x.v[t], x.g[t], x.b[t], slots, pool_g, out_g[t], stream=s)
+    pool_g.copy_(x.pool)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out_g, out_e)
+    assert torch.equal(pool_g, pool_e)
