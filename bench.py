@@ -41,7 +41,7 @@ METRIC = "KDA decode token-heads/s + HBM GB/s vs peak; chunked-prefill tokens/s"
 UNIT = "token-heads/s"
 L2_BYTES = 129 * 1024 * 1024
 
-# Algorithmic bytes per unit (token-head for decode; see DESIGN.md):
+# Algorithmic bytes per unit (token-head for decode):
 #   decode: state read + write 2 * dv * dk * 4, q/k/v 3 * d * 2 (bf16),
 #           g dk * 4, b 2, out dv * 2
 DECODE_BYTES_PER_TH = 2 * 128 * 128 * 4 + 3 * 128 * 2 + 128 * 4 + 2 + 128 * 2  # 132610
