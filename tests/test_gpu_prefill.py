@@ -66,6 +66,29 @@ def test_prefill_padding_and_bad_slot():
     assert_close(to_np64(pool), p_ref, atol, rtol, "states")
 
 
+def test_prefill_tensor_core_path_padding_and_bad_slot():
+    """The same slot rules on the tensor-core path (bf16, dk = dv = 128):
+    padding and out-of-range sequences get zero outputs and leave the pool
+    alone; the others match the oracle."""
+    kda = _kda()
+    x = inputs.prefill_inputs([130, 64, 70, 1], 2, 128, 128, dtype="bf16", num_slots=5, seed=12,
+                              zero_state=False)
+    x.slot_ids = torch.tensor([3, -1, 7, 0], dtype=torch.int32)   # ok, padding, out of range, ok
+    flag = err_flag()
+    pool_before = x.pool.clone()
+    out, pool = _run(kda, x, init=True, flag=flag)
+    assert flag.item() == kda.KDA_DEVERR_SLOT
+    o_ref, p_ref, e = oracle.prefill(x.q, x.k, x.v, x.g, x.b, x.cu_seqlens, x.slot_ids, x.pool,
+                                     init_from_pool=True)
+    assert e == 2  # one per head of the out-of-range sequence
+    atol, rtol = tol_for(torch.bfloat16)
+    assert torch.all(out[130:194] == 0) and torch.all(out[194:264] == 0)
+    assert_close(to_np64(out), round_to(o_ref, torch.bfloat16), atol, rtol, "outputs")
+    assert_close(to_np64(pool), p_ref, atol, rtol, "states")
+    for sl in (1, 2, 4):
+        assert torch.equal(pool[sl].cpu(), pool_before[sl])
+
+
 def test_prefill_bad_seqlens_and_workspace():
     kda = _kda()
     x = inputs.prefill_inputs([40, 40], 1, 32, 32, dtype="bf16", num_slots=2, seed=5)
