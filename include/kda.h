@@ -133,11 +133,15 @@ KDA_API int kda_decode(const kda_dims *dims, int32_t batch, const void *q,
 
 /*
  * kda_verify_record: ReplaySSM verification of `draft_len` (1..16) draft
- * tokens per sequence.  Runs the recurrence over the draft tokens in order
- * starting from the committed state of (slot_ids[n], h) WITHOUT writing the
- * pool, emits the output of every draft token, and stores only the update
+ * tokens per sequence.  Evaluates the recurrence over the draft tokens,
+ * starting from the committed state of (slot_ids[n], h), WITHOUT writing the
+ * pool; emits the output of every draft token and stores only the update
  * records (kda_records) instead of per-token states ("2.8x faster Kimi K3
- * inference on CANN", section 04 "ReplaySSM").
+ * inference on CANN", section 04 "ReplaySSM").  The outputs are computed
+ * from the window's chunk form, so they equal those of draft_len sequential
+ * kda_decode calls up to rounding (not bit for bit); the records are the
+ * decode routine's own coefficients, so committing them reproduces decode
+ * bit for bit.
  *
  *   q, k     dtype  [batch][draft_len][H][dk]
  *   v        dtype  [batch][draft_len][H][dv]
