@@ -387,7 +387,10 @@ def run_spec(kda, peaks):
     rec = kda.alloc_records(B, D, H, dk, dv, torch.bfloat16, "cuda")
     acc = x.num_accepted
     n = 30
-    vcalls = [kda.verify_record(x.q, x.k, x.v, x.g, x.b, ss, x.pool, out, rec, _prepare=True)
+    vws_bytes = kda.verify_workspace_bytes(H, dk, dv, kda.KDA_DT_BF16, B, D)
+    vws = torch.empty(max(vws_bytes, 1), dtype=torch.uint8, device="cuda")
+    vcalls = [kda.verify_record(x.q, x.k, x.v, x.g, x.b, ss, x.pool, out, rec, workspace=vws,
+                                _prepare=True)
               for ss in sets]
     tv = time_launches(lambda i: vcalls[i % len(sets)](), n)
     kda.verify_record(x.q, x.k, x.v, x.g, x.b, x.slot_ids, x.pool, out, rec)
@@ -407,7 +410,8 @@ def run_spec(kda, peaks):
         "commit": {"us": round(ct * 1e6, 2), "GB/s": round(cbytes / ct / 1e9, 1),
                    "frac_hbm": round(cbytes / ct / 1e9 / peaks["hbm_gbs"], 4),
                    "algorithmic_bytes": cbytes, "mean_accepted": round(sum(a_list) / B, 3)},
-        "launches": 2 * n,
+        "verify_workspace_bytes": vws_bytes,
+        "launches": 3 * n,  # verify: window + state kernels; commit: replay kernel
     }
 
 

@@ -84,10 +84,16 @@ int kda_decode(const kda_dims *dims, int32_t batch, const void *q, const void *k
     return from_cuda(kda::launch_decode(p, dims->dk, dims->dtype, (cudaStream_t)stream));
 }
 
+size_t kda_verify_workspace_bytes(const kda_dims *dims, int32_t batch, int32_t draft_len) {
+    if (check_dims(dims) != KDA_OK || batch < 0 || draft_len < 1 || draft_len > 16) return 0;
+    return kda::verify_workspace_bytes(dims->num_heads, dims->dk, dims->dv, dims->dtype, batch, draft_len);
+}
+
 int kda_verify_record(const kda_dims *dims, int32_t batch, int32_t draft_len, const void *q,
                       const void *k, const void *v, const float *g, const void *b,
                       const int32_t *slot_ids, const float *pool, int64_t num_slots, void *out,
-                      const kda_records *rec, int32_t *err_flag, void *stream) {
+                      const kda_records *rec, void *workspace, size_t workspace_bytes,
+                      int32_t *err_flag, void *stream) {
     int st = check_dims(dims);
     if (st != KDA_OK) return st;
     if (batch < 0 || num_slots < 0 || draft_len < 1 || draft_len > 16) return KDA_ERR_INVALID_ARG;
@@ -97,8 +103,14 @@ int kda_verify_record(const kda_dims *dims, int32_t batch, int32_t draft_len, co
         slot_ids == nullptr || rec->beta == nullptr)
         return KDA_ERR_INVALID_ARG;
     if (num_slots > 0 && !all_aligned({pool})) return KDA_ERR_INVALID_ARG;
+    const size_t need = kda::verify_workspace_bytes(dims->num_heads, dims->dk, dims->dv, dims->dtype,
+                                                    batch, draft_len);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return KDA_ERR_WORKSPACE;
     kda::VerifyParams p{};
     p.q = q; p.k = k; p.v = v; p.g = g; p.b = b;
+    p.workspace = need > 0 ? workspace : nullptr;
     p.slot_ids = slot_ids; p.pool = pool; p.num_slots = num_slots; p.out = out;
     p.rec_k_hat = rec->k_hat; p.rec_v = rec->v; p.rec_g = rec->g; p.rec_beta = rec->beta;
     p.err_flag = err_flag;

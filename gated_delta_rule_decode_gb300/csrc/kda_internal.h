@@ -33,6 +33,7 @@ struct VerifyParams {
     void *rec_v;
     float *rec_g;
     float *rec_beta;
+    void *workspace;  // scratch of verify_workspace_bytes(...) bytes, or null when that is 0
     int32_t *err_flag;
     int32_t batch, D, H, dv;
     float eps, scale;
@@ -72,8 +73,10 @@ struct PrefillParams {
 // Each launcher returns cudaSuccess or the launch error.
 cudaError_t launch_decode(const DecodeParams &p, int dk, int dtype, cudaStream_t s);
 cudaError_t launch_verify(const VerifyParams &p, int dk, int dtype, cudaStream_t s);
-// Tensor-core row phase of verify (bf16, dk = dv = 128, D <= 8): whether it
-// applies to these parameters, and its launcher.
+// Verify for bf16, dk = dv = 128, D <= 8 (window kernel + tensor-core state
+// kernel): the scratch it needs (0 for every other shape), whether it applies
+// to these parameters, and its launcher.
+size_t verify_workspace_bytes(int H, int dk, int dv, int dtype, int64_t batch, int D);
 bool verify_tc_supported(const VerifyParams &p, int dk, int dtype);
 cudaError_t launch_verify_tc(const VerifyParams &p, cudaStream_t st);
 cudaError_t launch_replay(const ReplayParams &p, int dk, int dtype, cudaStream_t s);

@@ -11,7 +11,8 @@
 // state (the algebra is in kda_window.cuh), writes the records, and never
 // writes the pool.  The records come from the decode kernel's coefficient
 // routine, bit for bit.  This is the general path; bf16 windows of up to 8
-// tokens at dk = dv = 128 take the tensor-core row phase (kda_spec_tc.cu).
+// tokens at dk = dv = 128 take the window + tensor-core state kernels of
+// kda_spec_tc.cu (they need the caller's workspace).
 // replay_kernel: a CTA owns one (sequence, head, block of 16*R state rows).
 // It skips the tile without any memory access when a = 0.  Otherwise it
 // reads the rows once, applies a records with the decode kernel's row math

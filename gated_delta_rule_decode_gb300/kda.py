@@ -31,7 +31,8 @@ KDA_DEVERR_TIMEOUT = 8
 EXPORTED = ("kda_decode", "kda_verify_record", "kda_replay_commit",
             "kda_prefill_chunked", "kda_prefill_workspace_bytes",
             "kda_records_bytes", "kda_status_string", "kda_abi_version",
-            "kda_prefill_chunked_static", "kda_static_scratch_bytes")
+            "kda_prefill_chunked_static", "kda_static_scratch_bytes",
+            "kda_verify_workspace_bytes")
 
 
 class KdaError(RuntimeError):
@@ -69,7 +70,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kda_decode.argtypes = [_PD, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                _I64, _VP, _VP, _VP]
     lib.kda_verify_record.argtypes = [_PD, _I32, _I32, _VP, _VP, _VP, _VP, _VP,
-                                      _VP, _VP, _I64, _VP, _PR, _VP, _VP]
+                                      _VP, _VP, _I64, _VP, _PR, _VP, _SZ, _VP, _VP]
+    lib.kda_verify_workspace_bytes.argtypes = [_PD, _I32, _I32]
+    lib.kda_verify_workspace_bytes.restype = _SZ
     lib.kda_replay_commit.argtypes = [_PD, _I32, _I32, _PR, _VP, _VP, _VP, _I64,
                                       _VP, _VP]
     lib.kda_prefill_chunked.argtypes = [_PD, _I32, _VP, _I64, _VP, _VP, _VP,
@@ -127,6 +130,15 @@ def _ptr(t):
 def _stream_handle(stream) -> ctypes.c_void_p:
     s = torch.cuda.current_stream() if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _scratch(nbytes: int, device, stream) -> torch.Tensor:
+    """Device scratch for one call; when the call runs on a stream other than
+    the current one, the allocator is told so it is not reused too early."""
+    t = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if stream is not None:
+        t.record_stream(stream)
+    return t
 
 
 def _need(t: torch.Tensor, name: str, shape, dtype=None):
@@ -195,12 +207,19 @@ def _records_struct(rec) -> KdaRecords:
                       rec["g"].data_ptr(), rec["beta"].data_ptr())
 
 
+def verify_workspace_bytes(H, dk, dv, dtype_code, batch, draft_len) -> int:
+    dims = make_dims(H, dk, dv, dtype_code)
+    return int(_lib.kda_verify_workspace_bytes(ctypes.byref(dims), int(batch), int(draft_len)))
+
+
 def verify_record(q, k, v, g, b, slot_ids, pool, out=None, records=None, *,
-                  eps=1e-6, scale=None, err_flag=None, stream=None, _prepare=False):
+                  workspace=None, eps=1e-6, scale=None, err_flag=None, stream=None,
+                  _prepare=False):
     """ReplaySSM verify of D draft tokens; pool is read only.
 
     q, k: [B, D, H, dk]; v: [B, D, H, dv]; g fp32; b: [B, D, H].
-    Returns (out [B, D, H, dv], records dict).
+    ``workspace``: device uint8 scratch of verify_workspace_bytes(...) bytes,
+    allocated here when omitted.  Returns (out [B, D, H, dv], records dict).
     """
     B, D, H, dk = k.shape
     dv = v.shape[3]
@@ -218,11 +237,15 @@ def verify_record(q, k, v, g, b, slot_ids, pool, out=None, records=None, *,
         records = alloc_records(B, D, H, dk, dv, dt, q.device)
     rs = _records_struct(records)
     dims = make_dims(H, dk, dv, _dtype_code(q), eps, scale)
+    need = int(_lib.kda_verify_workspace_bytes(ctypes.byref(dims), B, D))
+    if workspace is None and need > 0:
+        workspace = _scratch(need, q.device, stream)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     args = (ctypes.byref(dims), B, D, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b),
             _ptr(slot_ids), _ptr(pool), pool.shape[0], _ptr(out), ctypes.byref(rs),
-            _ptr(err_flag), _stream_handle(stream))
+            _ptr(workspace), ws_bytes, _ptr(err_flag), _stream_handle(stream))
     if _prepare:
-        return _Prepared(_lib.kda_verify_record, args, "kda_verify_record", (dims, rs),
+        return _Prepared(_lib.kda_verify_record, args, "kda_verify_record", (dims, rs, workspace),
                          (out, records))
     _check(_lib.kda_verify_record(*args), "kda_verify_record")
     return out, records
@@ -278,7 +301,7 @@ def prefill_chunked(q, k, v, g, b, cu_seqlens, slot_ids, pool, out=None, *,
     code = _dtype_code(q)
     need = prefill_workspace_bytes(H, dk, dv, code, n, T)
     if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = _scratch(need, q.device, stream)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     dims = make_dims(H, dk, dv, code, eps, scale)
     args = (ctypes.byref(dims), n, _ptr(cu_seqlens), T, _ptr(q), _ptr(k), _ptr(v), _ptr(g),

@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 1
+#define KDA_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define KDA_API __attribute__((visibility("default")))
@@ -68,7 +68,7 @@ typedef enum kda_status {
                                   draft length outside 1..16, bad dims        */
     KDA_ERR_UNSUPPORTED = -2,  /* dk/dv/dtype combination not built           */
     KDA_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed        */
-    KDA_ERR_WORKSPACE = -4     /* prefill workspace NULL, too small, unaligned*/
+    KDA_ERR_WORKSPACE = -4     /* workspace NULL, too small or unaligned     */
 } kda_status;
 
 typedef enum kda_dtype {
@@ -152,12 +152,30 @@ KDA_API int kda_decode(const kda_dims *dims, int32_t batch, const void *q,
  *   rec      records sized for (batch, draft_len); all four arrays written
  *            for every entry, padding and errors included (they only depend
  *            on the token inputs).
+ *   workspace      device scratch of at least
+ *                  kda_verify_workspace_bytes(dims, batch, draft_len) bytes,
+ *                  256-byte aligned, owned by the caller; it may be NULL
+ *                  when that size is 0.  Its contents on return are
+ *                  undefined.  Calls sharing one workspace must not overlap
+ *                  on the GPU.  A required workspace that is NULL, too small
+ *                  or unaligned returns KDA_ERR_WORKSPACE, launching nothing.
  */
 KDA_API int kda_verify_record(const kda_dims *dims, int32_t batch, int32_t draft_len,
                       const void *q, const void *k, const void *v,
                       const float *g, const void *b, const int32_t *slot_ids,
                       const float *pool, int64_t num_slots, void *out,
-                      const kda_records *rec, int32_t *err_flag, void *stream);
+                      const kda_records *rec, void *workspace,
+                      size_t workspace_bytes, int32_t *err_flag, void *stream);
+
+/*
+ * Workspace bytes kda_verify_record needs for (dims, batch, draft_len): about
+ * 12.6 KB per (sequence, head) for bf16 windows of up to 8 tokens at
+ * dk = dv = 128 (the per-(sequence, head) window products and the decayed key
+ * and query tile the state kernel consumes), 0 for every other shape.  0 for
+ * invalid arguments.
+ */
+KDA_API size_t kda_verify_workspace_bytes(const kda_dims *dims, int32_t batch,
+                                          int32_t draft_len);
 
 /*
  * kda_replay_commit: commit after acceptance.  For each sequence n with

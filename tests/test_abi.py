@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(kda):
     for name in declared_functions():
         assert hasattr(lib, name), name
     assert set(kda.EXPORTED) <= set(declared_functions())
-    assert lib.kda_abi_version() == 1
+    assert lib.kda_abi_version() == 2
 
 
 def test_status_strings(kda):
@@ -58,6 +58,20 @@ def test_sizing_helpers(kda):
     assert lib.kda_records_bytes(ctypes.byref(d32), 3, 2) == 3 * 2 * 2 * (32 * 8 + 64 * 4 + 4)
     bad = kda.make_dims(2, 48, 64, kda.KDA_DT_F32)
     assert lib.kda_records_bytes(ctypes.byref(bad), 3, 2) == 0
+    # verify scratch: one 12928-byte record per (sequence, head) for bf16
+    # windows of 1..8 tokens at dk = dv = 128, none for any other shape
+    for D in (1, 7, 8):
+        assert lib.kda_verify_workspace_bytes(ctypes.byref(d), 128, D) == 128 * 32 * 12928
+    assert lib.kda_verify_workspace_bytes(ctypes.byref(d), 128, 9) == 0
+    assert lib.kda_verify_workspace_bytes(ctypes.byref(d), 0, 7) == 0
+    assert lib.kda_verify_workspace_bytes(ctypes.byref(d32), 3, 2) == 0
+    df = kda.make_dims(32, 128, 128, kda.KDA_DT_F32)
+    assert lib.kda_verify_workspace_bytes(ctypes.byref(df), 128, 7) == 0
+    d64 = kda.make_dims(32, 128, 64, kda.KDA_DT_BF16)
+    assert lib.kda_verify_workspace_bytes(ctypes.byref(d64), 128, 7) == 0
+    for D in (0, 17):
+        assert lib.kda_verify_workspace_bytes(ctypes.byref(d), 128, D) == 0
+    assert lib.kda_verify_workspace_bytes(ctypes.byref(bad), 128, 7) == 0
     assert lib.kda_prefill_workspace_bytes(ctypes.byref(bad), 1, 64) == 0
 
 
@@ -80,11 +94,20 @@ def test_host_side_argument_errors_launch_nothing(kda):
     rec = kda.KdaRecords(256, 256, 256, 256)
     for D in (0, 17):
         assert lib.kda_verify_record(ctypes.byref(good), 1, D, P, P, P, P, P, P, P, 8, P,
-                                     ctypes.byref(rec), None, None) == kda.KDA_ERR_INVALID_ARG
+                                     ctypes.byref(rec), None, 0, None, None) == kda.KDA_ERR_INVALID_ARG
         assert lib.kda_replay_commit(ctypes.byref(good), 1, D, ctypes.byref(rec), P, P, P, 8,
                                      None, None) == kda.KDA_ERR_INVALID_ARG
     assert lib.kda_verify_record(ctypes.byref(good), 1, 7, P, P, P, P, P, P, P, 8, P,
-                                 None, None, None) == kda.KDA_ERR_INVALID_ARG
+                                 None, None, 0, None, None) == kda.KDA_ERR_INVALID_ARG
+    # the bf16 dk = dv = 128 window of <= 8 tokens needs its scratch: missing,
+    # too small or unaligned is rejected before any launch
+    big = kda.make_dims(2, 128, 128, kda.KDA_DT_BF16)
+    need = lib.kda_verify_workspace_bytes(ctypes.byref(big), 1, 7)
+    assert need > 0
+    for ws, nbytes in ((None, 0), (P, need - 1), (ctypes.c_void_p(256 + 16), need)):
+        assert lib.kda_verify_record(ctypes.byref(big), 1, 7, P, P, P, P, P, P, P, 8, P,
+                                     ctypes.byref(rec), ws, nbytes, None,
+                                     None) == kda.KDA_ERR_WORKSPACE
     assert lib.kda_replay_commit(ctypes.byref(good), 0, 7, ctypes.byref(rec), P, P, P, 8,
                                  None, None) == kda.KDA_OK
     assert lib.kda_prefill_chunked(ctypes.byref(good), 0, P, 0, P, P, P, P, P, P, P, 8, 0,

@@ -139,12 +139,16 @@ def test_verify_many_items_per_cta(D):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("g_mean,D", [(-8.0, 16), (-8.0, 8), (-3.0, 7), (6.0, 16), (6.0, 5), (3.0, 9)])
+@pytest.mark.parametrize("g_mean,D", [(-14.0, 8), (-8.0, 16), (-8.0, 8), (-6.0, 8), (-3.0, 7),
+                                      (6.0, 16), (6.0, 5), (3.0, 9)])
 def test_verify_decay_range(dtype, g_mean, D):
-    """Near-total decay (alpha ~ 3e-4 per token: the window's decay products
-    underflow), strong, negligible and typical decay, over windows that take
-    each verify path (bf16 windows of up to 8 tokens at dk = dv = 128 use the
-    tensor-core row phase)."""
+    """Near-total decay (alpha ~ 1e-6 and 3e-4 per token: the window's decay
+    products fall below 1e-30 and underflow), strong, negligible and typical
+    decay, over windows that take each verify path (bf16 windows of up to 8
+    tokens at dk = dv = 128 use the window + tensor-core state kernels, whose
+    factored window products give way to running products when a decay
+    product drops below 1e-30: at g_mean -14 and -8 every window does, at -6
+    the factored form runs with decay products down to ~4e-25)."""
     kda = _kda()
     B, H, dk, dv, NS = 4, 2, 128, 128, 6
     x = inputs.verify_inputs(B, D, H, dk, dv, dtype=dtype, num_slots=NS, seed=31 + D,
