@@ -262,15 +262,24 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             }
         };
         load_block(0, kb, qb, vb, gb);
+        // swizzled stores of channel c in rows rb + r0 + rr: the row's low
+        // three bits are rr (rb and r0 are multiples of 8), so the 16-byte
+        // chunk is (c's chunk) ^ rr and only the block's first row varies
+        const uint32_t cpart = (uint32_t)((c & 3) << 2), cx4 = (uint32_t)(((c & 31) >> 2) << 4);
+        unsigned char *const kq0 = sm.bufKQ + (c >> 5) * 128 * 128 + cpart;
+        unsigned char *const km0 = sm.bufKM + (c >> 5) * 64 * 128 + cpart;
+        unsigned char *const bw0 = img + IMG_BW + (c >> 5) * 128 * 128 + cpart + 64 * 128;
 #pragma unroll 1
         for (int r0 = 0; r0 < 32; r0 += 8) {
             float nk[8], nq[8], nv[8], ng[8];
             if (r0 + 8 < 32) load_block(r0 + 8, nk, nq, nv, ng);
             float bkt[8], bvt[8];
+            const int rowb = (rb + r0) * 128;
 #pragma unroll
             for (int rr = 0; rr < 8; ++rr) {
                 const int r = rb + r0 + rr;
                 const bool valid = r < L;
+                const uint32_t sw = (cx4 ^ (uint32_t)(rr << 4)) + rr * 128;
                 acc += gb[rr];
                 const float gam = acc;
                 const float kx = kb[rr] * sm.invk[r];
@@ -280,9 +289,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                     const float E = __expf(gam - ref);
                     const float Ei = __expf(ref - gam);
                     const float kp = kx * E, qp = qx * E;
-                    st_sw(sm.bufKQ, 128, r, c, kp);
-                    st_sw(sm.bufKQ, 128, 64 + r, c, qp);
-                    st_sw(sm.bufKM, 64, r, c, kx * Ei);
+                    *reinterpret_cast<float *>(kq0 + rowb + sw) = kp;
+                    *reinterpret_cast<float *>(kq0 + rowb + 64 * 128 + sw) = qp;
+                    *reinterpret_cast<float *>(km0 + rowb + sw) = kx * Ei;
                     ktil = kp * eref;
                     qtil = qp * eref;
                 } else {
@@ -295,7 +304,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                     qtil = qx * eg;
                     st_sw(img + IMG_KT, 128, c, r, valid ? kx * expf(gC - gam) : 0.f);
                 }
-                st_sw(img + IMG_BW, 128, 64 + r, c, qtil);  // Q~ rows of [W; Q~]
+                *reinterpret_cast<float *>(bw0 + rowb + sw) = qtil;  // Q~ rows of [W; Q~]
                 bkt[rr] = sm.beta[r] * ktil;
                 bvt[rr] = sm.beta[r] * vb[rr];
             }
