@@ -228,3 +228,69 @@ def test_verify_commit_full_size_sampled():
     touched = torch.zeros(NS, dtype=torch.bool, device="cuda")
     touched[x.slot_ids.long()[x.num_accepted > 0]] = True
     assert torch.equal(x.pool[~touched], pool_before[~touched])
+
+
+def _verify_with(kda, x, workspace, stream=None):
+    args = [t.cuda() for t in (x.q, x.k, x.v, x.g, x.b, x.slot_ids, x.pool)]
+    out, rec = kda.verify_record(*args, workspace=workspace, stream=stream)
+    return out, rec
+
+
+@pytest.mark.parametrize("D", [1, 5, 8])
+def test_verify_workspace_contents_do_not_matter(D):
+    """The window + state kernels (bf16, dk = dv = 128, D <= 8) pass a scratch
+    record through the caller's workspace.  Whatever the workspace held before
+    (here NaN bit patterns), every byte the state kernel uses is written first:
+    outputs and records are the same bits as with a zeroed workspace."""
+    kda = _kda()
+    B, H, NS = 6, 4, 10
+    x = inputs.verify_inputs(B, D, H, 128, 128, dtype="bf16", num_slots=NS, seed=70 + D)
+    need = kda.verify_workspace_bytes(H, 128, 128, kda.KDA_DT_BF16, B, D)
+    assert need == B * H * 12928
+    ws0 = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    wsn = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")  # all-ones: NaN floats
+    out0, rec0 = _verify_with(kda, x, ws0)
+    outn, recn = _verify_with(kda, x, wsn)
+    torch.cuda.synchronize()
+    assert torch.isfinite(outn.float()).all()
+    assert torch.equal(out0, outn)
+    for key in ("k_hat", "v", "g", "beta"):
+        assert torch.equal(rec0[key], recn[key]), key
+
+
+def test_verify_workspace_reused_across_batches():
+    """One workspace serving two different batches in turn (and a side
+    stream): the second batch gets the same bits as with fresh scratch, and
+    both match the oracle."""
+    kda = _kda()
+    H, D, NS = 4, 7, 16
+    xa = inputs.verify_inputs(8, D, H, 128, 128, dtype="bf16", num_slots=NS, seed=81)
+    xb = inputs.verify_inputs(5, D, H, 128, 128, dtype="bf16", num_slots=NS, seed=82, g_mean=-5.0)
+    need = kda.verify_workspace_bytes(H, 128, 128, kda.KDA_DT_BF16, 8, D)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        out_a, _ = _verify_with(kda, xa, ws, stream=side)
+        out_b, rec_b = _verify_with(kda, xb, ws, stream=side)
+    side.synchronize()
+    out_b2, rec_b2 = _verify_with(kda, xb, None)
+    torch.cuda.synchronize()
+    assert torch.equal(out_b, out_b2)
+    for key in ("k_hat", "v", "g", "beta"):
+        assert torch.equal(rec_b[key], rec_b2[key]), key
+    atol, rtol = tol_for(torch.bfloat16)
+    for x, out in ((xa, out_a), (xb, out_b)):
+        o_ref, _, e = oracle.verify(x.q, x.k, x.v, x.g, x.b, x.slot_ids, x.pool)
+        assert e == 0
+        assert_close(to_np64(out), round_to(o_ref, torch.bfloat16), atol, rtol, "verify outputs")
+
+
+def test_verify_rejects_missing_or_small_workspace():
+    kda = _kda()
+    B, D, H = 2, 7, 2
+    x = inputs.verify_inputs(B, D, H, 128, 128, dtype="bf16", num_slots=4, seed=5)
+    need = kda.verify_workspace_bytes(H, 128, 128, kda.KDA_DT_BF16, B, D)
+    small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kda.KdaError) as ei:
+        _verify_with(kda, x, small)
+    assert ei.value.status == -4  # KDA_ERR_WORKSPACE
