@@ -27,6 +27,21 @@ substituting S'_r gives (I + A) U = diag(beta) (V - K~ S0^T).
 
 It exists to show that the chunked re-association equals the token loop in
 exact arithmetic (to fp64 rounding), and to expose per-chunk intermediates.
+
+The same unrolling over a ReplaySSM draft window ("2.8x faster Kimi K3
+inference on CANN", section 04 "ReplaySSM": verify emits an output for every
+draft token and never writes the state; the page does not say how the
+outputs are formed) gives `verify_window`, starting from the committed state
+S0 with E_j = prod_{l<=j} alpha_l:
+
+  K~_j = k^_j (.) E_j,   Q~_j = q^_j (.) E_j
+  a_jm = sum_c k^_m[c] k^_j[c] prod_{l=m+1..j} alpha_l[c]       (m < j)
+  p_jm = sum_c k^_m[c] q^_j[c] prod_{l=m+1..j} alpha_l[c]       (m <= j)
+  u_j  = beta_j (v_j - S0 K~_j - sum_{m<j} a_jm u_m)
+  o_j  = scale (S0 Q~_j + sum_{m<=j} p_jm u_m)
+
+and, since prod_{l=m+1..j} alpha_l = E_j / E_m, the factored products
+a_jm = K~_j . (k^_m / E_m) and p_jm = Q~_j . (k^_m / E_m).
 """
 from __future__ import annotations
 
@@ -97,3 +112,47 @@ def prefill(q, k, v, g, b, S0=None, chunk: int = 64, eps: float = 1e-6,
                                     np.asarray(b)[c0:c1], eps)
         O[c0:c1], S = chunk_step(S, inter, scale)
     return O, S
+
+
+def verify_window(q, k, v, g, b, S0, eps: float = 1e-6, scale=None,
+                  factored: bool = False):
+    """Draft-window outputs of one (sequence, head) from the committed state.
+
+    q, k, g: [D, dk]; v: [D, dv]; b: [D]; S0: [dv, dk].  The window products
+    are running products of alpha, or with ``factored`` the dot products
+    K~_j . (k^_m / E_m).  Returns O [D, dv]; S0 is not changed.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    g = np.asarray(g, np.float64)
+    b = np.asarray(b, np.float64)
+    S0 = np.asarray(S0, np.float64)
+    D, dk = k.shape
+    scale = dk ** -0.5 if scale is None else scale
+    qh = _l2norm(q, eps)
+    kh = _l2norm(k, eps)
+    beta = 1.0 / (1.0 + np.exp(-b))
+    alpha = np.exp(g)
+    E = np.cumprod(alpha, axis=0)                      # [D, dk]
+    K_tilde = kh * E
+    Q_tilde = qh * E
+    A = np.zeros((D, D))
+    P = np.zeros((D, D))
+    for j in range(D):
+        for m in range(j + 1):
+            if factored:
+                w_k = kh[m] / E[m]
+                a, pp = K_tilde[j] @ w_k, Q_tilde[j] @ w_k
+            else:
+                w = np.prod(alpha[m + 1:j + 1], axis=0)   # empty product = 1
+                a, pp = (kh[m] * w) @ kh[j], (kh[m] * w) @ qh[j]
+            if m < j:
+                A[j, m] = a
+            P[j, m] = pp
+    U = np.zeros((D, S0.shape[0]))
+    O = np.zeros((D, S0.shape[0]))
+    for j in range(D):
+        U[j] = beta[j] * (v[j] - S0 @ K_tilde[j] - A[j, :j] @ U[:j])
+        O[j] = scale * (S0 @ Q_tilde[j] + P[j, :j + 1] @ U[:j + 1])
+    return O

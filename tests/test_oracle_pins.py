@@ -289,11 +289,11 @@ def test_decode_matches_recurrence_and_padding_rules():
             assert np.array_equal(P[s], pool[s])
 
 
-def _draft(rng, B, D, H, dk, dv):
+def _draft(rng, B, D, H, dk, dv, g_mean=3.0):
     q = rng.standard_normal((B, D, H, dk))
     k = rng.standard_normal((B, D, H, dk))
     v = rng.standard_normal((B, D, H, dv))
-    g = -np.log1p(np.exp(-(rng.standard_normal((B, D, H, dk)) + 3)))
+    g = -np.log1p(np.exp(-(rng.standard_normal((B, D, H, dk)) + g_mean)))
     b = rng.standard_normal((B, D, H))
     return q, k, v, g, b
 
@@ -376,6 +376,23 @@ def test_chunk_form_strong_decay():
     o_c, S_c = chunk_form.prefill(q, k, v, g, b, chunk=64)
     np.testing.assert_allclose(o_c, o_ref, rtol=1e-9, atol=1e-11)
     np.testing.assert_allclose(S_c, S_ref, rtol=1e-9, atol=1e-11)
+
+
+@pytest.mark.parametrize("D,g_mean", [(1, 3.0), (7, 3.0), (8, 3.0), (8, -6.0), (16, 0.0)])
+@pytest.mark.parametrize("factored", [False, True])
+def test_verify_window_form_equals_token_loop(D, g_mean, factored):
+    """The draft-window chunk form (running or factored window products)
+    equals the oracle's token-by-token verify on one (sequence, head)."""
+    rng = np.random.default_rng(200 + D)
+    dk, dv, NS = 16, 12, 3
+    pool = 0.3 * rng.standard_normal((NS, 1, dv, dk))
+    slots = np.array([2], np.int32)
+    q, k, v, g, b = _draft(rng, 1, D, 1, dk, dv, g_mean=g_mean)
+    o_ref, _, err = oracle.verify(q, k, v, g, b, slots, pool)
+    assert err == 0
+    o_w = chunk_form.verify_window(q[0, :, 0], k[0, :, 0], v[0, :, 0], g[0, :, 0], b[0, :, 0],
+                                   pool[2, 0], factored=factored)
+    np.testing.assert_allclose(o_w, o_ref[0, :, 0], rtol=1e-9, atol=1e-11)
 
 
 def test_prefill_varlen_matches_recurrence():
