@@ -147,7 +147,7 @@ class ClockSampler:
         if not self.rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         inside = [r for t, r in self.rows if self.t_on and self.t_off and self.t_on <= t <= self.t_off]
-        window = "timed"
+        window = "timed steps and the 0.5 s continuation of the same launches"
         if len(inside) < 3:
             inside = [r for t, r in self.rows]
             window = "whole run (timed region shorter than the sampling period)"
@@ -249,10 +249,28 @@ def run_decode(args, world, rank, kda, peaks, sampler):
     for i in range(args.steps):
         step(args.warmup + i)
     t1.record(stream)
+    # the same launches continue for about half a second so that the clock
+    # samples cover the timed region's conditions; event pairs every 100
+    # launches give a sustained per-launch time beside the timed one
+    sus = []
+    j = args.warmup + args.steps
+    deadline = time.time() + 0.5
+    while time.time() < deadline or len(sus) < 3:
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(100):
+            step(j)
+            j += 1
+        b.record(stream)
+        sus.append((a, b))
+        if len(sus) % 4 == 0:
+            b.synchronize()
     torch.cuda.synchronize()
     sampler.mark_off()
     barrier(world)
     total_ms = t0.elapsed_time(t1)
+    sus_us = statistics.median([a.elapsed_time(b) * 10.0 for a, b in sus])
     ms_per_step = max_over_ranks(total_ms / args.steps, world)
     units = B * H
     value = sum_over_ranks(units * args.steps, world) / (ms_per_step * args.steps / 1e3)
@@ -266,7 +284,10 @@ def run_decode(args, world, rank, kda, peaks, sampler):
                 "traffic": traffic, "kernel": "kda::decode_kernel<128,bf16,4>",
                 "algorithmic_bytes_per_launch": DECODE_BYTES_PER_TH * units,
                 "peak_source": f"{peaks['source']} hbm_gbs (copy)",
-                "avg_kernel_us": round(avg_kernel_s * 1e6, 2)}
+                "avg_kernel_us": round(avg_kernel_s * 1e6, 2),
+                "frac_of_nominal_8000_gbs": round(achieved / 8000.0, 4),
+                "sustained_us_per_launch_median": round(sus_us, 2),
+                "sustained_launches": 100 * len(sus)}
 
     # e2e: host buffers through the same C ABI entry point.  As in a serving
     # loop, step i+1's inputs are uploaded and step i-1's outputs read back on
@@ -353,7 +374,8 @@ def run_decode(args, world, rank, kda, peaks, sampler):
                       "copies": "upload, kernel and read-back in order on one stream"}}
     del pool
     return dict(value=value, ms_per_step=ms_per_step, roofline=roofline, e2e=e2e,
-                launches=args.steps, kernel_us=avg_kernel_s * 1e6)
+                launches=args.steps, kernel_us=avg_kernel_s * 1e6,
+                sustained_launches=100 * len(sus))
 
 
 # --------------------------------------------------------------------------- extra paths
@@ -415,8 +437,9 @@ def run_spec(kda, peaks):
     }
 
 
-def run_prefill(kda, peaks, T=8192, H=32, steps=10, key="prefill_t8192_h32_d128_bf16"):
-    x = inputs.prefill_inputs([T], H, 128, 128, dtype="bf16", seed=0, device="cuda")
+def run_prefill(kda, peaks, T=8192, H=32, steps=10, key="prefill_t8192_h32_d128_bf16", x=None):
+    if x is None:
+        x = inputs.prefill_inputs([T], H, 128, 128, dtype="bf16", seed=0, device="cuda")
     out = torch.empty((T, H, 128), dtype=torch.bfloat16, device="cuda")
     ws_bytes = kda.prefill_workspace_bytes(H, 128, 128, kda.KDA_DT_BF16, 1, T)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
@@ -440,16 +463,20 @@ def run_prefill(kda, peaks, T=8192, H=32, steps=10, key="prefill_t8192_h32_d128_
 
 def run_longmix(kda, peaks):
     res = {"workload": "longmix_prefill_t102400_h32_decode256_b1024_h64_pool16384"}
-    res["prefill_t102400"] = run_prefill(kda, peaks, T=102400, H=32, steps=3,
-                                         key="prefill_t102400_h32_d128_bf16")
-    # 256 decode steps, batch 1 x 32 heads, on a 1-slot pool (L2-resident
-    # state: latency-bound), captured in one CUDA graph
-    H = 32
-    pool = torch.zeros((1, H, 128, 128), device="cuda")
+    T, H = 102400, 32
+    xp = inputs.prefill_inputs([T], H, 128, 128, dtype="bf16", seed=0, device="cuda")
+    res["prefill_t102400"] = run_prefill(kda, peaks, T=T, H=H, steps=3,
+                                         key="prefill_t102400_h32_d128_bf16", x=xp)
+    # 256 decode steps, batch 1 x 32 heads, on the prefill's final state (its
+    # slot; L2-resident: latency-bound), captured in one CUDA graph.  Every
+    # timed replay starts again from the prefill's final state.
+    pool, slots = xp.pool, xp.slot_ids
+    del xp
+    torch.cuda.empty_cache()
+    s_final = pool.clone()
     x = inputs.decode_inputs(1, H, 128, 128, dtype="bf16", num_slots=1, seed=7, device="cuda",
                              tokens=256)
     out = torch.empty((256, 1, H, 128), dtype=torch.bfloat16, device="cuda")
-    slots = torch.zeros(1, dtype=torch.int32, device="cuda")
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -461,9 +488,23 @@ def run_longmix(kda, peaks):
     with torch.cuda.graph(graph, stream=s):
         for t in range(256):
             kda.decode(x.q[t], x.k[t], x.v[t], x.g[t], x.b[t], slots, pool, out[t], stream=s)
-    ts = time_launches(lambda i: graph.replay(), 5, warmup=2)
-    res["decode_256_steps_b1_h32"] = {"us_per_step": round(ts / 256, 3), "graph": True}
-    del pool, x, out, graph
+    times = []
+    cur = torch.cuda.current_stream()
+    for i in range(7):
+        pool.copy_(s_final)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        graph.replay()
+        b.record(cur)
+        torch.cuda.synchronize()
+        if i >= 2:
+            times.append(a.elapsed_time(b) * 1e3)
+    ts = statistics.median(times)
+    res["decode_256_steps_b1_h32"] = {"us_per_step": round(ts / 256, 3), "graph": True,
+                                      "state": "the T = 102400 prefill's final state",
+                                      "replays": len(times), "us_per_replay_median": round(ts, 1)}
+    del pool, s_final, x, out, graph
     # 1024 x 64 heads over a 16384-slot pool (64 GiB)
     B2, H2, NS2 = 1024, 64, 16384
     try:
@@ -491,35 +532,88 @@ def run_longmix(kda, peaks):
 
 # --------------------------------------------------------------------------- CPU oracle
 
-def cpu_baseline(seconds_budget=12.0, threads=None):
-    """The fp64 oracle as it stands, on a bounded sample of the decode
-    workload (a subset of the 256 x 32 batch), on the host cores."""
+def _timed_reps(fn, seconds):
+    """Repeat fn() for about `seconds` (at least once); (reps, elapsed s)."""
+    fn()  # warm
+    reps, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds or reps == 0:
+        fn()
+        reps += 1
+    return reps, time.perf_counter() - t0
+
+
+def cpu_baseline(seconds_budget=6.0, threads=None, per_path=True):
+    """The fp64 oracle as it stands, on bounded samples of the workloads, on
+    the host cores.  The headline figure is decode (a 32-sequence subset of
+    the 256 x 32-head batch) on every core; `paths` adds decode on one core,
+    verify + commit (16 sequences x 7 draft tokens x 32 heads, the accepted
+    lengths of the workload's draw) and the 8192-token prefill (1 head on one
+    core, 16 heads on every core), each on one core and on all of them."""
     import oracle
     threads = threads or os.cpu_count() or 1
     used = oracle.set_threads(threads)
     w = inputs.WORKLOADS["decode_b256_h32_d128_pool4096_bf16"]
-    Bs = 32
-    x = inputs.decode_inputs(Bs, w["H"], 128, 128, dtype="bf16", num_slots=Bs, seed=0,
+    H, Bs = w["H"], 32
+    x = inputs.decode_inputs(Bs, H, 128, 128, dtype="bf16", num_slots=Bs, seed=0,
                              g_mean=3.0, pool_std=0.02)
     pool = x.pool.double()
-    oracle.decode(x.q[:1], x.k[:1], x.v[:1], x.g[:1], x.b[:1], x.slot_ids[:1], pool)  # warm
-    done = 0
-    t0 = time.perf_counter()
-    reps = 0
-    while time.perf_counter() - t0 < seconds_budget or reps == 0:
+
+    def dec():
         oracle.decode(x.q, x.k, x.v, x.g, x.b, x.slot_ids, pool)
-        done += Bs * w["H"]
-        reps += 1
-    dt = time.perf_counter() - t0
-    return {"value": round(done / dt, 2), "unit": UNIT, "cores": used, "kind": "oracle",
-            "sample": f"{reps} oracle decode calls of {Bs} sequences x {w['H']} heads "
-                      f"(dk = dv = 128, fp64) = {done} token-heads in {dt:.1f} s"}
+
+    reps, dt = _timed_reps(dec, seconds_budget)
+    done = reps * Bs * H
+    res = {"value": round(done / dt, 2), "unit": UNIT, "cores": used, "kind": "oracle",
+           "sample": f"{reps} oracle decode calls of {Bs} sequences x {H} heads "
+                     f"(dk = dv = 128, fp64) = {done} token-heads in {dt:.1f} s"}
+    if not per_path:
+        return res
+    paths = {}
+    budget = max(1.0, seconds_budget / 3)
+    for nthr in (1, used):
+        oracle.set_threads(nthr)
+        tag = f"{nthr}_core" if nthr == 1 else f"{nthr}_cores"
+        if nthr == 1:
+            r1, d1 = _timed_reps(dec, budget)
+            paths["decode_b256_h32_d128_1_core"] = {
+                "value": round(r1 * Bs * H / d1, 2), "unit": "token-heads/s", "cores": 1,
+                "sample": f"{r1} calls of {Bs} x {H} token-heads in {d1:.1f} s"}
+        y = inputs.verify_inputs(16, 7, H, 128, 128, dtype="bf16", num_slots=16, seed=0)
+        ypool = y.pool.double()
+
+        def spec():
+            _, rec, _ = oracle.verify(y.q, y.k, y.v, y.g, y.b, y.slot_ids, ypool)
+            oracle.replay(rec, y.num_accepted, y.slot_ids, ypool.clone())
+
+        r2, d2 = _timed_reps(spec, budget)
+        paths[f"verify_commit_b128_d7_h32_d128_{tag}"] = {
+            "value": round(r2 * 16 * 7 * H / d2, 2), "unit": "draft token-heads/s (verify + commit)",
+            "cores": nthr,
+            "sample": f"{r2} verify + commit rounds of 16 sequences x 7 draft tokens x {H} heads "
+                      f"in {d2:.1f} s"}
+        Hp = 1 if nthr == 1 else min(16, H)
+        z = inputs.prefill_inputs([8192], Hp, 128, 128, dtype="bf16", seed=0)
+        zpool = z.pool.double()
+
+        def pre():
+            oracle.prefill(z.q, z.k, z.v, z.g, z.b, z.cu_seqlens, z.slot_ids, zpool)
+
+        t0 = time.perf_counter()
+        pre()
+        d3 = time.perf_counter() - t0
+        paths[f"prefill_t8192_d128_{tag}"] = {
+            "value": round(8192 * Hp / d3, 2), "unit": "token-heads/s", "cores": nthr,
+            "sample": f"one oracle prefill of 8192 tokens x {Hp} head(s) in {d3:.1f} s"}
+    oracle.set_threads(used)
+    res["paths"] = paths
+    return res
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
-    cb = cpu_baseline(seconds_budget=max(2.0, min(30.0, 1.5 * (args.steps + args.warmup))))
+    cb = cpu_baseline(seconds_budget=max(2.0, min(30.0, 1.5 * (args.steps + args.warmup))),
+                      per_path=False)
     line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(256 * 32 / cb["value"] * 1e3, 3),

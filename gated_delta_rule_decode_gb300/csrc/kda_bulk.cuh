@@ -2,13 +2,24 @@
 //
 // Every wait is bounded: a wait that runs out of iterations returns false so
 // the caller can record KDA_DEVERR_TIMEOUT instead of hanging the GPU.
+//
+// Two limits: kWaitLimit bounds the waits of a kernel's main path, and
+// kDrainLimit bounds the waits that, after a main-path wait gave up, let the
+// copies and products still in flight finish before the CTA releases its
+// shared and tensor memory.  KDA_WAIT_LIMIT lowers the first one in a test
+// build, so that the timeout path can be exercised without a stuck copy.
 #pragma once
 
 #include <stdint.h>
 
+#ifndef KDA_WAIT_LIMIT
+#define KDA_WAIT_LIMIT (1u << 22)
+#endif
+
 namespace kda {
 
-constexpr uint32_t kWaitLimit = 1u << 22;  // try_wait polls before giving up
+constexpr uint32_t kWaitLimit = KDA_WAIT_LIMIT;  // main-path try_wait polls before giving up
+constexpr uint32_t kDrainLimit = 1u << 22;       // polls of a drain wait
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -47,6 +58,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t phase) {
 // Bounded wait on phase `phase`; false if the limit ran out.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t phase) {
     for (uint32_t it = 0; it < kWaitLimit; ++it)
+        if (mbar_try_wait(bar, phase)) return true;
+    return false;
+}
+
+// Drain wait: phase `phase` must be the one of an operation that was issued
+// and not yet observed complete (a wait on a phase that nothing will complete
+// spins out the whole limit).
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t phase) {
+    for (uint32_t it = 0; it < kDrainLimit; ++it)
         if (mbar_try_wait(bar, phase)) return true;
     return false;
 }

@@ -76,11 +76,13 @@ __device__ __forceinline__ void sync_for_mma() {
 }
 
 // Bounded wait on an MMA-completion barrier; the result is made uniform across
-// the CTA and a timeout is recorded in the error flag.
+// the CTA and a timeout is recorded in the error flag.  `phase` advances only
+// when the wait succeeded, so after a timeout it still names the pending
+// phase, which is the one a drain must wait for.
 __device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t &phase, int32_t *err_flag) {
     const bool mine = mbar_wait(bar, phase & 1);
-    phase ^= 1;
     const bool ok = __syncthreads_and(mine) != 0;
+    if (ok) phase ^= 1;
     if (!ok && threadIdx.x == 0 && err_flag) atomicOr(err_flag, KDA_DEVERR_TIMEOUT);
     tc::fence_after_sync();
     return ok;
@@ -513,7 +515,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             }
         }
     }
-    if (!ok) mbar_wait(&sm.bar, (phase ^ 1) & 1);  // let a late MMA finish (bounded)
+    if (!ok) mbar_wait_drain(&sm.bar, phase & 1);  // the product whose wait gave up
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tm, PT_COLS);
@@ -630,6 +632,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
     const uint32_t tm = sm.tmem_base;
 
     uint32_t ph1 = 0, ph2 = 0, ph3 = 0;
+    // products committed and not yet observed complete (uniform across the CTA)
+    bool pend1 = false, pend2 = false, pend3 = false;
     bool ok = true;
     int last_bw0 = nchunks > 0 ? 0 : -1, last_bw1 = -1, last_pk = nchunks > 0 ? 0 : -1;
     // this token thread's U' values for the block (threads 0..63), the next
@@ -696,8 +700,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
         // the previous chunk's output goes out while this chunk's first product runs
         if (ci > 0 && lr >= C) write_output(ci - 1, CT_D1 + (b ^ 1) * NR);
         if (lr < C && ci + 1 < nchunks) load_up(ci + 1, upn);
+        pend1 = true;
         ok = wait_mma(&sm.mma1, ph1, p.err_flag);
         if (!ok) break;
+        pend1 = false;
         // ---- U = U' - W Sb^T (thread = token r = TMEM lane r)
         if (lr < C) {
             float d[NH];
@@ -731,8 +737,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
                 tc::mma_tf32_ss(tm + d1, tc::desc_tf32_kstep(ap, 128, ks), tc::desc_tf32_kstep(b0, NR, ks), id, 1);
             tc::commit(&sm.mma2);
         }
+        pend2 = pend3 = true;
         ok = wait_mma(&sm.mma3, ph3, p.err_flag);
         if (!ok) break;
+        pend3 = false;
         // ---- Sb <- Sb diag(e^{gamma_C}) + D3^T (thread = channel c = TMEM lane c)
         {
             float d[NH];
@@ -753,6 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
         // other e^{gamma_C} slot was last read by chunk ci - 1
         ok = wait_mma(&sm.mma2, ph2, p.err_flag);
         if (!ok) break;
+        pend2 = false;
         if (tid == 0 && ci + 1 < nchunks) {
             issue_pk(ci + 1);
             last_pk = ci + 1;
@@ -772,13 +781,15 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
         }
     } else if (tid == 0) {
         // bounded waits so that no product or bulk copy is still writing when
-        // the CTA releases its memory
-        mbar_wait(&sm.mma1, ph1 & 1);
-        mbar_wait(&sm.mma2, ph2 & 1);
-        mbar_wait(&sm.mma3, ph3 & 1);
-        if (last_bw0 >= 0) mbar_wait(&sm.full_bw[0], (last_bw0 >> 1) & 1);
-        if (last_bw1 >= 0) mbar_wait(&sm.full_bw[1], (last_bw1 >> 1) & 1);
-        if (last_pk >= 0) mbar_wait(&sm.full_pk, last_pk & 1);
+        // the CTA releases its memory: each product still outstanding on its
+        // pending phase, and the last copy issued into each buffer (a copy
+        // already observed complete passes its phase at once)
+        if (pend1) mbar_wait_drain(&sm.mma1, ph1 & 1);
+        if (pend2) mbar_wait_drain(&sm.mma2, ph2 & 1);
+        if (pend3) mbar_wait_drain(&sm.mma3, ph3 & 1);
+        if (last_bw0 >= 0) mbar_wait_drain(&sm.full_bw[0], (last_bw0 >> 1) & 1);
+        if (last_bw1 >= 0) mbar_wait_drain(&sm.full_bw[1], (last_bw1 >> 1) & 1);
+        if (last_pk >= 0) mbar_wait_drain(&sm.full_pk, last_pk & 1);
     }
     tc::fence_before_sync();
     __syncthreads();

@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(256, (DMAX <= 8 ? 2 : 1)) verify_kernel(const 
         // the outcome is made CTA-uniform so that no thread skips a barrier
         if (__syncthreads_and(mbar_wait(&sm.bar, 0)) == 0) {
             if (threadIdx.x == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
-            mbar_wait(&sm.bar, 0);  // bounded second chance for the copy in flight
+            mbar_wait_drain(&sm.bar, 0);  // the copy still in flight
             return;
         }
         window_rows<DK, DMAX>(st, ngroups, gid, l, D, p.scale, &sm.kt[0][0], &sm.qt[0][0], &sm.A[0][0], &sm.P[0][0],

@@ -420,9 +420,9 @@ __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyPar
         } else {
             if (tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
             // bounded second chances: no copy or product may still be running
-            mbar_wait(&sm.rbar, 0);
-            mbar_wait(&sm.sbar, 0);
-            if (issued) mbar_wait(&sm.mbar, 0);
+            mbar_wait_drain(&sm.rbar, 0);
+            mbar_wait_drain(&sm.sbar, 0);
+            if (issued) mbar_wait_drain(&sm.mbar, 0);
         }
     }
     {

@@ -25,8 +25,11 @@
  * ----------------------------------------
  * - All tensor pointers are DEVICE pointers to contiguous row-major buffers,
  *   16-byte aligned.  The caller allocates and frees everything; the library
- *   never allocates device memory and keeps no global mutable state, so calls
- *   on different streams are independent.
+ *   never allocates device memory.  Every entry point but one keeps no global
+ *   mutable state, so calls on different streams are independent (given
+ *   separate outputs and workspaces).  The exception is
+ *   kda_prefill_chunked_static, whose scratch is one device array shared by
+ *   all its calls; see its comment below.
  * - State pool: float32 [num_slots][H][dv][dk]; the state of (slot, head) is
  *   one contiguous dv x dk block with dk fastest.
  * - Slot ids are int32.  A negative slot id marks a padding entry: it is
