@@ -92,7 +92,24 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src_gmem, uint32_t 
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
 }
 
+// Shared -> global 2-D tensor store (box of the tensor map at (x, y)) in the
+// thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const void *map, int x, int y, const void *src_smem) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(smem_addr(src_smem))
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until at most one committed bulk group still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_le1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+// Waits until every committed bulk group has completed (writes included).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Waits until the committed bulk stores have finished READING shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() {

@@ -1,6 +1,7 @@
 // Internal launch interface between the C ABI (kda_api.cu) and the kernels.
 #pragma once
 
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -69,6 +70,10 @@ struct PrefillParams {
     int32_t num_seqs, H, dk, dv;
     float eps, scale;
 };
+
+// The driver's cuTensorMapEncodeTiled (looked up once through the runtime),
+// or nullptr when the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encode_fn();
 
 // Each launcher returns cudaSuccess or the launch error.
 cudaError_t launch_decode(const DecodeParams &p, int dk, int dtype, cudaStream_t s);

@@ -11,25 +11,37 @@
 //   U^T = U'^T - S W^T,  O^T = scale (S Q~^T + U^T P^T),
 //   S <- S diag(e^{gamma_C}) + U^T K^                            (chunk step)
 //
-// Two kernels, both on tcgen05 (kind::tf32, fp32 accumulate):
+// Two kernels on tcgen05 (fp32 accumulate):
 //
 // prep_tc_kernel  one CTA per (chunk, head), all chunks of all sequences in
 //   parallel over the whole GPU.  Computes everything that does not depend on
-//   the state and writes, per (chunk, head), an operand image that the chain
-//   kernel copies into shared memory with one bulk copy:
-//     [W; Q~] (128 x 128), P (64 x 64), K^^T (128 x 64) as K-major 128B-swizzled
-//     tf32 tiles, e^{gamma_C} (128) and U' (64 x 128, plain fp32).
-// chain_tc_kernel  one CTA per (sequence, head, block of 32 value rows) walks
-//   the chunks in order; rows of the state are independent, so four CTAs
-//   share a head.  The rows sit on the N side of the products and the state
-//   block is a swizzled tile in shared memory (the B operand).  The operand
-//   images of the next chunk are in flight (bulk copies) while a chunk computes.
+//   the state (A/P on kind::tf32, the WY factors on kind::tf32) and writes,
+//   per (chunk, head), an operand image that the chain kernel copies into
+//   shared memory with two bulk copies:
+//     [W; Q~] (128 x 128), P (64 x 64) and K^^T (128 x 64) as K-major
+//     128B-swizzled fp16 tiles, e^{gamma_C} (128 fp32) and U'^T (128 x 64 fp32,
+//     each row's 16-byte units swizzled).
+// chain_kernel  one CTA per (sequence, head) walks the chunks in order with
+//   the state in tensor memory (value row i = TMEM lane i), so the state is
+//   the A operand of the chunk step's products and never leaves the SM:
+//     X = S [W; Q~]^T,  U^T = U'^T - X[:, :64],  S <- S diag(e^{gamma_C}),
+//     S += U^T K^,  O^T = scale (X[:, 64:] + U^T P^T)
+//   all on kind::f16.  The next chunk's operand images are in flight while a
+//   chunk computes, and a chunk's outputs are written while the next chunk's
+//   first product runs.
+//
+// Operand precision of the chain: fp16 has the same 10-bit mantissa as tf32
+// and rounds to nearest; the operands (normalised keys and queries times
+// decays <= 1, the WY factors, U and the state) stay far inside its range
+// for the recurrence's inputs.  A value beyond +-65504 sets KDA_DEVERR_RANGE
+// (that sequence's results are then not valid).
 //
 // Decay factors in the A/P product: with ref = gamma at token 31 of the chunk,
 // K+ = k^ e^{gamma-ref}, Q+ = q^ e^{gamma-ref}, K- = k^ e^{ref-gamma}, so that
 // [K+; Q+] K-^T carries e^{gamma_r - gamma_j}.  A chunk whose gamma spans more
 // than 80 (natural units) around ref on some channel would overflow these
 // factors; that chunk computes A and P with one exp per (r, j, c) instead.
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "kda.h"
@@ -43,17 +55,16 @@ namespace prefill_tc {
 
 constexpr int C = 64;   // chunk length
 constexpr int D = 128;  // dk = dv
-constexpr int kThreads = 256;  // chain CTA
 constexpr float kSpanLimit = 80.f;
 
 // Operand image of one (chunk, head) in the workspace (bytes).
-constexpr uint32_t IMG_BW = 0;                         // [W; Q~]  128 rows x K 128
-constexpr uint32_t IMG_P = IMG_BW + 128 * 128 * 4;     // P        64 rows x K 64
-constexpr uint32_t IMG_KT = IMG_P + 64 * 64 * 4;       // K^^T     128 rows x K 64
-constexpr uint32_t IMG_TILES = IMG_KT + 128 * 64 * 4;  // = 112 KiB, one bulk copy
-constexpr uint32_t IMG_EGC = IMG_TILES;                // e^{gamma_C}, 128 fp32
-constexpr uint32_t IMG_UP = IMG_EGC + 1024;            // U' plain [64 tokens][128 value rows] fp32
-constexpr uint32_t IMG_BYTES = IMG_UP + 64 * 128 * 4;
+constexpr uint32_t IMG_BW = 0;                         // [W; Q~] fp16, 128 rows x K 128
+constexpr uint32_t IMG_P = IMG_BW + 128 * 128 * 2;     // P       fp16, 64 rows x K 64
+constexpr uint32_t IMG_KT = IMG_P + 64 * 64 * 2;       // K^^T    fp16, 128 rows x K 64
+constexpr uint32_t IMG_EGC = IMG_KT + 128 * 64 * 2;    // e^{gamma_C}, 128 fp32
+constexpr uint32_t IMG_UP = IMG_EGC + 1024;            // U'^T [128 value rows][64 tokens] fp32, unit-swizzled rows
+constexpr uint32_t IMG_BYTES = IMG_UP + 64 * 128 * 4;  // 89 KiB
+constexpr float kHalfMax = 65504.f;                    // largest finite fp16
 
 __host__ __device__ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -64,8 +75,15 @@ __host__ __device__ inline int64_t max_chunks(int32_t num_seqs, int64_t total_to
     return (total_tokens + C - 1) / C + num_seqs;
 }
 
-__device__ __forceinline__ void st_sw(unsigned char *tile, int rows, int row, int k, float x) {
-    *reinterpret_cast<float *>(tile + tc::sw128_off(row, k, rows)) = x;
+// fp16 element (row, k) of a K-major 128B-swizzled tile
+__device__ __forceinline__ void st_h(unsigned char *tile, int rows, int row, int k, float x) {
+    *reinterpret_cast<__half *>(tile + tc::sw128_off16(row, k, rows)) = __float2half_rn(x);
+}
+
+// two fp16 values in one 32-bit word: a in the low half, b in the high half
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
 }
 
 __device__ __forceinline__ void sync_for_mma() {
@@ -79,8 +97,10 @@ __device__ __forceinline__ void sync_for_mma() {
 // the CTA and a timeout is recorded in the error flag.  `phase` advances only
 // when the wait succeeded, so after a timeout it still names the pending
 // phase, which is the one a drain must wait for.
+// Thread 0 alone polls; the other threads wait in the CTA barrier, where
+// they spend no issue slots.
 __device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t &phase, int32_t *err_flag) {
-    const bool mine = mbar_wait(bar, phase & 1);
+    const bool mine = threadIdx.x == 0 ? mbar_wait(bar, phase & 1) : true;
     const bool ok = __syncthreads_and(mine) != 0;
     if (ok) phase ^= 1;
     if (!ok && threadIdx.x == 0 && err_flag) atomicOr(err_flag, KDA_DEVERR_TIMEOUT);
@@ -270,7 +290,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         const uint32_t cpart = (uint32_t)((c & 3) << 2), cx4 = (uint32_t)(((c & 31) >> 2) << 4);
         unsigned char *const kq0 = sm.bufKQ + (c >> 5) * 128 * 128 + cpart;
         unsigned char *const km0 = sm.bufKM + (c >> 5) * 64 * 128 + cpart;
-        unsigned char *const bw0 = img + IMG_BW + (c >> 5) * 128 * 128 + cpart + 64 * 128;
 #pragma unroll 1
         for (int r0 = 0; r0 < 32; r0 += 8) {
             float nk[8], nq[8], nv[8], ng[8];
@@ -304,9 +323,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                     const float eg = expf(gam);
                     ktil = kx * eg;
                     qtil = qx * eg;
-                    st_sw(img + IMG_KT, 128, c, r, valid ? kx * expf(gC - gam) : 0.f);
+                    st_h(img + IMG_KT, 128, c, r, valid ? kx * expf(gC - gam) : 0.f);
                 }
-                *reinterpret_cast<float *>(bw0 + rowb + sw) = qtil;  // Q~ rows of [W; Q~]
+                st_h(img + IMG_BW, 128, 64 + r, c, qtil);  // Q~ rows of [W; Q~]
                 bkt[rr] = sm.beta[r] * ktil;
                 bvt[rr] = sm.beta[r] * vb[rr];
             }
@@ -325,6 +344,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
     sync_for_mma();
 
     bool ok = true;
+    bool big = false;  // a W entry beyond the fp16 range of the chain's operands
     // ---- 3. A and P
     if (!unsafe) {
         if (tid == 0) {
@@ -347,7 +367,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                 const int cc = 16 * warp + (it >> 1);
                 const int r = 32 * (it & 1) + lane;
                 const float km = *reinterpret_cast<const float *>(sm.bufKM + tc::sw128_off(r, cc, 64));
-                st_sw(img + IMG_KT, 128, cc, r, r < L ? km * sm.egcref[cc] : 0.f);
+                st_h(img + IMG_KT, 128, cc, r, r < L ? km * sm.egcref[cc] : 0.f);
             }
             // G rows (TMEM lanes): 0..63 are A', 64..127 are P; warp w takes
             // columns 32 (w >> 2) .. 32 (w >> 2) + 31
@@ -367,9 +387,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
 #pragma unroll
                     for (int jj = 0; jj < 16; jj += 4) {
                         const int j = j0 + jb + jj;
-                        *reinterpret_cast<float4 *>(img + IMG_P + tc::sw128_off(r, j, 64)) =
-                            make_float4(j <= r ? g16[jj] : 0.f, j + 1 <= r ? g16[jj + 1] : 0.f,
-                                        j + 2 <= r ? g16[jj + 2] : 0.f, j + 3 <= r ? g16[jj + 3] : 0.f);
+                        *reinterpret_cast<uint2 *>(img + IMG_P + tc::sw128_off16(r, j, 64)) =
+                            make_uint2(pack_h2(j <= r ? g16[jj] : 0.f, j + 1 <= r ? g16[jj + 1] : 0.f),
+                                       pack_h2(j + 2 <= r ? g16[jj + 2] : 0.f, j + 3 <= r ? g16[jj + 3] : 0.f));
                     }
                 }
             }
@@ -393,7 +413,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                 }
             }
             areg[it] = (j < r) ? sm.beta[r] * a : 0.f;
-            *reinterpret_cast<float *>(img + IMG_P + tc::sw128_off(r, j, 64)) = (j <= r) ? pp : 0.f;
+            st_h(img + IMG_P, 64, r, j, (j <= r) ? pp : 0.f);
         }
         __syncthreads();
 #pragma unroll
@@ -498,24 +518,34 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         }
         ok = wait_mma(&sm.bar, phase, p.err_flag);
         if (ok) {
-            // lane c: W[r][c] and U'[r][c] for this thread's token half (a warp's
-            // stores of one token row are one 128-byte line)
+            // lane c: W[r][c] and U'[r][c] for this thread's token half; W goes
+            // to its swizzled tile, U' to row c of U'^T in 16-byte units of
+            // four tokens, unit u at (u & 8) | ((u & 7) ^ (c & 7)) so that the
+            // chain's shared-memory reads of eight rows hit distinct banks
             float w16[16];
-            float *up = reinterpret_cast<float *>(img + IMG_UP);
+            unsigned char *up = img + IMG_UP + (size_t)c * C * 4;
 #pragma unroll
             for (int r0 = 0; r0 < 32; r0 += 16) {
                 tc::ld16(tc::lane_addr(tm, warp, PT_WT + rb + r0), w16);
                 tc::wait_ld();
 #pragma unroll
-                for (int rr = 0; rr < 16; ++rr) st_sw(img + IMG_BW, 128, rb + r0 + rr, c, w16[rr]);
+                for (int rr = 0; rr < 16; ++rr) {
+                    big |= !(fabsf(w16[rr]) <= kHalfMax) && w16[rr] == w16[rr];
+                    st_h(img + IMG_BW, 128, rb + r0 + rr, c, w16[rr]);
+                }
                 tc::ld16(tc::lane_addr(tm, warp, PT_UPT + rb + r0), w16);
                 tc::wait_ld();
 #pragma unroll
-                for (int rr = 0; rr < 16; ++rr) up[(rb + r0 + rr) * D + c] = w16[rr];
+                for (int rr = 0; rr < 16; rr += 4) {
+                    const int u = (rb + r0 + rr) >> 2;
+                    *reinterpret_cast<float4 *>(up + (((u & 8) | ((u & 7) ^ (c & 7))) << 4)) =
+                        make_float4(w16[rr], w16[rr + 1], w16[rr + 2], w16[rr + 3]);
+                }
             }
         }
     }
     if (!ok) mbar_wait_drain(&sm.bar, phase & 1);  // the product whose wait gave up
+    if (__syncthreads_or(big) && tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_RANGE);
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tm, PT_COLS);
@@ -523,273 +553,314 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
 
 // ================================================================== chain
 
-// One CTA per (sequence, head, block of NR value rows).  With the rows on the
-// N side, a chunk step is
-//   D1 = [W; Q~] Sb^T            M = 128 (token rows of W, then of Q~), N = NR, K = 128
-//   U = U' - D1[0:64]            token r = TMEM lane r, into the swizzled U tile
-//   D3 = K^^T U                  M = 128 channels, N = NR, K = 64 tokens
-//   D1[64:128] += P U            A = P placed in rows 64..127 of a 128-row tile
-//   Sb <- Sb diag(e^{gamma_C}) + D3^T,   O = scale D1[64:128]
-// (the A operands come from the chunk's operand image; Sb and U are K-major
-// 128-byte-swizzled tiles in shared memory).  Only D1 -> U -> D3 -> Sb is on
-// the serial path: P U has its own completion barrier and D1 alternates
-// between two TMEM regions, so a chunk's output is written while the next
-// chunk's first product runs.  The thread phases run on 8 warps: warps w and
-// w + 4 read the same TMEM lanes and take one half of the NR columns each
-// (256 threads measured 807 us per 8192-token prefill, 128 threads 842 us,
-// 512 threads 830 us).
-constexpr int NR = 32;
-constexpr int kRowBlocks = D / NR;
-constexpr uint32_t CT_D1 = 0, CT_D3 = 2 * NR;  // D1 ping-pongs between columns 0 and NR
-constexpr uint32_t CT_COLS = 128;
-constexpr uint32_t kPKBytes = 2 * 8192 + 128 * 64 * 4 + D * 4;  // P, K^^T, e^{gamma_C}
+// One CTA per (sequence, head): 16 data warps and one issuing warp.  Value
+// row i of the state is TMEM lane i; the data warps w, w + 4, w + 8, w + 12
+// serve the same 32 lanes and take one quarter of the columns each.  The fp32
+// state lives in the data warps' registers (thread (i, quarter q) holds
+// S[i][32 q .. 32 q + 31]); its fp16 copy S16 in TMEM is the A operand of the
+// first product.  Per chunk c:
+//   X  = S16 [W; Q~]^T        kind::f16, N = 128 (tokens of W, then of Q~), K = 128
+//   U^T = U'^T - X[:, 0:64]   data warps, written as fp16 into TMEM
+//   Z  = U^T K^               kind::f16, N = 128 channels, K = 64 tokens
+//   O^T = X[:, 64:] + U^T P^T kind::f16, N = 64 tokens, K = 64
+//   S = S diag(e^{gamma_C}) + Z, S16 = fp16(S)   data warps
+// The issuing warp (one thread) waits on "S16 ready" and "U16 ready"
+// barriers that the data warps arrive on, issues the products and the bulk
+// copies of the operand images (one per chunk, two buffers, the chunk after
+// next prefetched into L2).  The data warps observe the products' completion
+// barriers themselves, one lane per warp polling, so no CTA-wide barrier
+// sits in the chunk loop.  Only X -> U -> Z -> S16 is on the serial path: a
+// chunk's outputs go out (one tensor store per full chunk) while the next
+// chunk's X runs.
+constexpr int kDataWarps = 16;
+constexpr int kDataThreads = 32 * kDataWarps;
+constexpr int kChainThreads = kDataThreads + 32;  // + the issuing warp
+constexpr uint32_t CT_D1 = 0;     // X (64 columns) then O (64), two buffers of 128
+constexpr uint32_t CT_Z = 256;    // U^T K^, 128 columns
+constexpr uint32_t CT_S16 = 384;  // fp16 state, two per column: 64 columns
+constexpr uint32_t CT_U16 = 448;  // fp16 U^T: two buffers of 32 columns
+constexpr uint32_t CT_COLS = 512;
+static_assert(IMG_BYTES % 1024 == 0, "image buffers stay 1024-aligned");
 
 struct ChainSmem {
-    unsigned char bw[2][128 * 128 * 4];  // [W; Q~], double-buffered
-    unsigned char p128[2][128 * 128];    // 2 token atoms of a 128-row tile; P in rows 64..127
-    unsigned char kt[2][128 * 128];      // K^^T: 2 token atoms of 128 channel rows
-    unsigned char sb[4][NR * 128];       // state block: 4 channel atoms of NR rows
-    unsigned char ub[2][NR * 128];       // U block: 2 token atoms of NR rows
-    float egc[2][D];
-    uint64_t full_bw[2];
-    uint64_t full_pk;
-    uint64_t mma1, mma2, mma3;  // [W; Q~] Sb^T, P U, K^^T U done
+    unsigned char img[2][IMG_BYTES];  // a chunk's operand image, as laid out in the workspace
+    unsigned char ot[2][C * D * 2];   // a full chunk's outputs [64 tokens][128 value rows], for the TMA store
+    uint64_t full[2];                 // chunk images landed
+    uint64_t mma1, mma2s, mma2o;      // X, Z, output product done
+    uint64_t s16_ready, u16_ready;    // the data warps' hand-offs (one arrival per data warp)
+    uint64_t tile_full;               // an output tile written (one arrival per data warp)
+    uint64_t tile_free[2];            // an output tile's tensor store has read it (thread 0)
     uint32_t tmem_base;
 };
 constexpr size_t kChainSmem = sizeof(ChainSmem) + 1024;
 
+// One lane of the warp polls `bar` (bounded); on success every lane observes
+// the completed phase itself.  Warp-uniform result.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
+    bool okw = true;
+    if ((threadIdx.x & 31) == 0) okw = mbar_wait(bar, parity);
+    okw = __shfl_sync(0xffffffffu, okw ? 1 : 0, 0) != 0;
+    if (okw) mbar_try_wait(bar, parity);
+    tc::fence_after_sync();
+    return okw;
+}
+
+// The data warp's hand-off: its TMEM stores are complete and ordered before
+// lane 0's arrival.
+__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
+    tc::wait_st();
+    tc::fence_before_sync();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillParams p,
+                                                                  const __grid_constant__ CUtensorMap omap) {
     extern __shared__ unsigned char smem_raw[];
     ChainSmem &sm =
         *reinterpret_cast<ChainSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int32_t *plan = static_cast<const int32_t *>(p.workspace);
     const int n = p.num_seqs;
     if (plan[n + 1] == 0) return;
-    const int s = blockIdx.x, h = blockIdx.y, i0 = blockIdx.z * NR, H = p.H;
+    const int s = blockIdx.x, h = blockIdx.y, H = p.H;
     const int tid = threadIdx.x, warp = tid >> 5;
-    // TMEM lane of this thread (warps w and w + 4 share lanes 32 (w & 3) ..),
-    // and the half of the block's NR value rows (columns) it takes
-    const int lr = ((warp & 3) << 5) | (tid & 31), hf = warp >> 2;
-    constexpr int NH = NR / 2;
     const int32_t cs = p.cu_seqlens[s], ce = p.cu_seqlens[s + 1];
     const int slot = p.slot_ids[s];
     T *out = static_cast<T *>(p.out);
-    const int64_t tok_stride = (int64_t)H * D, hoff = (int64_t)h * D + i0;
+    const int64_t tok_stride = (int64_t)H * D, hoff = (int64_t)h * D;
     if (slot < 0 || (int64_t)slot >= p.num_slots) {
-        for (int64_t t = cs; t < ce; ++t)
-            if (tid < NR) Elem<T>::store1(out + t * tok_stride + hoff + tid, 0.f);
-        if (slot >= 0 && h == 0 && blockIdx.z == 0 && tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_SLOT);
+        for (int64_t t = cs + (tid >> 7); t < ce; t += kChainThreads / D)
+            Elem<T>::store1(out + t * tok_stride + hoff + (tid & 127), 0.f);
+        if (slot >= 0 && h == 0 && tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_SLOT);
         return;
     }
     const int nchunks = plan[s + 1] - plan[s];
     const unsigned char *ws = static_cast<const unsigned char *>(p.workspace) + plan_bytes(n);
-    auto image = [&](int ci) {
-        return ws + ((size_t)(plan[s] + ci) * H + h) * (size_t)IMG_BYTES;
-    };
-    auto issue_bw = [&](int ci, int b) {
-        mbar_arrive_expect_tx(&sm.full_bw[b], 128 * 128 * 4);
-        bulk_g2s(sm.bw[b], image(ci) + IMG_BW, 128 * 128 * 4, &sm.full_bw[b]);
-    };
-    auto issue_pk = [&](int ci) {
-        mbar_arrive_expect_tx(&sm.full_pk, kPKBytes);
-        bulk_g2s(sm.p128[0] + 8192, image(ci) + IMG_P, 8192, &sm.full_pk);
-        bulk_g2s(sm.p128[1] + 8192, image(ci) + IMG_P + 8192, 8192, &sm.full_pk);
-        bulk_g2s(sm.kt, image(ci) + IMG_KT, 128 * 64 * 4, &sm.full_pk);
-        bulk_g2s(sm.egc[ci & 1], image(ci) + IMG_EGC, D * 4, &sm.full_pk);
-    };
+    auto image = [&](int ci) { return ws + ((size_t)(plan[s] + ci) * H + h) * (size_t)IMG_BYTES; };
 
     if (warp == 0) tc::tmem_alloc(&sm.tmem_base, CT_COLS);
     if (tid == 0) {
-        mbar_init(&sm.full_bw[0], 1);
-        mbar_init(&sm.full_bw[1], 1);
-        mbar_init(&sm.full_pk, 1);
+        mbar_init(&sm.full[0], 1);
+        mbar_init(&sm.full[1], 1);
         mbar_init(&sm.mma1, 1);
-        mbar_init(&sm.mma2, 1);
-        mbar_init(&sm.mma3, 1);
+        mbar_init(&sm.mma2s, 1);
+        mbar_init(&sm.mma2o, 1);
+        mbar_init(&sm.s16_ready, kDataWarps);
+        mbar_init(&sm.u16_ready, kDataWarps);
+        mbar_init(&sm.tile_full, kDataWarps);
+        mbar_init(&sm.tile_free[0], 1);
+        mbar_init(&sm.tile_free[1], 1);
         fence_barrier_init();
-        if (nchunks > 0) {
-            issue_bw(0, 0);
-            issue_pk(0);
-        }
     }
-    // rows 0..63 of the P tile only feed discarded accumulator lanes; zeroed
-    // once so that they hold finite values
-    for (int idx = tid; idx < 2 * 8192 / 16; idx += kThreads)
-        *reinterpret_cast<uint4 *>(sm.p128[idx >> 9] + (idx & 511) * 16) = make_uint4(0, 0, 0, 0);
-    // initial state block (rows i0 .. i0 + NR) into the swizzled tile
-    float *Sg = p.pool + ((int64_t)slot * H + h) * (int64_t)D * D + (int64_t)i0 * D;
-    for (int idx = tid; idx < NR * (D / 4); idx += kThreads) {
-        const int i = idx / (D / 4), c4 = (idx % (D / 4)) * 4;
-        const float4 x = p.init_from_pool ? *reinterpret_cast<const float4 *>(Sg + (int64_t)i * D + c4)
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4 *>(&sm.sb[0][0] + tc::sw128_off(i, c4, NR)) = x;
-    }
-    fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tm = sm.tmem_base;
-
-    uint32_t ph1 = 0, ph2 = 0, ph3 = 0;
-    // products committed and not yet observed complete (uniform across the CTA)
-    bool pend1 = false, pend2 = false, pend3 = false;
     bool ok = true;
-    int last_bw0 = nchunks > 0 ? 0 : -1, last_bw1 = -1, last_pk = nchunks > 0 ? 0 : -1;
-    // this token thread's U' values for the block (threads 0..63), the next
-    // chunk's in flight while the current one computes
-    float upc[NH], upn[NH];
-    auto load_up = [&](int ci, float (&dst)[NH]) {
-        const float4 *src =
-            reinterpret_cast<const float4 *>(image(ci) + IMG_UP) + ((size_t)lr * D + i0 + hf * NH) / 4;
-#pragma unroll
-        for (int j = 0; j < NH / 4; ++j) {
-            const float4 x = __ldg(src + j);
-            dst[4 * j] = x.x; dst[4 * j + 1] = x.y; dst[4 * j + 2] = x.z; dst[4 * j + 3] = x.w;
-        }
-    };
-    // O = scale D1[64:128] of chunk cj from the D1 region at column col
-    // (token threads 64..127; warp-uniform)
-    auto write_output = [&](int cj, uint32_t col) {
-        const int64_t tj = (int64_t)cs + (int64_t)cj * C;
-        const int Lj = (int)((int64_t)ce - tj < C ? (int64_t)ce - tj : C);
-        float o[NH];
-        tc::ld16(tc::lane_addr(tm, warp, col + hf * NH), o);
-        tc::wait_ld();
-        if (lr - C < Lj) {
-            T *dst = out + (tj + lr - C) * tok_stride + hoff + hf * NH;
-            constexpr int V = 16 / sizeof(T);  // elements per 16-byte store
-#pragma unroll
-            for (int v0 = 0; v0 < NH; v0 += V) {
-                alignas(16) T pack[V];
-#pragma unroll
-                for (int e2 = 0; e2 < V; ++e2) Elem<T>::store1(&pack[e2], p.scale * o[v0 + e2]);
-                *reinterpret_cast<uint4 *>(dst + v0) = *reinterpret_cast<const uint4 *>(pack);
-            }
-        }
-    };
-    if (lr < C && nchunks > 0) load_up(0, upc);
+    float *Sg = nullptr;
+    float S[32];
 
-    for (int ci = 0; ci < nchunks; ++ci) {
-        const int b = ci & 1;
-        const uint32_t d1 = CT_D1 + b * NR;
-        const bool landed = mbar_wait(&sm.full_bw[b], (ci >> 1) & 1);
-        if (__syncthreads_and(landed) == 0) {
-            if (tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
-            ok = false;
-            break;
-        }
-        tc::fence_after_sync();
-        // ---- D1 = [W; Q~] Sb^T
-        if (tid == 0) {
-            constexpr uint32_t id = tc::idesc_tf32(128, NR);
-            const uint32_t a0 = tc::smem_u32(sm.bw[b]), b0 = tc::smem_u32(sm.sb);
+    if (warp == kDataWarps) {
+        // ================= issuing warp (lane 0)
+        if ((tid & 31) == 0) {
+            int last_issue[2] = {-1, -1};
+            auto issue = [&](int ci) {
+                const int b = ci & 1;
+                mbar_arrive_expect_tx(&sm.full[b], IMG_BYTES);
+                bulk_g2s(sm.img[b], image(ci), IMG_BYTES, &sm.full[b]);
+                last_issue[b] = ci;
+                if (ci + 2 < nchunks) bulk_prefetch_l2(image(ci + 2), IMG_BYTES);
+            };
+            if (nchunks > 0) issue(0);
+            if (nchunks > 1) issue(1);
+            int nx = 0, nz = 0;  // products committed so far (X; Z and O)
+            for (int c = 0; c < nchunks && ok; ++c) {
+                const int b = c & 1;
+                // ---- X of chunk c: S16 (its hand-off) and the image
+                ok = mbar_wait(&sm.s16_ready, c & 1) && mbar_wait(&sm.full[b], (c >> 1) & 1);
+                if (!ok) break;
+                tc::fence_after_sync();
+                {
+                    constexpr uint32_t id = tc::idesc_f16(128, 128);
+                    const uint32_t b0 = tc::smem_u32(sm.img[b] + IMG_BW), d1 = CT_D1 + b * 128;
 #pragma unroll
-            for (int ks = 0; ks < D / 8; ++ks)
-                tc::mma_tf32_ss(tm + d1, tc::desc_tf32_kstep(a0, 128, ks), tc::desc_tf32_kstep(b0, NR, ks), id,
-                                ks > 0);
-            tc::commit(&sm.mma1);
-            // the other [W; Q~] buffer's last product (chunk ci - 1) has completed
-            if (ci + 1 < nchunks) {
-                issue_bw(ci + 1, b ^ 1);
-                if (b) last_bw0 = ci + 1; else last_bw1 = ci + 1;
-                // the next chunk's P, K^^T and e^{gamma_C} towards L2 ahead of their copy
-                bulk_prefetch_l2(image(ci + 1) + IMG_P, IMG_EGC + D * 4 - IMG_P);
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        tc::mma_f16_ts(tm + d1, tm + CT_S16 + 8 * ks, tc::desc_tf32_kstep(b0, 128, ks), id, ks > 0);
+                    tc::commit(&sm.mma1);
+                    ++nx;
+                }
+                // ---- chunk c - 1's buffer is free once its products are done
+                // (and its readers, the data warps, handed over S16 of chunk c)
+                if (c >= 1 && c + 1 < nchunks) {
+                    ok = mbar_wait(&sm.mma2o, (c - 1) & 1);
+                    if (!ok) break;
+                    issue(c + 1);
+                }
+                // ---- Z, then O, of chunk c: U16 (its hand-off)
+                ok = mbar_wait(&sm.u16_ready, c & 1);
+                if (!ok) break;
+                tc::fence_after_sync();
+                {
+                    const uint32_t u16 = CT_U16 + b * 32, d1 = CT_D1 + b * 128;
+                    const uint32_t kt = tc::smem_u32(sm.img[b] + IMG_KT), pp = tc::smem_u32(sm.img[b] + IMG_P);
+#pragma unroll
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        tc::mma_f16_ts(tm + CT_Z, tm + u16 + 8 * ks, tc::desc_tf32_kstep(kt, 128, ks),
+                                       tc::idesc_f16(128, 128), ks > 0);
+                    tc::commit(&sm.mma2s);
+#pragma unroll
+                    for (int ks = 0; ks < C / 16; ++ks)
+                        tc::mma_f16_ts(tm + d1 + 64, tm + u16 + 8 * ks, tc::desc_tf32_kstep(pp, 64, ks),
+                                       tc::idesc_f16(128, 64), 1);
+                    tc::commit(&sm.mma2o);
+                    ++nz;
+                }
             }
-        }
-        // the previous chunk's output goes out while this chunk's first product runs
-        if (ci > 0 && lr >= C) write_output(ci - 1, CT_D1 + (b ^ 1) * NR);
-        if (lr < C && ci + 1 < nchunks) load_up(ci + 1, upn);
-        pend1 = true;
-        ok = wait_mma(&sm.mma1, ph1, p.err_flag);
-        if (!ok) break;
-        pend1 = false;
-        // ---- U = U' - W Sb^T (thread = token r = TMEM lane r)
-        if (lr < C) {
-            float d[NH];
-            tc::ld16(tc::lane_addr(tm, warp, d1 + hf * NH), d);
-            tc::wait_ld();
-#pragma unroll
-            for (int i = 0; i < NH; ++i) st_sw(&sm.ub[0][0], NR, hf * NH + i, lr, upc[i] - d[i]);
-        }
-        fence_proxy_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
-        // ---- D3 = K^^T U (serial path), then D1[64:128] += P U
-        const bool pk = mbar_wait(&sm.full_pk, ci & 1);
-        if (__syncthreads_and(pk) == 0) {
-            if (tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
-            ok = false;
-            break;
-        }
-        tc::fence_after_sync();
-        if (tid == 0) {
-            constexpr uint32_t id = tc::idesc_tf32(128, NR);
-            const uint32_t ap = tc::smem_u32(sm.p128), ak = tc::smem_u32(sm.kt), b0 = tc::smem_u32(sm.ub);
-#pragma unroll
-            for (int ks = 0; ks < C / 8; ++ks)
-                tc::mma_tf32_ss(tm + CT_D3, tc::desc_tf32_kstep(ak, 128, ks), tc::desc_tf32_kstep(b0, NR, ks), id,
-                                ks > 0);
-            tc::commit(&sm.mma3);
-#pragma unroll
-            for (int ks = 0; ks < C / 8; ++ks)
-                tc::mma_tf32_ss(tm + d1, tc::desc_tf32_kstep(ap, 128, ks), tc::desc_tf32_kstep(b0, NR, ks), id, 1);
-            tc::commit(&sm.mma2);
-        }
-        pend2 = pend3 = true;
-        ok = wait_mma(&sm.mma3, ph3, p.err_flag);
-        if (!ok) break;
-        pend3 = false;
-        // ---- Sb <- Sb diag(e^{gamma_C}) + D3^T (thread = channel c = TMEM lane c)
-        {
-            float d[NH];
-            tc::ld16(tc::lane_addr(tm, warp, CT_D3 + hf * NH), d);
-            tc::wait_ld();
-            const float e = sm.egc[b][lr];
-#pragma unroll
-            for (int i = 0; i < NH; ++i) {
-                float *sp = reinterpret_cast<float *>(&sm.sb[0][0] + tc::sw128_off(hf * NH + i, lr, NR));
-                *sp = fmaf(*sp, e, d[i]);
+            if (!ok && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
+            // no product or copy may still be writing when the CTA releases its
+            // memory: the last commit of each barrier and the last copy into
+            // each buffer (a phase already complete passes at once)
+            if (nx > 0) mbar_wait_drain(&sm.mma1, (nx - 1) & 1);
+            if (nz > 0) {
+                mbar_wait_drain(&sm.mma2s, (nz - 1) & 1);
+                mbar_wait_drain(&sm.mma2o, (nz - 1) & 1);
             }
+            for (int b = 0; b < 2; ++b)
+                if (last_issue[b] >= 0) mbar_wait_drain(&sm.full[b], (last_issue[b] >> 1) & 1);
         }
-        if (lr < C) {
+    } else {
+        // ================= data warps
+        const int lr = ((warp & 3) << 5) | (tid & 31);  // value row = TMEM lane
+        const int cq = warp >> 2;                        // quarter of the columns this thread takes
+        auto taddr = [&](uint32_t col) { return tc::lane_addr(tm, warp, (int)col); };
+        bool bad = false;  // a U entry beyond the fp16 range (or not a number)
+        Sg = p.pool + ((int64_t)slot * H + h) * (int64_t)D * D + (int64_t)lr * D + cq * 32;
 #pragma unroll
-            for (int j = 0; j < NH; ++j) upc[j] = upn[j];
+        for (int e = 0; e < 32; e += 4) {
+            const float4 v4 = p.init_from_pool ? *reinterpret_cast<const float4 *>(Sg + e)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            S[e] = v4.x; S[e + 1] = v4.y; S[e + 2] = v4.z; S[e + 3] = v4.w;
         }
-        // P U is done (it ran during the update): P and K^^T are free, and the
-        // other e^{gamma_C} slot was last read by chunk ci - 1
-        ok = wait_mma(&sm.mma2, ph2, p.err_flag);
-        if (!ok) break;
-        pend2 = false;
-        if (tid == 0 && ci + 1 < nchunks) {
-            issue_pk(ci + 1);
-            last_pk = ci + 1;
+        auto store_s16 = [&]() {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w[e] = pack_h2(S[2 * e], S[2 * e + 1]);
+            tc::st16u(taddr(CT_S16 + cq * 16), w);
+        };
+        // outputs of chunk cj (tokens cq * 16 .. + 15 of value row lr): a full
+        // chunk through its tile and one tensor store, a partial one straight
+        // to global memory.  Tile hand-offs go through mbarriers (bounded
+        // waits): the data warps arrive on tile_full once their part is
+        // written, thread 0 then issues the store and, once the previous
+        // store has read its tile, arrives on that tile's tile_free.
+        auto output = [&](int cj) {
+            if (!warp_wait(&sm.mma2o, cj & 1)) return false;
+            const int64_t tj = (int64_t)cs + (int64_t)cj * C;
+            const int Lj = (int)((int64_t)ce - tj < C ? (int64_t)ce - tj : C);
+            float o[16];
+            tc::ld16(taddr(CT_D1 + (cj & 1) * 128 + 64 + cq * 16), o);
+            tc::wait_ld();
+            if (Lj == C) {
+                const int t = cj & 1, use = cj >> 1;  // the tile and its use count
+                if (use > 0 && !warp_wait(&sm.tile_free[t], (use - 1) & 1)) return false;
+                T *tile = reinterpret_cast<T *>(sm.ot[t]) + (cq * 16) * D + lr;
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Elem<T>::store1(tile + r * D, p.scale * o[r]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if ((tid & 31) == 0) mbar_arrive(&sm.tile_full);
+                if (warp == 0) {
+                    bool stored = true;
+                    if (tid == 0) {
+                        stored = mbar_wait(&sm.tile_full, cj & 1);
+                        if (stored) {
+                            tma_store_2d(&omap, h * D, cs + cj * C, sm.ot[t]);
+                            bulk_commit();
+                            if (cj > 0) {
+                                bulk_wait_read_le1();
+                                mbar_arrive(&sm.tile_free[t ^ 1]);
+                            }
+                        }
+                    }
+                    if (__shfl_sync(0xffffffffu, stored ? 1 : 0, 0) == 0) return false;  // warp-uniform
+                }
+            } else {
+                T *dst = out + (tj + cq * 16) * tok_stride + hoff + lr;
+#pragma unroll
+                for (int r = 0; r < 16; ++r)
+                    if (cq * 16 + r < Lj) Elem<T>::store1(dst + (int64_t)r * tok_stride, p.scale * o[r]);
+            }
+            return true;
+        };
+        store_s16();
+        warp_arrive(&sm.s16_ready);
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int b = c & 1;
+            const unsigned char *im = sm.img[b];
+            // ---- the previous chunk's outputs while X runs
+            if (c > 0) {
+                ok = output(c - 1);
+                if (!ok) break;
+            }
+            // ---- U^T = U'^T - X[:, 0:64], fp16 into TMEM (each warp also
+            // observes chunk c's image barrier before reading U'^T and e^gamma)
+            ok = warp_wait(&sm.mma1, c & 1) && warp_wait(&sm.full[b], (c >> 1) & 1);
+            if (!ok) break;
+            {
+                float x[16];
+                tc::ld16(taddr(CT_D1 + b * 128 + cq * 16), x);
+                const unsigned char *urow = im + IMG_UP + lr * (C * 4);
+                float up[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int u = cq * 4 + j;
+                    const float4 v4 =
+                        *reinterpret_cast<const float4 *>(urow + (((u & 8) | ((u & 7) ^ (lr & 7))) << 4));
+                    up[4 * j] = v4.x; up[4 * j + 1] = v4.y; up[4 * j + 2] = v4.z; up[4 * j + 3] = v4.w;
+                }
+                tc::wait_ld();
+                uint32_t w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float u0 = up[2 * e] - x[2 * e], u1 = up[2 * e + 1] - x[2 * e + 1];
+                    bad |= !(fabsf(u0) <= kHalfMax) || !(fabsf(u1) <= kHalfMax);
+                    w[e] = pack_h2(u0, u1);
+                }
+                tc::st8u(taddr(CT_U16 + b * 32 + cq * 8), w);
+            }
+            warp_arrive(&sm.u16_ready);
+            // ---- S = S diag(e^{gamma_C}) + Z, and its fp16 copy
+            ok = warp_wait(&sm.mma2s, c & 1);
+            if (!ok) break;
+            {
+                float z[32];
+                tc::ld32(taddr(CT_Z + cq * 32), z);
+                const float4 *e4 = reinterpret_cast<const float4 *>(im + IMG_EGC) + cq * 8;
+                tc::wait_ld();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 g4 = e4[j];
+                    S[4 * j] = fmaf(S[4 * j], g4.x, z[4 * j]);
+                    S[4 * j + 1] = fmaf(S[4 * j + 1], g4.y, z[4 * j + 1]);
+                    S[4 * j + 2] = fmaf(S[4 * j + 2], g4.z, z[4 * j + 2]);
+                    S[4 * j + 3] = fmaf(S[4 * j + 3], g4.w, z[4 * j + 3]);
+                }
+                store_s16();
+            }
+            warp_arrive(&sm.s16_ready);
         }
-        fence_proxy_async_smem();  // Sb writes before the next product; e^{gamma_C} reads before its refill
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
+        if (ok && nchunks > 0) ok = output(nchunks - 1);
+        if (tid == 0) bulk_wait_all();  // every tensor store complete before shared memory goes
+        if (bad && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_RANGE);
+        if (!ok && (tid & 31) == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
     }
-    if (ok && nchunks > 0 && lr >= C) write_output(nchunks - 1, CT_D1 + ((nchunks - 1) & 1) * NR);
-
-    if (ok) {
-        for (int idx = tid; idx < NR * (D / 4); idx += kThreads) {
-            const int i = idx / (D / 4), c4 = (idx % (D / 4)) * 4;
-            *reinterpret_cast<float4 *>(Sg + (int64_t)i * D + c4) =
-                *reinterpret_cast<const float4 *>(&sm.sb[0][0] + tc::sw128_off(i, c4, NR));
-        }
-    } else if (tid == 0) {
-        // bounded waits so that no product or bulk copy is still writing when
-        // the CTA releases its memory: each product still outstanding on its
-        // pending phase, and the last copy issued into each buffer (a copy
-        // already observed complete passes its phase at once)
-        if (pend1) mbar_wait_drain(&sm.mma1, ph1 & 1);
-        if (pend2) mbar_wait_drain(&sm.mma2, ph2 & 1);
-        if (pend3) mbar_wait_drain(&sm.mma3, ph3 & 1);
-        if (last_bw0 >= 0) mbar_wait_drain(&sm.full_bw[0], (last_bw0 >> 1) & 1);
-        if (last_bw1 >= 0) mbar_wait_drain(&sm.full_bw[1], (last_bw1 >> 1) & 1);
-        if (last_pk >= 0) mbar_wait_drain(&sm.full_pk, last_pk & 1);
+    // the final state, only when every warp finished its loop
+    const bool all_ok = __syncthreads_and(ok) != 0;
+    if (all_ok && warp < kDataWarps) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4 *>(Sg + e) = make_float4(S[e], S[e + 1], S[e + 2], S[e + 3]);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -803,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const PrefillPara
 #endif
 
 bool prefill_tc_supported(int dk, int dv, int dtype) {
-    return KDA_PREFILL_TC && dtype == KDA_DT_BF16 && dk == 128 && dv == 128;
+    return KDA_PREFILL_TC && dtype == KDA_DT_BF16 && dk == 128 && dv == 128 && tensor_map_encode_fn() != nullptr;
 }
 
 size_t prefill_tc_workspace_bytes(int H, int32_t num_seqs, int64_t total_tokens) {
@@ -816,7 +887,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(prep_tc_kernel<__nv_bfloat16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(chain_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(chain_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kChainSmem);
     if (e != cudaSuccess) return e;
     const int64_t mc = max_chunks(p.num_seqs, p.total_tokens);
@@ -825,8 +896,18 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    chain_tc_kernel<__nv_bfloat16>
-        <<<dim3((unsigned)p.num_seqs, (unsigned)p.H, (unsigned)kRowBlocks), kThreads, kChainSmem, st>>>(p);
+    // the output tensor as [total_tokens][H * 128] bf16, boxes of 64 tokens x
+    // one head's 128 values (the chain's full-chunk tensor stores)
+    CUtensorMap omap;
+    const cuuint64_t dims[2] = {(cuuint64_t)p.H * D, (cuuint64_t)(p.total_tokens > 0 ? p.total_tokens : 1)};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.H * D * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)C};
+    const cuuint32_t elem[2] = {1, 1};
+    const CUresult r = tensor_map_encode_fn()(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.out, dims, strides, box,
+                                              elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    chain_kernel<__nv_bfloat16><<<dim3((unsigned)p.num_seqs, (unsigned)p.H), kChainThreads, kChainSmem, st>>>(p, omap);
     return cudaGetLastError();
 }
 

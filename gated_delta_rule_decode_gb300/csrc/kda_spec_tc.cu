@@ -436,22 +436,22 @@ __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyPar
     if (warp == 0) tc::tmem_dealloc(tm, kTmemCols);
 }
 
-using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
 
-EncodeTiled encode_fn() {
-    static const EncodeTiled fn = [] {
+
+}  // namespace verify_tc
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encode_fn() {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void *f = nullptr;
         cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
                 cudaSuccess ||
             q != cudaDriverEntryPointSuccess)
-            return static_cast<EncodeTiled>(nullptr);
-        return reinterpret_cast<EncodeTiled>(f);
+            return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
     }();
     return fn;
 }
-
-}  // namespace verify_tc
 
 size_t verify_workspace_bytes(int H, int dk, int dv, int dtype, int64_t batch, int D) {
     if (dtype != KDA_DT_BF16 || dk != verify_tc::DK || dv != 128 || D < 1 || D > verify_tc::kDraft || batch <= 0 ||
@@ -463,7 +463,7 @@ size_t verify_workspace_bytes(int H, int dk, int dv, int dtype, int64_t batch, i
 bool verify_tc_supported(const VerifyParams &p, int dk, int dtype) {
     return verify_workspace_bytes(p.H, dk, p.dv, dtype, p.batch, p.D) > 0 && p.workspace != nullptr &&
            p.num_slots > 0 && p.num_slots * (int64_t)p.H <= 0x7fffffffLL &&
-           (int64_t)p.batch * p.H <= 0x7fffffffLL && verify_tc::encode_fn() != nullptr;
+           (int64_t)p.batch * p.H <= 0x7fffffffLL && tensor_map_encode_fn() != nullptr;
 }
 
 cudaError_t launch_verify_tc(const VerifyParams &p, cudaStream_t st) {
@@ -475,7 +475,7 @@ cudaError_t launch_verify_tc(const VerifyParams &p, cudaStream_t st) {
     const cuuint64_t strides[2] = {(cuuint64_t)DK * 4, (cuuint64_t)128 * DK * 4};
     const cuuint32_t box[3] = {32, 128, 1};
     const cuuint32_t elem[3] = {1, 1, 1};
-    const CUresult r = encode_fn()(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(p.pool), dims,
+    const CUresult r = tensor_map_encode_fn()(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(p.pool), dims,
                                    strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;

@@ -27,6 +27,7 @@ KDA_DEVERR_SLOT = 1
 KDA_DEVERR_ACCEPTED = 2
 KDA_DEVERR_SEQLENS = 4
 KDA_DEVERR_TIMEOUT = 8
+KDA_DEVERR_RANGE = 16
 
 EXPORTED = ("kda_decode", "kda_verify_record", "kda_replay_commit",
             "kda_prefill_chunked", "kda_prefill_workspace_bytes",

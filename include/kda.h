@@ -84,7 +84,10 @@ enum {
     KDA_DEVERR_SLOT = 1,      /* slot id >= num_slots                          */
     KDA_DEVERR_ACCEPTED = 2,  /* num_accepted outside 0..draft_len             */
     KDA_DEVERR_SEQLENS = 4,   /* cu_seqlens not non-decreasing / past total_T  */
-    KDA_DEVERR_TIMEOUT = 8    /* an internal bounded wait gave up (prefill)    */
+    KDA_DEVERR_TIMEOUT = 8,   /* an internal bounded wait gave up (prefill)    */
+    KDA_DEVERR_RANGE = 16     /* a value passed to the tensor-core prefill's
+                                 fp16 products exceeded +-65504; the outputs and
+                                 final state of that sequence are not valid  */
 };
 
 typedef struct kda_dims {
