@@ -92,6 +92,16 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src_gmem, uint32_t 
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
 }
 
+// Global -> shared 2-D tensor load (box of the tensor map at (x, y)),
+// completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_addr(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // Shared -> global 2-D tensor store (box of the tensor map at (x, y)) in the
 // thread's bulk group.
 __device__ __forceinline__ void tma_store_2d(const void *map, int x, int y, const void *src_smem) {

@@ -42,6 +42,7 @@
 // than 80 (natural units) around ref on some channel would overflow these
 // factors; that chunk computes A and P with one exp per (r, j, c) instead.
 #include <cuda_fp16.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "kda.h"
@@ -120,18 +121,34 @@ __device__ inline int find_seq(const int32_t *plan, int n, int32_t c) {
 
 // ================================================================== prep
 
-// TMEM columns of the prep kernel (256 per CTA, so two CTAs share an SM):
-// W^T is written over G once G has been read.
-constexpr int PT_BKT = 0, PT_BVT = 64, PT_G = 128, PT_WT = 128, PT_UPT = 192;
+// One CTA of 8 warps per (chunk, head), two CTAs per SM.  TMEM lane l of a
+// warp's quarter is either a token row (row phases: lanes 0..63 the chunk's
+// keys, 64..127 its queries) or a key channel / value row (channel phases);
+// warps w and w + 4 serve the same lanes and take one half of the columns
+// (row phases) or of the tokens (channel phases).
+//
+// The chunk's k, q and g arrive by TMA as K-major 128B-swizzled boxes (the
+// layout of an MMA operand tile, so both row and column reads are free of
+// bank conflicts); v follows into q's buffer once q has been used.  Steps:
+//   1. gamma = running sum of g per channel, in place (first token half, then
+//      the second continuing from gamma_31 = ref); span check
+//   2. L2Norm sums of squares per token row
+//   3. row phase: [K+; Q+] into TMEM (the A operand of the A/P product),
+//      K- into a shared tile (its B operand), Q~ rows of the image
+//   4. channel phase, while G = [K+; Q+] K-^T runs: beta K~^T into TMEM (the
+//      A operand of W^T), K^^T rows of the image
+//   5. A' and P from G; P rows of the image
+//   6. T = (I + A)^-1 by doubling
+//   7. beta V^T into TMEM; W^T = (beta K~)^T T^T, U'^T = (beta V)^T T^T
+//   8. W rows and U'^T rows of the image
+// TMEM columns: [K+; Q+] 0..127 (then beta V^T 0..63 and W^T 64..127),
+// G 128..191 (then U'^T), beta K~^T 192..255.
+constexpr uint32_t PT_A = 0, PT_BV = 0, PT_WT = 64, PT_G = 128, PT_UPT = 128, PT_BK = 192;
 constexpr uint32_t PT_COLS = 256;
-
-// 8 warps: thread (warp w, lane) owns key channel c = 32 (w & 3) + lane, which
-// is also its TMEM lane and its row of the value-side tiles, for the token
-// half 32 (w >> 2) .. 32 (w >> 2) + 31.
 constexpr int kPrepThreads = 256;
 
-// Scratch of the UT inverse, laid over the [K+; Q+] tile once the A/P
-// product that reads it has completed.
+// Scratch of the UT inverse, laid over the k staging and the K- tile once the
+// A/P product and the channel phase have read them.
 struct InvScratch {
     float As[C][C + 1];
     float Ts[C][C + 1];
@@ -139,27 +156,45 @@ struct InvScratch {
 
 struct PrepSmem {
     union {
-        unsigned char bufKQ[128 * 128 * 4];  // [K+; Q+]  (A of the A/P product)
+        struct {
+            unsigned char kst[C * D * 2];  // k: two 64-channel boxes, bf16, 128B-swizzled
+            unsigned char km[C * D * 4];   // K- (B of the A/P product): 64 rows x K 128, tf32
+        } a;
         InvScratch inv;
-    };
+    } u1;
+    unsigned char qv[C * D * 2];           // q, then v (the same box layout as k)
     union {
-        unsigned char bufKM[64 * 128 * 4];   // K-        (B of the A/P product)
-        unsigned char bufT[64 * 64 * 4];     // T         (B of the WY products)
-    };
+        unsigned char gam[C * D * 4];      // g, then gamma in place: four 32-channel fp32 boxes
+        unsigned char t[C * C * 4];        // T (B of the WY products) once gamma is no longer read
+    } u2;
     float invk[C], invq[C], beta[C];
     float nrm[2][2 * C];  // sums of squares over each channel half: rows k_0..k_63, q_0..q_63
     float ref[D];         // gamma at token 31
+    float lo[D], hi[D];   // extremes of gamma over the chunk
     float gC[D];          // gamma at the chunk's last token
-    float egcref[D];      // e^{gamma_C - ref}
+    float eref[D];        // e^{ref}
     float xs[32][33];     // partial products of the UT inverse
-    uint64_t bar;
+    uint64_t bar_in, bar_v, bar_mma;
     uint32_t tmem_base;
 };
 constexpr size_t kPrepSmem = sizeof(PrepSmem) + 1024;
-static_assert(sizeof(InvScratch) <= 128 * 128 * 4, "inverse scratch must fit the [K+; Q+] tile");
+static_assert(sizeof(InvScratch) <= C * D * 6, "inverse scratch must fit the k staging and the K- tile");
+static_assert(offsetof(PrepSmem, qv) % 1024 == 0 && offsetof(PrepSmem, u2) % 1024 == 0, "TMA boxes");
+
+// staged bf16 element (row r, channel c) and fp32 element of a 64-row tile
+__device__ __forceinline__ float st_bf16(const unsigned char *box, int r, int c) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(box + tc::sw128_off16(r, c, C)));
+}
+__device__ __forceinline__ float &st_f32(unsigned char *tile, int r, int c) {
+    return *reinterpret_cast<float *>(tile + tc::sw128_off(r, c, C));
+}
 
 template <typename T>
-__global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillParams p,
+                                                                   const __grid_constant__ CUtensorMap kmap,
+                                                                   const __grid_constant__ CUtensorMap qmap,
+                                                                   const __grid_constant__ CUtensorMap vmap,
+                                                                   const __grid_constant__ CUtensorMap gmap) {
     extern __shared__ unsigned char smem_raw[];
     PrepSmem &sm =
         *reinterpret_cast<PrepSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -172,266 +207,303 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
     const int s = find_seq(plan, n, chunk);
     const int slot = p.slot_ids[s];
     if (slot < 0 || (int64_t)slot >= p.num_slots) return;  // the chain writes zeros
-    const int64_t t0 = (int64_t)p.cu_seqlens[s] + (int64_t)(chunk - plan[s]) * C;
-    const int L = (int)((int64_t)p.cu_seqlens[s + 1] - t0 < C ? (int64_t)p.cu_seqlens[s + 1] - t0 : C);
+    const int t0 = p.cu_seqlens[s] + (chunk - plan[s]) * C;
+    const int L = p.cu_seqlens[s + 1] - t0 < C ? p.cu_seqlens[s + 1] - t0 : C;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = ((warp & 3) << 5) | lane;  // key channel = TMEM lane
-    const int rb = 32 * (warp >> 2);          // first token of this thread's half
-    const T *__restrict__ q = static_cast<const T *>(p.q);
-    const T *__restrict__ k = static_cast<const T *>(p.k);
-    const T *__restrict__ v = static_cast<const T *>(p.v);
-    const T *__restrict__ bb = static_cast<const T *>(p.b);
-    const float *__restrict__ gptr = p.g;
-    const int64_t tok_stride = (int64_t)H * D, hoff = (int64_t)h * D;
+    const int lr = ((warp & 3) << 5) | lane;  // TMEM lane
+    const int hf = warp >> 2;                 // half of the columns or tokens
     unsigned char *__restrict__ img = static_cast<unsigned char *>(p.workspace) + plan_bytes(n) +
                                       ((size_t)chunk * H + h) * (size_t)IMG_BYTES;
+    unsigned char *kst = sm.u1.a.kst, *km = sm.u1.a.km, *qv = sm.qv, *gam = sm.u2.gam;
 
     if (warp == 0) tc::tmem_alloc(&sm.tmem_base, PT_COLS);
     if (tid == 0) {
-        mbar_init(&sm.bar, 1);
+        mbar_init(&sm.bar_in, 1);
+        mbar_init(&sm.bar_v, 1);
+        mbar_init(&sm.bar_mma, 1);
         fence_barrier_init();
-    }
-
-    // this channel's gates over its token half, in flight during the norms
-    float gh[32];
+        mbar_arrive_expect_tx(&sm.bar_in, 2 * (C * D * 2) + C * D * 4);  // k, q (bf16) and g (fp32)
+        tma_load_2d(kst, &kmap, h * D, t0, &sm.bar_in);
+        tma_load_2d(kst + C * 128, &kmap, h * D + 64, t0, &sm.bar_in);
+        tma_load_2d(qv, &qmap, h * D, t0, &sm.bar_in);
+        tma_load_2d(qv + C * 128, &qmap, h * D + 64, t0, &sm.bar_in);
 #pragma unroll
-    for (int r = 0; r < 32; ++r) gh[r] = (rb + r < L) ? __ldg(gptr + (t0 + rb + r) * tok_stride + hoff + c) : 0.f;
-
-    // ---- 1a. sums of squares: thread = (row of k or q, half of the channels);
-    // the loop is unrolled so that the row is in flight at once
-    {
-        const int row = tid & (2 * C - 1), ch = tid >> 7;
-        const int r = row & (C - 1);
-        float ss = 0.f;
-        if (r < L) {
-            const T *src = (row >= C ? q : k) + (t0 + r) * tok_stride + hoff + 64 * ch;
-#pragma unroll
-            for (int j = 0; j < 64; j += 4) {
-                const float4 x = Elem<T>::load4(src + j);
-                ss = fmaf(x.x, x.x, ss);
-                ss = fmaf(x.y, x.y, ss);
-                ss = fmaf(x.z, x.z, ss);
-                ss = fmaf(x.w, x.w, ss);
-            }
-        }
-        sm.nrm[ch][row] = ss;
+        for (int i = 0; i < 4; ++i) tma_load_2d(gam + i * C * 128, &gmap, h * D + 32 * i, t0, &sm.bar_in);
     }
-    // ---- 1b. gamma (thread = key channel c): the first half's running sum
-    // ends at ref = gamma_31; the second half continues it from there.  Rows
-    // past the chunk's end repeat gamma_C.
-    float acc = 0.f, gmin = 0.f, gmax = 0.f, gC = 0.f;
-    if (rb == 0) {
-#pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            acc += gh[r];
-            if (r == L - 1) gC = acc;
-            gmin = r == 0 ? acc : fminf(gmin, acc);
-            gmax = r == 0 ? acc : fmaxf(gmax, acc);
-        }
-        sm.ref[c] = acc;
-        if (L <= 32) sm.gC[c] = gC;
-    }
+    const T *__restrict__ bb = static_cast<const T *>(p.b);
+    const float bval = (tid < L) ? Elem<T>::load1(bb + (int64_t)(t0 + tid) * H + h) : 0.f;
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (tid < 2 * C) {
-        const int r = tid & (C - 1);
-        const float inv = (r < L) ? rsqrtf(sm.nrm[0][tid] + sm.nrm[1][tid] + p.eps) : 0.f;
-        if (tid >= C) {
-            sm.invq[r] = inv;
-        } else {
-            sm.invk[r] = inv;
-            sm.beta[r] = (r < L) ? sigmoid_f(Elem<T>::load1(bb + (t0 + r) * H + h)) : 0.f;
-        }
-    }
-    const float ref = sm.ref[c];
-    if (rb == 32) {
-        acc = ref;
-#pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            acc += gh[r];
-            if (32 + r == L - 1) gC = acc;
-            gmin = r == 0 ? acc : fminf(gmin, acc);
-            gmax = r == 0 ? acc : fmaxf(gmax, acc);
-        }
-        if (L > 32) sm.gC[c] = gC;
-    }
-    const float span = fmaxf(gmax - ref, ref - gmin);
-    const bool unsafe = __syncthreads_or(span > kSpanLimit) != 0;
-    gC = sm.gC[c];
-    if (rb == 0) {
-        reinterpret_cast<float *>(img + IMG_EGC)[c] = expf(gC);
-        sm.egcref[c] = expf(gC - ref);
-    }
     const uint32_t tm = sm.tmem_base;
     uint32_t phase = 0;
-
-    // ---- 2. this thread's 32 tokens, 8 at a time; the next block's loads are
-    // in flight while the current block computes
-    {
-        const float eref = expf(ref);
-        acc = rb == 0 ? 0.f : ref;
-        float kb[8], qb[8], vb[8], gb[8];
-        auto load_block = [&](int r0, float (&kk)[8], float (&qq)[8], float (&vv)[8], float (&gg)[8]) {
-#pragma unroll
-            for (int rr = 0; rr < 8; ++rr) {
-                const bool ok_r = rb + r0 + rr < L;
-                const int64_t off = (t0 + rb + r0 + rr) * tok_stride + hoff + c;
-                kk[rr] = ok_r ? Elem<T>::load1(k + off) : 0.f;
-                qq[rr] = ok_r ? Elem<T>::load1(q + off) : 0.f;
-                vv[rr] = ok_r ? Elem<T>::load1(v + off) : 0.f;
-                gg[rr] = ok_r ? __ldg(gptr + off) : 0.f;
-            }
-        };
-        load_block(0, kb, qb, vb, gb);
-        // swizzled stores of channel c in rows rb + r0 + rr: the row's low
-        // three bits are rr (rb and r0 are multiples of 8), so the 16-byte
-        // chunk is (c's chunk) ^ rr and only the block's first row varies
-        const uint32_t cpart = (uint32_t)((c & 3) << 2), cx4 = (uint32_t)(((c & 31) >> 2) << 4);
-        unsigned char *const kq0 = sm.bufKQ + (c >> 5) * 128 * 128 + cpart;
-        unsigned char *const km0 = sm.bufKM + (c >> 5) * 64 * 128 + cpart;
-#pragma unroll 1
-        for (int r0 = 0; r0 < 32; r0 += 8) {
-            float nk[8], nq[8], nv[8], ng[8];
-            if (r0 + 8 < 32) load_block(r0 + 8, nk, nq, nv, ng);
-            float bkt[8], bvt[8];
-            const int rowb = (rb + r0) * 128;
-#pragma unroll
-            for (int rr = 0; rr < 8; ++rr) {
-                const int r = rb + r0 + rr;
-                const bool valid = r < L;
-                const uint32_t sw = (cx4 ^ (uint32_t)(rr << 4)) + rr * 128;
-                acc += gb[rr];
-                const float gam = acc;
-                const float kx = kb[rr] * sm.invk[r];
-                const float qx = qb[rr] * sm.invq[r];
-                float ktil, qtil;
-                if (!unsafe) {
-                    const float E = __expf(gam - ref);
-                    const float Ei = __expf(ref - gam);
-                    const float kp = kx * E, qp = qx * E;
-                    *reinterpret_cast<float *>(kq0 + rowb + sw) = kp;
-                    *reinterpret_cast<float *>(kq0 + rowb + 64 * 128 + sw) = qp;
-                    *reinterpret_cast<float *>(km0 + rowb + sw) = kx * Ei;
-                    ktil = kp * eref;
-                    qtil = qp * eref;
-                } else {
-                    // plain [64][128] copies of k^, q^ and gamma for the exact path
-                    reinterpret_cast<float *>(sm.bufKQ)[r * D + c] = kx;
-                    reinterpret_cast<float *>(sm.bufKQ)[C * D + r * D + c] = qx;
-                    reinterpret_cast<float *>(sm.bufKM)[r * D + c] = gam;
-                    const float eg = expf(gam);
-                    ktil = kx * eg;
-                    qtil = qx * eg;
-                    st_h(img + IMG_KT, 128, c, r, valid ? kx * expf(gC - gam) : 0.f);
-                }
-                st_h(img + IMG_BW, 128, 64 + r, c, qtil);  // Q~ rows of [W; Q~]
-                bkt[rr] = sm.beta[r] * ktil;
-                bvt[rr] = sm.beta[r] * vb[rr];
-            }
-            tc::st8(tc::lane_addr(tm, warp, PT_BKT + rb + r0), bkt);
-            tc::st8(tc::lane_addr(tm, warp, PT_BVT + rb + r0), bvt);
-#pragma unroll
-            for (int rr = 0; rr < 8; ++rr) {
-                kb[rr] = nk[rr];
-                qb[rr] = nq[rr];
-                vb[rr] = nv[rr];
-                gb[rr] = ng[rr];
-            }
-        }
+    // outstanding asynchronous work, for the drain after a timeout
+    bool in_pend = true, v_pend = false, mma_pend = false;
+    bool ok = __syncthreads_and(tid == 0 ? mbar_wait(&sm.bar_in, 0) : true) != 0;
+    if (ok) {
+        in_pend = false;
+        mbar_try_wait(&sm.bar_in, 0);
+    } else if (tid == 0 && p.err_flag) {
+        atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
     }
-    tc::wait_st();
-    sync_for_mma();
-
-    bool ok = true;
     bool big = false;  // a W entry beyond the fp16 range of the chain's operands
-    // ---- 3. A and P
-    if (!unsafe) {
-        if (tid == 0) {
-            constexpr uint32_t id = tc::idesc_tf32(128, 64);
-            const uint32_t a0 = tc::smem_u32(sm.bufKQ), b0 = tc::smem_u32(sm.bufKM);
-#pragma unroll
-            for (int ks = 0; ks < D / 8; ++ks)
-                tc::mma_tf32_ss(tm + PT_G, tc::desc_tf32_kstep(a0, 128, ks), tc::desc_tf32_kstep(b0, 64, ks), id,
-                                ks > 0);
-            tc::commit(&sm.bar);
-        }
-        ok = wait_mma(&sm.bar, phase, p.err_flag);
-        if (ok) {
-            // the K^^T image tile, transposed out of K- (K^ = K- e^{gamma_C - ref})
-            // now that its product has completed: warp w writes rows
-            // 16 w .. 16 w + 15 of both 32-token halves, one token per lane, so
-            // every store is one 128-byte line
-#pragma unroll 4
-            for (int it = 0; it < 32; ++it) {
-                const int cc = 16 * warp + (it >> 1);
-                const int r = 32 * (it & 1) + lane;
-                const float km = *reinterpret_cast<const float *>(sm.bufKM + tc::sw128_off(r, cc, 64));
-                st_h(img + IMG_KT, 128, cc, r, r < L ? km * sm.egcref[cc] : 0.f);
-            }
-            // G rows (TMEM lanes): 0..63 are A', 64..127 are P; warp w takes
-            // columns 32 (w >> 2) .. 32 (w >> 2) + 31
-            const int grow = c, r = grow & (C - 1), j0 = rb;
-            float g16[16];
-#pragma unroll
-            for (int jb = 0; jb < 32; jb += 16) {
-                tc::ld16(tc::lane_addr(tm, warp, PT_G + j0 + jb), g16);
-                tc::wait_ld();
-                if (grow < C) {
-#pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int j = j0 + jb + jj;
-                        sm.inv.As[r][j] = (j < r) ? sm.beta[r] * g16[jj] : 0.f;
-                    }
-                } else {
-#pragma unroll
-                    for (int jj = 0; jj < 16; jj += 4) {
-                        const int j = j0 + jb + jj;
-                        *reinterpret_cast<uint2 *>(img + IMG_P + tc::sw128_off16(r, j, 64)) =
-                            make_uint2(pack_h2(j <= r ? g16[jj] : 0.f, j + 1 <= r ? g16[jj + 1] : 0.f),
-                                       pack_h2(j + 2 <= r ? g16[jj + 2] : 0.f, j + 3 <= r ? g16[jj + 3] : 0.f));
-                    }
-                }
-            }
-        }
-    } else {
-        // exact path; A goes to registers first because its scratch overlays k^
-        const float *kh = reinterpret_cast<const float *>(sm.bufKQ);
-        const float *qh = kh + C * D;
-        const float *gm = reinterpret_cast<const float *>(sm.bufKM);
-        float areg[C * C / kPrepThreads];
-#pragma unroll 1
-        for (int it = 0; it < C * C / kPrepThreads; ++it) {
-            const int idx = tid + it * kPrepThreads;
-            const int r = idx / C, j = idx % C;
-            float a = 0.f, pp = 0.f;
-            if (j <= r) {
-                for (int cc = 0; cc < D; ++cc) {
-                    const float m = kh[j * D + cc] * expf(gm[r * D + cc] - gm[j * D + cc]);
-                    a = fmaf(kh[r * D + cc], m, a);
-                    pp = fmaf(qh[r * D + cc], m, pp);
-                }
-            }
-            areg[it] = (j < r) ? sm.beta[r] * a : 0.f;
-            st_h(img + IMG_P, 64, r, j, (j <= r) ? pp : 0.f);
-        }
-        __syncthreads();
-#pragma unroll
-        for (int it = 0; it < C * C / kPrepThreads; ++it) {
-            const int idx = tid + it * kPrepThreads;
-            sm.inv.As[idx / C][idx % C] = areg[it];
-        }
-    }
-    __syncthreads();
+    bool unsafe = false;
+    auto issue_v = [&]() {  // thread 0, once q has been read
+        mbar_arrive_expect_tx(&sm.bar_v, C * D * 2);
+        tma_load_2d(qv, &vmap, h * D, t0, &sm.bar_v);
+        tma_load_2d(qv + C * 128, &vmap, h * D + 64, t0, &sm.bar_v);
+    };
 
     if (ok) {
-        // ---- 4. T = (I + A)^-1 (unit lower triangular) by doubling: the four
+        // ---- 1. L2Norm sums of squares (thread = row of k (0..63) or q, one
+        // 64-channel half; the 16-byte units of a row are read in its swizzled
+        // order, so a warp's rows hit distinct banks)
+        {
+            const int row = tid & 127, ch = tid >> 7;
+            const int r = row & 63;
+            const unsigned char *box = (row < 64 ? kst : qv) + ch * C * 128;
+            float ss = 0.f;
+            if (r < L) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(box + r * 128 + ((u ^ (r & 7)) << 4));
+                    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float a = __uint_as_float(w4[e] << 16), b = __uint_as_float(w4[e] & 0xffff0000u);
+                        ss = fmaf(a, a, ss);
+                        ss = fmaf(b, b, ss);
+                    }
+                }
+            }
+            sm.nrm[ch][row] = ss;
+        }
+        // ---- 2. gamma, in place (thread = channel lr): tokens 0..31 (running
+        // sum ending at ref = gamma_31), then 32..63 continuing from ref; rows
+        // past the chunk's end repeat gamma_C
+        float gmin = 0.f, gmax = 0.f, gc = 0.f;
+        if (hf == 0) {
+            float acc = 0.f;
+#pragma unroll 8
+            for (int r = 0; r < 32; ++r) {
+                float &g = st_f32(gam, r, lr);
+                acc += r < L ? g : 0.f;
+                g = acc;
+                if (r == L - 1) gc = acc;
+                gmin = r == 0 ? acc : fminf(gmin, acc);
+                gmax = r == 0 ? acc : fmaxf(gmax, acc);
+            }
+            sm.ref[lr] = acc;
+            sm.lo[lr] = gmin;
+            sm.hi[lr] = gmax;
+            if (L <= 32) sm.gC[lr] = gc;
+        }
+        __syncthreads();
+        if (hf == 1) {
+            const float ref = sm.ref[lr];
+            float acc = ref;
+            gmin = sm.lo[lr];
+            gmax = sm.hi[lr];
+#pragma unroll 8
+            for (int r = 32; r < 64; ++r) {
+                float &g = st_f32(gam, r, lr);
+                acc += r < L ? g : 0.f;
+                g = acc;
+                if (r == L - 1) gc = acc;
+                gmin = fminf(gmin, acc);
+                gmax = fmaxf(gmax, acc);
+            }
+            if (L > 32) sm.gC[lr] = gc;
+            const float gCv = L > 32 ? gc : sm.gC[lr];
+            unsafe = fmaxf(gmax - ref, ref - gmin) > kSpanLimit;
+            reinterpret_cast<float *>(img + IMG_EGC)[lr] = expf(gCv);
+            sm.eref[lr] = expf(ref);
+        } else {
+            // (thread = k row, then q row) the norms and beta
+            const int r = tid & (C - 1);
+            const float inv = (r < L) ? rsqrtf(sm.nrm[0][tid] + sm.nrm[1][tid] + p.eps) : 0.f;
+            if (tid >= C) {
+                sm.invq[r] = inv;
+            } else {
+                sm.invk[r] = inv;
+                sm.beta[r] = (r < L) ? sigmoid_f(bval) : 0.f;
+            }
+        }
+        unsafe = __syncthreads_or(unsafe) != 0;
+
+        // ---- 3. row phase (thread = token row lr of k (lr < 64) or of q,
+        // channels 64 hf .. 64 hf + 63, eight at a time)
+        {
+            const int tok = lr & (C - 1);
+            const bool isq = lr >= C;
+            const float inv = isq ? sm.invq[tok] : sm.invk[tok];
+            const unsigned char *box = (isq ? qv : kst) + hf * C * 128;
+#pragma unroll 1
+            for (int u = 0; u < 8; ++u) {
+                const int c0 = 64 * hf + 8 * u;
+                const uint4 raw = *reinterpret_cast<const uint4 *>(box + tok * 128 + ((u ^ (tok & 7)) << 4));
+                const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+                float x[8], gm[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    x[2 * e] = __uint_as_float(w4[e] << 16) * inv;
+                    x[2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u) * inv;
+                }
+                {
+                    const float4 g0 = *reinterpret_cast<const float4 *>(gam + tc::sw128_off(tok, c0, C));
+                    const float4 g1 = *reinterpret_cast<const float4 *>(gam + tc::sw128_off(tok, c0 + 4, C));
+                    gm[0] = g0.x; gm[1] = g0.y; gm[2] = g0.z; gm[3] = g0.w;
+                    gm[4] = g1.x; gm[5] = g1.y; gm[6] = g1.z; gm[7] = g1.w;
+                }
+                float plus[8], qt[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    if (!unsafe) {
+                        plus[e] = x[e] * __expf(gm[e] - sm.ref[c0 + e]);
+                        qt[e] = plus[e] * sm.eref[c0 + e];
+                    } else {
+                        plus[e] = 0.f;
+                        qt[e] = x[e] * expf(gm[e]);
+                    }
+                }
+                if (!unsafe) {
+                    tc::st8(tc::lane_addr(tm, warp, PT_A + c0), plus);  // [K+; Q+] row lr
+                    if (!isq) {
+                        float mi[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) mi[e] = x[e] * __expf(sm.ref[c0 + e] - gm[e]);
+                        *reinterpret_cast<float4 *>(km + tc::sw128_off(tok, c0, C)) =
+                            make_float4(mi[0], mi[1], mi[2], mi[3]);
+                        *reinterpret_cast<float4 *>(km + tc::sw128_off(tok, c0 + 4, C)) =
+                            make_float4(mi[4], mi[5], mi[6], mi[7]);
+                    }
+                }
+                if (isq)  // Q~ = q^ e^{gamma}: row 64 + tok of [W; Q~], one 16-byte unit
+                    *reinterpret_cast<uint4 *>(img + IMG_BW + tc::sw128_off16(C + tok, c0, 128)) =
+                        make_uint4(pack_h2(qt[0], qt[1]), pack_h2(qt[2], qt[3]), pack_h2(qt[4], qt[5]),
+                                   pack_h2(qt[6], qt[7]));
+            }
+        }
+        tc::wait_st();
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (!unsafe) {
+            if (tid == 0) {
+                // G = [K+; Q+] K-^T: M = 128, N = 64, K = 128 (kind::tf32)
+                constexpr uint32_t id = tc::idesc_tf32(128, 64);
+                const uint32_t b0 = tc::smem_u32(km);
+#pragma unroll
+                for (int ks = 0; ks < D / 8; ++ks)
+                    tc::mma_tf32_ts(tm + PT_G, tm + PT_A + 8 * ks, tc::desc_tf32_kstep(b0, 64, ks), id, ks > 0);
+                tc::commit(&sm.bar_mma);
+                issue_v();  // q has been read: v takes its buffer
+            }
+            mma_pend = v_pend = true;
+        }
+
+        // ---- 4. channel phase (thread = channel lr, tokens 32 hf .. + 31):
+        // beta K~^T into TMEM, K^^T row lr of the image
+        {
+            const float gCv = sm.gC[lr];
+            float bk[32];
+            uint32_t kw[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                float kh2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int r = 32 * hf + i + e;
+                    const float kx = st_bf16(kst, r, lr) * sm.invk[r];
+                    const float g = st_f32(gam, r, lr);
+                    bk[i + e] = sm.beta[r] * kx * __expf(g);
+                    kh2[e] = r < L ? kx * __expf(gCv - g) : 0.f;
+                }
+                kw[i >> 1] = pack_h2(kh2[0], kh2[1]);
+            }
+            tc::st16(tc::lane_addr(tm, warp, PT_BK + 32 * hf), *reinterpret_cast<float(*)[16]>(&bk[0]));
+            tc::st16(tc::lane_addr(tm, warp, PT_BK + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(&bk[16]));
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4 *>(img + IMG_KT + tc::sw128_off16(lr, 32 * hf + 8 * j, 128)) =
+                    make_uint4(kw[4 * j], kw[4 * j + 1], kw[4 * j + 2], kw[4 * j + 3]);
+        }
+
+        // ---- 5. A' and P
+        if (!unsafe) {
+            ok = wait_mma(&sm.bar_mma, phase, p.err_flag);
+            if (ok) {
+                mma_pend = false;
+                // G rows (TMEM lanes): 0..63 are A', 64..127 are P; columns
+                // (tokens j) 32 hf .. + 31
+                float g32[32];
+                tc::ld16(tc::lane_addr(tm, warp, PT_G + 32 * hf), *reinterpret_cast<float(*)[16]>(&g32[0]));
+                tc::ld16(tc::lane_addr(tm, warp, PT_G + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(&g32[16]));
+                tc::wait_ld();
+                if (lr < C) {
+                    const int r = lr;
+                    const float br = sm.beta[r];
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int j = 32 * hf + jj;
+                        sm.u1.inv.As[r][j] = (j < r) ? br * g32[jj] : 0.f;
+                    }
+                } else {
+                    const int r = lr - C;
+#pragma unroll
+                    for (int j8 = 0; j8 < 4; ++j8) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = 32 * hf + 8 * j8 + 2 * e;
+                            w[e] = pack_h2(j <= r ? g32[8 * j8 + 2 * e] : 0.f, j + 1 <= r ? g32[8 * j8 + 2 * e + 1] : 0.f);
+                        }
+                        *reinterpret_cast<uint4 *>(img + IMG_P + tc::sw128_off16(r, 32 * hf + 8 * j8, 64)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+        } else {
+            // exact path: one exp per (r, j, c); A goes to registers first
+            // because its scratch overlays the k staging
+            float areg[C * C / kPrepThreads];
+#pragma unroll 1
+            for (int it = 0; it < C * C / kPrepThreads; ++it) {
+                const int idx = tid + it * kPrepThreads;
+                const int r = idx / C, j = idx % C;
+                float a = 0.f, pp = 0.f;
+                if (j <= r) {
+                    for (int cc = 0; cc < D; ++cc) {
+                        const float gr = st_f32(gam, r, cc), gj = st_f32(gam, j, cc);
+                        const float m = st_bf16(kst, j, cc) * sm.invk[j] * expf(gr - gj);
+                        a = fmaf(st_bf16(kst, r, cc) * sm.invk[r], m, a);
+                        pp = fmaf(st_bf16(qv, r, cc) * sm.invq[r], m, pp);
+                    }
+                }
+                areg[it] = (j < r) ? sm.beta[r] * a : 0.f;
+                st_h(img + IMG_P, 64, r, j, (j <= r) ? pp : 0.f);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int it = 0; it < C * C / kPrepThreads; ++it) {
+                const int idx = tid + it * kPrepThreads;
+                sm.u1.inv.As[idx / C][idx % C] = areg[it];
+            }
+            if (tid == 0) issue_v();
+            v_pend = true;
+        }
+        __syncthreads();
+    }
+
+    if (ok) {
+        // ---- 6. T = (I + A)^-1 (unit lower triangular) by doubling: the four
         // 16 x 16 diagonal blocks by forward substitution (one column per
         // thread, in registers); then the lower-left 16 x 16 block of each
         // 32-row block as -T22 (A21 T11); then the lower-left 32 x 32 block of
-        // the whole matrix the same way.
-        float(*As)[C + 1] = sm.inv.As;
-        float(*Ts)[C + 1] = sm.inv.Ts;
+        // the whole matrix the same way
+        float(*As)[C + 1] = sm.u1.inv.As;
+        float(*Ts)[C + 1] = sm.u1.inv.Ts;
         if (tid < C) {
             const int I = tid >> 4, jj = tid & 15, o = 16 * I;
             float col[16];
@@ -446,14 +518,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
 #pragma unroll
             for (int r = 0; r < 16; ++r) Ts[o + r][o + jj] = col[r];
         } else {
-            // zero the blocks above the diagonal
             for (int idx = tid - C; idx < C * C; idx += kPrepThreads - C) {
                 const int r = idx / C, j = idx % C;
                 if ((j >> 4) > (r >> 4)) Ts[r][j] = 0.f;
             }
         }
         __syncthreads();
-        // level 1: both 32-row blocks at once (o = 0, 32)
         for (int idx = tid; idx < 2 * 256; idx += kPrepThreads) {
             const int o = 32 * (idx >> 8), r = (idx >> 4) & 15, j = idx & 15;
             float x0 = 0.f, x1 = 0.f;
@@ -474,7 +544,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             Ts[o + 16 + r][o + j] = -t;
         }
         __syncthreads();
-        // level 2: the 32 x 32 blocks
         for (int idx = tid; idx < 32 * 32; idx += kPrepThreads) {
             const int r = idx >> 5, j = idx & 31;
             float x0 = 0.f, x1 = 0.f;
@@ -488,63 +557,92 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         __syncthreads();
         for (int idx = tid; idx < 32 * 32; idx += kPrepThreads) {
             const int r = idx >> 5, j = idx & 31;
-            float t0 = 0.f, t1 = 0.f;
+            float t0v = 0.f, t1v = 0.f;
 #pragma unroll
             for (int m = 0; m < 32; m += 2) {
-                if (m <= r) t0 = fmaf(Ts[32 + r][32 + m], sm.xs[m][j], t0);
-                if (m + 1 <= r) t1 = fmaf(Ts[32 + r][32 + m + 1], sm.xs[m + 1][j], t1);
+                if (m <= r) t0v = fmaf(Ts[32 + r][32 + m], sm.xs[m][j], t0v);
+                if (m + 1 <= r) t1v = fmaf(Ts[32 + r][32 + m + 1], sm.xs[m + 1][j], t1v);
             }
-            Ts[32 + r][j] = -(t0 + t1);
+            Ts[32 + r][j] = -(t0v + t1v);
         }
         __syncthreads();
+        // T into its swizzled tile (over gamma, which nothing reads any more)
         for (int idx = tid; idx < C * C / 4; idx += kPrepThreads) {
             const int r = idx / (C / 4), j = (idx % (C / 4)) * 4;
-            *reinterpret_cast<float4 *>(sm.bufT + tc::sw128_off(r, j, 64)) =
-                make_float4(sm.inv.Ts[r][j], sm.inv.Ts[r][j + 1], sm.inv.Ts[r][j + 2], sm.inv.Ts[r][j + 3]);
+            *reinterpret_cast<float4 *>(sm.u2.t + tc::sw128_off(r, j, 64)) =
+                make_float4(Ts[r][j], Ts[r][j + 1], Ts[r][j + 2], Ts[r][j + 3]);
         }
-        sync_for_mma();
-
-        // ---- 5. W^T = (beta K~)^T T^T and U'^T = (beta V)^T T^T
+        // ---- 7. beta V^T into TMEM (thread = value row lr, tokens 32 hf ..)
+        ok = __syncthreads_and(tid == 0 ? mbar_wait(&sm.bar_v, 0) : true) != 0;
+        if (ok) {
+            v_pend = false;
+            mbar_try_wait(&sm.bar_v, 0);
+            float bv[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int r = 32 * hf + i;
+                bv[i] = r < L ? sm.beta[r] * st_bf16(qv, r, lr) : 0.f;
+            }
+            tc::st16(tc::lane_addr(tm, warp, PT_BV + 32 * hf), *reinterpret_cast<float(*)[16]>(&bv[0]));
+            tc::st16(tc::lane_addr(tm, warp, PT_BV + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(&bv[16]));
+            tc::wait_st();
+        } else if (tid == 0 && p.err_flag) {
+            atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
+        }
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+    }
+    if (ok) {
+        // ---- W^T = (beta K~)^T T^T and U'^T = (beta V)^T T^T
         if (tid == 0) {
             constexpr uint32_t id = tc::idesc_tf32(128, 64);
-            const uint32_t b0 = tc::smem_u32(sm.bufT);
+            const uint32_t b0 = tc::smem_u32(sm.u2.t);
 #pragma unroll
             for (int ks = 0; ks < C / 8; ++ks) {
                 const uint64_t bd = tc::desc_tf32_kstep(b0, 64, ks);
-                tc::mma_tf32_ts(tm + PT_WT, tm + PT_BKT + 8 * ks, bd, id, ks > 0);
-                tc::mma_tf32_ts(tm + PT_UPT, tm + PT_BVT + 8 * ks, bd, id, ks > 0);
+                tc::mma_tf32_ts(tm + PT_WT, tm + PT_BK + 8 * ks, bd, id, ks > 0);
+                tc::mma_tf32_ts(tm + PT_UPT, tm + PT_BV + 8 * ks, bd, id, ks > 0);
             }
-            tc::commit(&sm.bar);
+            tc::commit(&sm.bar_mma);
         }
-        ok = wait_mma(&sm.bar, phase, p.err_flag);
+        mma_pend = true;
+        ok = wait_mma(&sm.bar_mma, phase, p.err_flag);
         if (ok) {
-            // lane c: W[r][c] and U'[r][c] for this thread's token half; W goes
-            // to its swizzled tile, U' to row c of U'^T in 16-byte units of
-            // four tokens, unit u at (u & 8) | ((u & 7) ^ (c & 7)) so that the
-            // chain's shared-memory reads of eight rows hit distinct banks
-            float w16[16];
-            unsigned char *up = img + IMG_UP + (size_t)c * C * 4;
+            mma_pend = false;
+            // ---- 8. lane lr: W[r][lr] (column lr of the W rows of [W; Q~])
+            // and U'[r][lr] (row lr of U'^T, 16-byte units of four tokens at
+            // (u & 8) | ((u & 7) ^ (lr & 7))), tokens 32 hf .. + 31
+            unsigned char *up = img + IMG_UP + (size_t)lr * C * 4;
 #pragma unroll
             for (int r0 = 0; r0 < 32; r0 += 16) {
-                tc::ld16(tc::lane_addr(tm, warp, PT_WT + rb + r0), w16);
+                float w16[16];
+                tc::ld16(tc::lane_addr(tm, warp, PT_WT + 32 * hf + r0), w16);
                 tc::wait_ld();
 #pragma unroll
                 for (int rr = 0; rr < 16; ++rr) {
                     big |= !(fabsf(w16[rr]) <= kHalfMax) && w16[rr] == w16[rr];
-                    st_h(img + IMG_BW, 128, rb + r0 + rr, c, w16[rr]);
+                    st_h(img + IMG_BW, 128, 32 * hf + r0 + rr, lr, w16[rr]);
                 }
-                tc::ld16(tc::lane_addr(tm, warp, PT_UPT + rb + r0), w16);
+                tc::ld16(tc::lane_addr(tm, warp, PT_UPT + 32 * hf + r0), w16);
                 tc::wait_ld();
 #pragma unroll
                 for (int rr = 0; rr < 16; rr += 4) {
-                    const int u = (rb + r0 + rr) >> 2;
-                    *reinterpret_cast<float4 *>(up + (((u & 8) | ((u & 7) ^ (c & 7))) << 4)) =
+                    const int u = (32 * hf + r0 + rr) >> 2;
+                    *reinterpret_cast<float4 *>(up + (((u & 8) | ((u & 7) ^ (lr & 7))) << 4)) =
                         make_float4(w16[rr], w16[rr + 1], w16[rr + 2], w16[rr + 3]);
                 }
             }
         }
     }
-    if (!ok) mbar_wait_drain(&sm.bar, phase & 1);  // the product whose wait gave up
+    if (!ok && tid == 0) {
+        // let every copy and product still in flight finish before the CTA
+        // releases its memory
+        if (in_pend) mbar_wait_drain(&sm.bar_in, 0);
+        if (v_pend) mbar_wait_drain(&sm.bar_v, 0);
+        if (mma_pend) mbar_wait_drain(&sm.bar_mma, phase & 1);
+    }
     if (__syncthreads_or(big) && tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_RANGE);
     tc::fence_before_sync();
     __syncthreads();
@@ -891,8 +989,28 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
                              (int)kChainSmem);
     if (e != cudaSuccess) return e;
     const int64_t mc = max_chunks(p.num_seqs, p.total_tokens);
-    if (mc > 0) {
-        prep_tc_kernel<__nv_bfloat16><<<dim3((unsigned)mc, (unsigned)p.H), kPrepThreads, kPrepSmem, st>>>(p);
+    if (mc > 0 && p.total_tokens > 0) {
+        // the token inputs as [total_tokens][H * 128] tensors, boxes of 64
+        // tokens x 64 channels (bf16) or 32 channels (g, fp32), 128B-swizzled
+        CUtensorMap kmap, qmap, vmap, gmap;
+        const cuuint64_t dims[2] = {(cuuint64_t)p.H * D, (cuuint64_t)p.total_tokens};
+        const cuuint64_t sb[1] = {(cuuint64_t)p.H * D * 2}, sf[1] = {(cuuint64_t)p.H * D * 4};
+        const cuuint32_t boxb[2] = {64, (cuuint32_t)C}, boxf[2] = {32, (cuuint32_t)C};
+        const cuuint32_t elem[2] = {1, 1};
+        const void *srcs[3] = {p.k, p.q, p.v};
+        CUtensorMap *maps[3] = {&kmap, &qmap, &vmap};
+        for (int i = 0; i < 3; ++i)
+            if (tensor_map_encode_fn()(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(srcs[i]), dims,
+                                       sb, boxb, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return cudaErrorInvalidValue;
+        if (tensor_map_encode_fn()(&gmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(p.g), dims, sf, boxf,
+                                   elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        prep_tc_kernel<__nv_bfloat16>
+            <<<dim3((unsigned)mc, (unsigned)p.H), kPrepThreads, kPrepSmem, st>>>(p, kmap, qmap, vmap, gmap);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
