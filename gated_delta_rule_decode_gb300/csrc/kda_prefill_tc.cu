@@ -355,14 +355,25 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                     gm[0] = g0.x; gm[1] = g0.y; gm[2] = g0.z; gm[3] = g0.w;
                     gm[4] = g1.x; gm[5] = g1.y; gm[6] = g1.z; gm[7] = g1.w;
                 }
-                float plus[8], qt[8];
+                float plus[8], qt[8], ei[8];
+                if (!unsafe) {
+                    float rf[8], er[8];
+                    *reinterpret_cast<float4 *>(&rf[0]) = *reinterpret_cast<const float4 *>(&sm.ref[c0]);
+                    *reinterpret_cast<float4 *>(&rf[4]) = *reinterpret_cast<const float4 *>(&sm.ref[c0 + 4]);
+                    *reinterpret_cast<float4 *>(&er[0]) = *reinterpret_cast<const float4 *>(&sm.eref[c0]);
+                    *reinterpret_cast<float4 *>(&er[4]) = *reinterpret_cast<const float4 *>(&sm.eref[c0 + 4]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    if (!unsafe) {
-                        plus[e] = x[e] * __expf(gm[e] - sm.ref[c0 + e]);
-                        qt[e] = plus[e] * sm.eref[c0 + e];
-                    } else {
+                    for (int e = 0; e < 8; ++e) {
+                        const float E = __expf(gm[e] - rf[e]);  // e^{gamma - ref}
+                        plus[e] = x[e] * E;
+                        qt[e] = plus[e] * er[e];
+                        ei[e] = __expf(rf[e] - gm[e]);          // e^{ref - gamma}
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
                         plus[e] = 0.f;
+                        ei[e] = 0.f;
                         qt[e] = x[e] * expf(gm[e]);
                     }
                 }
@@ -371,7 +382,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                     if (!isq) {
                         float mi[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) mi[e] = x[e] * __expf(sm.ref[c0 + e] - gm[e]);
+                        for (int e = 0; e < 8; ++e) mi[e] = x[e] * ei[e];
                         *reinterpret_cast<float4 *>(km + tc::sw128_off(tok, c0, C)) =
                             make_float4(mi[0], mi[1], mi[2], mi[3]);
                         *reinterpret_cast<float4 *>(km + tc::sw128_off(tok, c0 + 4, C)) =
@@ -406,7 +417,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         // ---- 4. channel phase (thread = channel lr, tokens 32 hf .. + 31):
         // beta K~^T into TMEM, K^^T row lr of the image
         {
+            // K^ = k^ e^{gamma_C - gamma} = K- e^{gamma_C - ref} on the split
+            // path (K- is zero past the chunk's end); directly otherwise
             const float gCv = sm.gC[lr];
+            const float egcref = unsafe ? 0.f : expf(gCv - sm.ref[lr]);
             float bk[32];
             uint32_t kw[16];
 #pragma unroll
@@ -418,7 +432,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                     const float kx = st_bf16(kst, r, lr) * sm.invk[r];
                     const float g = st_f32(gam, r, lr);
                     bk[i + e] = sm.beta[r] * kx * __expf(g);
-                    kh2[e] = r < L ? kx * __expf(gCv - g) : 0.f;
+                    kh2[e] = !unsafe ? st_f32(km, r, lr) * egcref : (r < L ? kx * expf(gCv - g) : 0.f);
                 }
                 kw[i >> 1] = pack_h2(kh2[0], kh2[1]);
             }
@@ -614,7 +628,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             // ---- 8. lane lr: W[r][lr] (column lr of the W rows of [W; Q~])
             // and U'[r][lr] (row lr of U'^T, 16-byte units of four tokens at
             // (u & 8) | ((u & 7) ^ (lr & 7))), tokens 32 hf .. + 31
+            // W rows go to a shared copy of their part of the [W; Q~] tile
+            // (over the inverse's scratch), which two bulk copies then store
             unsigned char *up = img + IMG_UP + (size_t)lr * C * 4;
+            unsigned char *wt = reinterpret_cast<unsigned char *>(&sm.u1);
 #pragma unroll
             for (int r0 = 0; r0 < 32; r0 += 16) {
                 float w16[16];
@@ -623,7 +640,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
 #pragma unroll
                 for (int rr = 0; rr < 16; ++rr) {
                     big |= !(fabsf(w16[rr]) <= kHalfMax) && w16[rr] == w16[rr];
-                    st_h(img + IMG_BW, 128, 32 * hf + r0 + rr, lr, w16[rr]);
+                    st_h(wt, 64, 32 * hf + r0 + rr, lr, w16[rr]);
                 }
                 tc::ld16(tc::lane_addr(tm, warp, PT_UPT + 32 * hf + r0), w16);
                 tc::wait_ld();
@@ -634,6 +651,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                         make_float4(w16[rr], w16[rr + 1], w16[rr + 2], w16[rr + 3]);
                 }
             }
+        }
+    }
+    if (ok) {
+        // the W rows: rows 0..63 of each 64-channel column of [W; Q~]
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            const unsigned char *wt = reinterpret_cast<const unsigned char *>(&sm.u1);
+            bulk_s2g(img + IMG_BW, wt, C * 128);
+            bulk_s2g(img + IMG_BW + 128 * 128, wt + C * 128, C * 128);
+            bulk_commit();
+            bulk_wait_all();
         }
     }
     if (!ok && tid == 0) {
