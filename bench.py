@@ -452,13 +452,30 @@ def run_prefill(kda, peaks, T=8192, H=32, steps=10, key="prefill_t8192_h32_d128_
     bytes_ = T * H * PREFILL_BYTES_PER_TH + H * 128 * 128 * 4
     flops = T * H * PREFILL_FLOP_PER_TH
     t_roof = max(bytes_ / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+    snap = None
+    if T % 1024 == 0 and T <= 16384:
+        # the same prefill writing the state every 1024 tokens into pool slots
+        # (the prefix-cache snapshots): its extra cost
+        n_snap = T // 1024
+        pool2 = torch.zeros((n_snap + 1, H, 128, 128), device="cuda")
+        snaps = (torch.zeros(n_snap, dtype=torch.int32, device="cuda"),
+                 torch.arange(1, n_snap + 1, dtype=torch.int32, device="cuda") * 1024,
+                 torch.arange(1, n_snap + 1, dtype=torch.int32, device="cuda"))
+        slot0 = torch.zeros(1, dtype=torch.int32, device="cuda")
+        call_s = kda.prefill_chunked(x.q, x.k, x.v, x.g, x.b, x.cu_seqlens, slot0, pool2, out,
+                                     workspace=ws, snapshots=snaps, _prepare=True)
+        ts = time_launches(lambda i: call_s(), steps, warmup=2) / 1e6
+        snap = {"snapshots": n_snap, "every_tokens": 1024, "us": round(ts * 1e6, 1),
+                "extra_us": round((ts - t) * 1e6, 1),
+                "extra_bytes": n_snap * H * 128 * 128 * 4}
+        del pool2
     return {"workload": key, "us": round(t * 1e6, 1), "tokens_per_s": round(T / t, 1),
             "token_heads_per_s": round(T * H / t, 1), "GB/s": round(bytes_ / t / 1e9, 1),
             "frac_hbm": round(bytes_ / t / 1e9 / peaks["hbm_gbs"], 4),
             "TFLOP/s": round(flops / t / 1e12, 2),
             "frac_tc_dense_bf16": round(flops / t / 1e12 / peaks["bf16_tflops"], 4),
             "frac_roofline": round(t_roof / t, 4), "algorithmic_bytes": bytes_,
-            "algorithmic_flop": flops}
+            "algorithmic_flop": flops, "with_snapshots": snap}
 
 
 def run_longmix(kda, peaks):

@@ -144,11 +144,15 @@ size_t kda_prefill_workspace_bytes(const kda_dims *dims, int32_t num_seqs, int64
                                         total_tokens);
 }
 
-int kda_prefill_chunked(const kda_dims *dims, int32_t num_seqs, const int32_t *cu_seqlens,
+static int prefill_impl(const kda_dims *dims, int32_t num_seqs, const int32_t *cu_seqlens,
                         int64_t total_tokens, const void *q, const void *k, const void *v,
                         const float *g, const void *b, const int32_t *slot_ids, float *pool,
-                        int64_t num_slots, int32_t init_from_pool, void *out, void *workspace,
-                        size_t workspace_bytes, int32_t *err_flag, void *stream) {
+                        int64_t num_slots, int32_t init_from_pool, void *out, int32_t num_snaps,
+                        const int32_t *snap_seq, const int32_t *snap_tokens, const int32_t *snap_slot,
+                        void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream) {
+    if (num_snaps < 0) return KDA_ERR_INVALID_ARG;
+    if (num_snaps > 0 && (snap_seq == nullptr || snap_tokens == nullptr || snap_slot == nullptr))
+        return KDA_ERR_INVALID_ARG;
     int st = check_dims(dims);
     if (st != KDA_OK) return st;
     if (num_seqs < 0 || total_tokens < 0 || num_slots < 0) return KDA_ERR_INVALID_ARG;
@@ -171,7 +175,30 @@ int kda_prefill_chunked(const kda_dims *dims, int32_t num_seqs, const int32_t *c
     p.workspace = workspace; p.workspace_bytes = workspace_bytes; p.err_flag = err_flag;
     p.num_seqs = num_seqs; p.H = dims->num_heads; p.dk = dims->dk; p.dv = dims->dv;
     p.eps = dims->eps; p.scale = resolve_scale(dims);
+    p.num_snaps = num_snaps; p.snap_seq = snap_seq; p.snap_tokens = snap_tokens; p.snap_slot = snap_slot;
     return from_cuda(kda::launch_prefill(p, dims->dtype, (cudaStream_t)stream));
+}
+
+int kda_prefill_chunked(const kda_dims *dims, int32_t num_seqs, const int32_t *cu_seqlens,
+                        int64_t total_tokens, const void *q, const void *k, const void *v,
+                        const float *g, const void *b, const int32_t *slot_ids, float *pool,
+                        int64_t num_slots, int32_t init_from_pool, void *out, void *workspace,
+                        size_t workspace_bytes, int32_t *err_flag, void *stream) {
+    return prefill_impl(dims, num_seqs, cu_seqlens, total_tokens, q, k, v, g, b, slot_ids, pool, num_slots,
+                        init_from_pool, out, 0, nullptr, nullptr, nullptr, workspace, workspace_bytes, err_flag,
+                        stream);
+}
+
+int kda_prefill_chunked_snapshots(const kda_dims *dims, int32_t num_seqs, const int32_t *cu_seqlens,
+                                  int64_t total_tokens, const void *q, const void *k, const void *v,
+                                  const float *g, const void *b, const int32_t *slot_ids, float *pool,
+                                  int64_t num_slots, int32_t init_from_pool, void *out, int32_t num_snaps,
+                                  const int32_t *snap_seq, const int32_t *snap_tokens,
+                                  const int32_t *snap_slot, void *workspace, size_t workspace_bytes,
+                                  int32_t *err_flag, void *stream) {
+    return prefill_impl(dims, num_seqs, cu_seqlens, total_tokens, q, k, v, g, b, slot_ids, pool, num_slots,
+                        init_from_pool, out, num_snaps, snap_seq, snap_tokens, snap_slot, workspace,
+                        workspace_bytes, err_flag, stream);
 }
 
 }  // extern "C"

@@ -69,7 +69,48 @@ struct PrefillParams {
     int32_t *err_flag;
     int32_t num_seqs, H, dk, dv;
     float eps, scale;
+    // state snapshots at chunk boundaries (num_snaps = 0: none); requests
+    // sorted by sequence, then by token count
+    int32_t num_snaps;
+    const int32_t *snap_seq, *snap_tokens, *snap_slot;
 };
+
+// Snapshot requests of sequence s: [lo, hi) of the sorted request list.
+__device__ __forceinline__ void snap_range(const PrefillParams &p, int s, int &lo, int &hi) {
+    int a = 0, b = p.num_snaps;  // first request with sequence >= s
+    while (a < b) {
+        const int m = (a + b) >> 1;
+        if (p.snap_seq[m] < s) a = m + 1; else b = m;
+    }
+    lo = a;
+    b = p.num_snaps;  // first request with sequence > s
+    while (a < b) {
+        const int m = (a + b) >> 1;
+        if (p.snap_seq[m] <= s) a = m + 1; else b = m;
+    }
+    hi = a;
+}
+
+// The snapshot requests due once `done` tokens of the sequence are in the
+// state: calls store(slot) for each valid one and returns the next pending
+// request.  A request that can no longer be met (its token count is not a
+// positive multiple of the chunk length, it is out of order, or its slot is
+// out of range) is skipped and flagged in `bad`.
+template <typename F>
+__device__ __forceinline__ int snap_due(const PrefillParams &p, int ptr, int hi, int64_t done, int chunk_len,
+                                        bool &bad, F &&store) {
+    while (ptr < hi && (int64_t)p.snap_tokens[ptr] <= done) {
+        const int64_t t = p.snap_tokens[ptr];
+        const int slot = p.snap_slot[ptr];
+        if (t == done && t > 0 && t % chunk_len == 0 && (int64_t)slot < p.num_slots) {
+            if (slot >= 0) store(slot);
+        } else {
+            bad = true;
+        }
+        ++ptr;
+    }
+    return ptr;
+}
 
 // The driver's cuTensorMapEncodeTiled (looked up once through the runtime),
 // or nullptr when the driver does not provide it.

@@ -360,6 +360,14 @@ __global__ void __launch_bounds__(kChainThreads) chunk_chain_kernel(const Prefil
         sm.S[idx / DK][idx % DK] = p.init_from_pool ? Sg[idx] : 0.f;
     const float scale = p.scale;
     const int nchunks = plan[s + 1] - plan[s];
+    // snapshot requests of this sequence (the same for every thread)
+    int snap_ptr = 0, snap_hi = 0;
+    bool snap_bad = false;
+    if (p.num_snaps > 0) snap_range(p, s, snap_ptr, snap_hi);
+    auto store_snapshot = [&](int sl) {
+        float *dst = p.pool + ((int64_t)sl * H + h) * (int64_t)DV * DK + (int64_t)rb * kChainRows * DK;
+        for (int idx = tid; idx < kChainRows * DK; idx += kChainThreads) dst[idx] = sm.S[idx / DK][idx % DK];
+    };
     for (int ci = 0; ci < nchunks; ++ci) {
         const int32_t chunk = plan[s] + ci;
         const int64_t t0 = (int64_t)cs + (int64_t)ci * C;
@@ -409,7 +417,16 @@ __global__ void __launch_bounds__(kChainThreads) chunk_chain_kernel(const Prefil
             for (int j = 0; j < len; ++j) acc = fmaf(sm.U[j][i], sm.K[j][c], acc);
             sm.S[i][c] = acc;
         }
+        // the state after ci + 1 chunks, where a snapshot asks for it
+        if (snap_ptr < snap_hi) {
+            __syncthreads();
+            snap_ptr = snap_due(p, snap_ptr, snap_hi, min((int64_t)(ci + 1) * C, (int64_t)ce - cs), C, snap_bad,
+                                store_snapshot);
+        }
     }
+    // requests past the sequence's last whole chunk can never be met
+    if (snap_ptr < snap_hi) snap_bad = true;
+    if (snap_bad && rb == 0 && h == 0 && tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_SNAPSHOT);
     __syncthreads();
     for (int idx = tid; idx < kChainRows * DK; idx += kChainThreads) Sg[idx] = sm.S[idx / DK][idx % DK];
 }

@@ -922,6 +922,16 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
         };
         store_s16();
         warp_arrive(&sm.s16_ready);
+        // snapshot requests of this sequence (the same for every thread)
+        int snap_ptr = 0, snap_hi = 0;
+        bool snap_bad = false;
+        if (p.num_snaps > 0) snap_range(p, s, snap_ptr, snap_hi);
+        auto store_snapshot = [&](int sl) {
+            float *dst = p.pool + ((int64_t)sl * H + h) * (int64_t)D * D + (int64_t)lr * D + cq * 32;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4 *>(dst + e) = make_float4(S[e], S[e + 1], S[e + 2], S[e + 3]);
+        };
         for (int c = 0; c < nchunks && ok; ++c) {
             const int b = c & 1;
             const unsigned char *im = sm.img[b];
@@ -976,8 +986,15 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
                 store_s16();
             }
             warp_arrive(&sm.s16_ready);
+            // the state after c + 1 chunks, where a snapshot asks for it
+            if (snap_ptr < snap_hi)
+                snap_ptr = snap_due(p, snap_ptr, snap_hi, min((int64_t)(c + 1) * C, (int64_t)ce - cs), C, snap_bad,
+                                    store_snapshot);
         }
         if (ok && nchunks > 0) ok = output(nchunks - 1);
+        // requests past the sequence's last whole chunk can never be met
+        if (ok && snap_ptr < snap_hi) snap_bad = true;
+        if (snap_bad && h == 0 && tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_SNAPSHOT);
         if (tid == 0) bulk_wait_all();  // every tensor store complete before shared memory goes
         if (bad && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_RANGE);
         if (!ok && (tid & 31) == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);

@@ -28,12 +28,13 @@ KDA_DEVERR_ACCEPTED = 2
 KDA_DEVERR_SEQLENS = 4
 KDA_DEVERR_TIMEOUT = 8
 KDA_DEVERR_RANGE = 16
+KDA_DEVERR_SNAPSHOT = 32
 
 EXPORTED = ("kda_decode", "kda_verify_record", "kda_replay_commit",
             "kda_prefill_chunked", "kda_prefill_workspace_bytes",
             "kda_records_bytes", "kda_status_string", "kda_abi_version",
             "kda_prefill_chunked_static", "kda_static_scratch_bytes",
-            "kda_verify_workspace_bytes")
+            "kda_verify_workspace_bytes", "kda_prefill_chunked_snapshots")
 
 
 class KdaError(RuntimeError):
@@ -79,6 +80,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kda_prefill_chunked.argtypes = [_PD, _I32, _VP, _I64, _VP, _VP, _VP,
                                         _VP, _VP, _VP, _VP, _I64, _I32, _VP,
                                         _VP, _SZ, _VP, _VP]
+    lib.kda_prefill_chunked_snapshots.argtypes = [_PD, _I32, _VP, _I64, _VP, _VP, _VP, _VP, _VP, _VP,
+                                                  _VP, _I64, _I32, _VP, _I32, _VP, _VP, _VP, _VP, _SZ,
+                                                  _VP, _VP]
+    lib.kda_prefill_chunked_snapshots.restype = ctypes.c_int
     lib.kda_prefill_chunked_static.argtypes = [_PD, _I32, _VP, _I64, _VP, _VP, _VP, _VP,
                                                _VP, _VP, _VP, _I64, _I32, _VP, _VP, _VP]
     lib.kda_prefill_chunked_static.restype = ctypes.c_int
@@ -278,13 +283,16 @@ def prefill_workspace_bytes(H, dk, dv, dtype_code, num_seqs, total_tokens) -> in
 
 
 def prefill_chunked(q, k, v, g, b, cu_seqlens, slot_ids, pool, out=None, *,
-                    init_from_pool=False, workspace=None, eps=1e-6, scale=None,
-                    err_flag=None, stream=None, _prepare=False):
+                    init_from_pool=False, workspace=None, snapshots=None, eps=1e-6,
+                    scale=None, err_flag=None, stream=None, _prepare=False):
     """Chunked prefill of a packed variable-length batch.
 
     q, k: [T, H, dk]; v: [T, H, dv]; g: [T, H, dk] fp32; b: [T, H];
     cu_seqlens: [n+1] int32 (device); slot_ids: [n] int32.  The final state of
-    each sequence goes to its slot.  Returns out [T, H, dv].
+    each sequence goes to its slot.  ``snapshots``: optional (seq, tokens,
+    slot) int32 device tensors of equal length, sorted by sequence then token
+    count: the state after that many tokens of that sequence also goes to
+    that slot (kda_prefill_chunked_snapshots).  Returns out [T, H, dv].
     """
     T, H, dk = k.shape
     dv = v.shape[2]
@@ -305,11 +313,22 @@ def prefill_chunked(q, k, v, g, b, cu_seqlens, slot_ids, pool, out=None, *,
         workspace = _scratch(need, q.device, stream)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     dims = make_dims(H, dk, dv, code, eps, scale)
-    args = (ctypes.byref(dims), n, _ptr(cu_seqlens), T, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
-            _ptr(b), _ptr(slot_ids), _ptr(pool), pool.shape[0], 1 if init_from_pool else 0,
-            _ptr(out), _ptr(workspace), ws_bytes, _ptr(err_flag), _stream_handle(stream))
+    if snapshots is not None:
+        sseq, stok, sslot = snapshots
+        m = sseq.shape[0]
+        for name, t in (("snapshot seq", sseq), ("snapshot tokens", stok), ("snapshot slot", sslot)):
+            _need(t, name, (m,), torch.int32)
+        args = (ctypes.byref(dims), n, _ptr(cu_seqlens), T, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                _ptr(b), _ptr(slot_ids), _ptr(pool), pool.shape[0], 1 if init_from_pool else 0,
+                _ptr(out), m, _ptr(sseq), _ptr(stok), _ptr(sslot), _ptr(workspace), ws_bytes,
+                _ptr(err_flag), _stream_handle(stream))
+        fn, name = _lib.kda_prefill_chunked_snapshots, "kda_prefill_chunked_snapshots"
+    else:
+        args = (ctypes.byref(dims), n, _ptr(cu_seqlens), T, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                _ptr(b), _ptr(slot_ids), _ptr(pool), pool.shape[0], 1 if init_from_pool else 0,
+                _ptr(out), _ptr(workspace), ws_bytes, _ptr(err_flag), _stream_handle(stream))
+        fn, name = _lib.kda_prefill_chunked, "kda_prefill_chunked"
     if _prepare:
-        return _Prepared(_lib.kda_prefill_chunked, args, "kda_prefill_chunked",
-                         (dims, workspace), out)
-    _check(_lib.kda_prefill_chunked(*args), "kda_prefill_chunked")
+        return _Prepared(fn, args, name, (dims, workspace), out)
+    _check(fn(*args), name)
     return out

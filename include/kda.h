@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 2
+#define KDA_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define KDA_API __attribute__((visibility("default")))
@@ -85,9 +85,13 @@ enum {
     KDA_DEVERR_ACCEPTED = 2,  /* num_accepted outside 0..draft_len             */
     KDA_DEVERR_SEQLENS = 4,   /* cu_seqlens not non-decreasing / past total_T  */
     KDA_DEVERR_TIMEOUT = 8,   /* an internal bounded wait gave up (prefill)    */
-    KDA_DEVERR_RANGE = 16     /* a value passed to the tensor-core prefill's
+    KDA_DEVERR_RANGE = 16,    /* a value passed to the tensor-core prefill's
                                  fp16 products exceeded +-65504; the outputs and
                                  final state of that sequence are not valid  */
+    KDA_DEVERR_SNAPSHOT = 32  /* a prefill snapshot request was skipped: token
+                                 count not a positive multiple of 64 within its
+                                 sequence, requests out of order, or slot id
+                                 >= num_slots                                */
 };
 
 typedef struct kda_dims {
@@ -240,6 +244,43 @@ KDA_API int kda_prefill_chunked(const kda_dims *dims, int32_t num_seqs,
                         int64_t num_slots, int32_t init_from_pool, void *out,
                         void *workspace, size_t workspace_bytes,
                         int32_t *err_flag, void *stream);
+
+/*
+ * kda_prefill_chunked_snapshots: kda_prefill_chunked that also writes the
+ * state reached at chosen chunk boundaries into pool slots, so that a later
+ * prefill can resume from a cached prefix with init_from_pool = 1 (the KDA
+ * Prefix-Cache of "Ascend day-0 support for Kimi K3", Kimi K3 overview; the
+ * serving engine's prefix cache and chunked prefill in the vLLM Ascend
+ * paragraph of the same page).  Arguments and results are those of
+ * kda_prefill_chunked, plus num_snaps requests, sorted by sequence and then
+ * by token count:
+ *   snap_seq     i32 [num_snaps] device: the sequence (0 .. num_seqs-1)
+ *   snap_tokens  i32 [num_snaps] device: t, a positive multiple of 64 with
+ *                t <= that sequence's length; the snapshot is the state after
+ *                the sequence's first t tokens (starting from its initial
+ *                state, zero or the pool's per init_from_pool)
+ *   snap_slot    i32 [num_snaps] device: destination slot; the state of every
+ *                head goes to pool[snap_slot][h] (dv x dk fp32).  A negative
+ *                slot skips the request silently.
+ * A request that cannot be met (token count not a positive multiple of 64,
+ * beyond the sequence, out of order, or slot >= num_slots) is skipped and
+ * sets KDA_DEVERR_SNAPSHOT.  Requests of a padding or out-of-range sequence
+ * are ignored.  Destination slots must differ from each other and from the
+ * sequences' own slots (precondition).  num_snaps = 0 is kda_prefill_chunked;
+ * num_snaps < 0, or a NULL request array when num_snaps > 0, returns
+ * KDA_ERR_INVALID_ARG.  Each snapshot adds dv x dk x 4 bytes per head of
+ * writes; the workspace is the same as kda_prefill_chunked's.
+ */
+KDA_API int kda_prefill_chunked_snapshots(const kda_dims *dims, int32_t num_seqs,
+                                          const int32_t *cu_seqlens, int64_t total_tokens,
+                                          const void *q, const void *k, const void *v,
+                                          const float *g, const void *b,
+                                          const int32_t *slot_ids, float *pool,
+                                          int64_t num_slots, int32_t init_from_pool, void *out,
+                                          int32_t num_snaps, const int32_t *snap_seq,
+                                          const int32_t *snap_tokens, const int32_t *snap_slot,
+                                          void *workspace, size_t workspace_bytes,
+                                          int32_t *err_flag, void *stream);
 
 /*
  * kda_prefill_chunked_static: kda_prefill_chunked without a caller-provided
