@@ -423,6 +423,36 @@ def run_spec(kda, peaks):
     cbytes = H * sum(commit_bytes_per_sh(a) for a in a_list)
     vt = tv / 1e6
     ct = tc / 1e6
+    # the u-record variant: verify into u records, commit without dot
+    # products, and the previous window's commit fused with the next verify
+    recu = kda.alloc_records_u(B, D, H, dk, dv, "cuda")
+    rec2 = kda.alloc_records_u(B, D, H, dk, dv, "cuda")
+    kda.verify_record_u(x.q, x.k, x.v, x.g, x.b, x.slot_ids, x.pool, out, recu, workspace=vws)
+    ucalls = [kda.verify_record_u(x.q, x.k, x.v, x.g, x.b, ss, x.pool, out, rec2, workspace=vws, _prepare=True)
+              for ss in sets]
+    tvu = time_launches(lambda i: ucalls[i % len(sets)](), n) / 1e6
+    cucalls = [kda.replay_commit_u(recu, acc, ss, x.pool, _prepare=True) for ss in sets]
+    tcu = time_launches(lambda i: cucalls[i % len(sets)](), n) / 1e6
+    fcalls = [kda.commit_verify_u(recu, acc, x.q, x.k, x.v, x.g, x.b, ss, x.pool, out, rec2, workspace=vws,
+                                  _prepare=True) for ss in sets]
+    tf = time_launches(lambda i: fcalls[i % len(sets)](), n) / 1e6
+    ubytes_rec = 512 + 512 + 512  # k_hat, g, u per token-head
+    cubytes = H * sum(0 if a == 0 else 2 * 128 * 128 * 4 + a * ubytes_rec for a in a_list)
+    vubytes = B * H * (128 * 128 * 4 + D * (768 + 512 + 2 + 256 + ubytes_rec))
+    fbytes = H * sum((2 if a else 1) * 128 * 128 * 4 + a * ubytes_rec for a in a_list) + \
+        B * H * D * (768 + 512 + 2 + 256 + ubytes_rec)
+    urec = {
+        "verify_u": {"us": round(tvu * 1e6, 2), "GB/s": round(vubytes / tvu / 1e9, 1),
+                     "frac_hbm": round(vubytes / tvu / 1e9 / peaks["hbm_gbs"], 4)},
+        "commit_u": {"us": round(tcu * 1e6, 2), "GB/s": round(cubytes / tcu / 1e9, 1),
+                     "frac_hbm": round(cubytes / tcu / 1e9 / peaks["hbm_gbs"], 4),
+                     "algorithmic_bytes": cubytes,
+                     "bytes_per_seq_head_a": "131072 + 1536 a (a >= 1); value records 131072 + 1284 a"},
+        "commit_then_verify_fused": {"us": round(tf * 1e6, 2), "GB/s": round(fbytes / tf / 1e9, 1),
+                                     "frac_hbm": round(fbytes / tf / 1e9 / peaks["hbm_gbs"], 4),
+                                     "algorithmic_bytes": fbytes,
+                                     "separate_us": round((tcu + tvu) * 1e6, 2)},
+    }
     return {
         "workload": "verify_commit_b128_d7_h32_d128_bf16",
         "verify": {"us": round(vt * 1e6, 2), "GB/s": round(vbytes / vt / 1e9, 1),
@@ -433,6 +463,7 @@ def run_spec(kda, peaks):
                    "frac_hbm": round(cbytes / ct / 1e9 / peaks["hbm_gbs"], 4),
                    "algorithmic_bytes": cbytes, "mean_accepted": round(sum(a_list) / B, 3)},
         "verify_workspace_bytes": vws_bytes,
+        "u_records": urec,
         "launches": 3 * n,  # verify: window + state kernels; commit: replay kernel
     }
 

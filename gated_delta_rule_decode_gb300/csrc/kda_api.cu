@@ -119,6 +119,89 @@ int kda_verify_record(const kda_dims *dims, int32_t batch, int32_t draft_len, co
     return from_cuda(kda::launch_verify(p, dims->dk, dims->dtype, (cudaStream_t)stream));
 }
 
+size_t kda_records_u_bytes(const kda_dims *dims, int32_t batch, int32_t draft_len) {
+    if (check_dims(dims) != KDA_OK || batch < 0 || draft_len < 1) return 0;
+    const size_t tokens = (size_t)batch * (size_t)draft_len * (size_t)dims->num_heads;
+    return tokens * ((size_t)dims->dk * 4 * 2 + (size_t)dims->dv * 4);
+}
+
+// Verify into u records, optionally after committing the previous window's
+// accepted u records (prev != NULL).
+static int verify_u_impl(const kda_dims *dims, int32_t batch, int32_t prev_draft_len,
+                         const kda_records_u *prev, const int32_t *prev_accepted, int32_t draft_len,
+                         const void *q, const void *k, const void *v, const float *g, const void *b,
+                         const int32_t *slot_ids, const float *pool, int64_t num_slots, void *out,
+                         const kda_records_u *rec, void *workspace, size_t workspace_bytes,
+                         int32_t *err_flag, void *stream) {
+    int st = check_dims(dims);
+    if (st != KDA_OK) return st;
+    if (batch < 0 || num_slots < 0 || draft_len < 1 || draft_len > 16) return KDA_ERR_INVALID_ARG;
+    if (prev != nullptr && (prev_draft_len < 1 || prev_draft_len > 16 || prev_accepted == nullptr ||
+                            !all_aligned({prev->k_hat, prev->g, prev->u})))
+        return KDA_ERR_INVALID_ARG;
+    if (batch == 0) return KDA_OK;
+    if (rec == nullptr) return KDA_ERR_INVALID_ARG;
+    if (!all_aligned({q, k, v, g, out, rec->k_hat, rec->g, rec->u}) || b == nullptr || slot_ids == nullptr)
+        return KDA_ERR_INVALID_ARG;
+    if (num_slots > 0 && !all_aligned({pool})) return KDA_ERR_INVALID_ARG;
+    const size_t need = kda::verify_workspace_bytes(dims->num_heads, dims->dk, dims->dv, dims->dtype,
+                                                    batch, draft_len);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return KDA_ERR_WORKSPACE;
+    kda::VerifyParams p{};
+    p.q = q; p.k = k; p.v = v; p.g = g; p.b = b;
+    p.workspace = need > 0 ? workspace : nullptr;
+    p.slot_ids = slot_ids; p.pool = pool; p.num_slots = num_slots; p.out = out;
+    p.rec_k_hat = rec->k_hat; p.rec_g = rec->g; p.rec_u = rec->u;
+    p.err_flag = err_flag;
+    p.batch = batch; p.D = draft_len; p.H = dims->num_heads; p.dv = dims->dv;
+    p.eps = dims->eps; p.scale = resolve_scale(dims);
+    if (prev != nullptr) {
+        p.prev_k_hat = prev->k_hat; p.prev_g = prev->g; p.prev_u = prev->u;
+        p.prev_accepted = prev_accepted; p.prev_D = prev_draft_len;
+    }
+    return from_cuda(kda::launch_verify(p, dims->dk, dims->dtype, (cudaStream_t)stream));
+}
+
+int kda_verify_record_u(const kda_dims *dims, int32_t batch, int32_t draft_len, const void *q,
+                        const void *k, const void *v, const float *g, const void *b,
+                        const int32_t *slot_ids, const float *pool, int64_t num_slots, void *out,
+                        const kda_records_u *rec, void *workspace, size_t workspace_bytes,
+                        int32_t *err_flag, void *stream) {
+    return verify_u_impl(dims, batch, 0, nullptr, nullptr, draft_len, q, k, v, g, b, slot_ids, pool,
+                         num_slots, out, rec, workspace, workspace_bytes, err_flag, stream);
+}
+
+int kda_commit_verify_u(const kda_dims *dims, int32_t batch, int32_t prev_draft_len,
+                        const kda_records_u *prev, const int32_t *prev_accepted, int32_t draft_len,
+                        const void *q, const void *k, const void *v, const float *g, const void *b,
+                        const int32_t *slot_ids, float *pool, int64_t num_slots, void *out,
+                        const kda_records_u *rec, void *workspace, size_t workspace_bytes,
+                        int32_t *err_flag, void *stream) {
+    if (prev == nullptr) return KDA_ERR_INVALID_ARG;
+    return verify_u_impl(dims, batch, prev_draft_len, prev, prev_accepted, draft_len, q, k, v, g, b, slot_ids,
+                         pool, num_slots, out, rec, workspace, workspace_bytes, err_flag, stream);
+}
+
+int kda_replay_commit_u(const kda_dims *dims, int32_t batch, int32_t draft_len, const kda_records_u *rec,
+                        const int32_t *num_accepted, const int32_t *slot_ids, float *pool,
+                        int64_t num_slots, int32_t *err_flag, void *stream) {
+    int st = check_dims(dims);
+    if (st != KDA_OK) return st;
+    if (batch < 0 || num_slots < 0 || draft_len < 1 || draft_len > 16) return KDA_ERR_INVALID_ARG;
+    if (batch == 0) return KDA_OK;
+    if (rec == nullptr || num_accepted == nullptr || slot_ids == nullptr) return KDA_ERR_INVALID_ARG;
+    if (!all_aligned({rec->k_hat, rec->g, rec->u})) return KDA_ERR_INVALID_ARG;
+    if (num_slots > 0 && !all_aligned({pool})) return KDA_ERR_INVALID_ARG;
+    kda::ReplayParams p{};
+    p.rec_k_hat = rec->k_hat; p.rec_g = rec->g; p.rec_u = rec->u;
+    p.num_accepted = num_accepted; p.slot_ids = slot_ids;
+    p.pool = pool; p.num_slots = num_slots; p.err_flag = err_flag;
+    p.batch = batch; p.D = draft_len; p.H = dims->num_heads; p.dv = dims->dv;
+    return from_cuda(kda::launch_replay_u(p, dims->dk, (cudaStream_t)stream));
+}
+
 int kda_replay_commit(const kda_dims *dims, int32_t batch, int32_t draft_len,
                       const kda_records *rec, const int32_t *num_accepted,
                       const int32_t *slot_ids, float *pool, int64_t num_slots,

@@ -38,6 +38,15 @@ struct VerifyParams {
     int32_t *err_flag;
     int32_t batch, D, H, dv;
     float eps, scale;
+    // u-record variant: u_j = beta_j (v_j - S'_j k^_j) per value row, fp32
+    // [B][D][H][dv] (null: not written; rec_v and rec_beta may then be null)
+    float *rec_u;
+    // fused commit: before this window, the accepted prefix of the previous
+    // window's u records is applied to the committed state, which is written
+    // back (prev_accepted null: no commit)
+    const float *prev_k_hat, *prev_g, *prev_u;
+    const int32_t *prev_accepted;
+    int32_t prev_D;
 };
 
 struct ReplayParams {
@@ -45,6 +54,7 @@ struct ReplayParams {
     const void *rec_v;
     const float *rec_g;
     const float *rec_beta;
+    const float *rec_u;  // u-record commit (rec_v and rec_beta unused)
     const int32_t *num_accepted;
     const int32_t *slot_ids;
     float *pool;
@@ -126,6 +136,8 @@ size_t verify_workspace_bytes(int H, int dk, int dv, int dtype, int64_t batch, i
 bool verify_tc_supported(const VerifyParams &p, int dk, int dtype);
 cudaError_t launch_verify_tc(const VerifyParams &p, cudaStream_t st);
 cudaError_t launch_replay(const ReplayParams &p, int dk, int dtype, cudaStream_t s);
+// Commit from u records: S <- S diag(exp g_j) + u_j k^_j^T for the accepted prefix.
+cudaError_t launch_replay_u(const ReplayParams &p, int dk, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams &p, int dtype, cudaStream_t s);
 size_t prefill_workspace_bytes(int H, int dk, int dv, int dtype, int32_t num_seqs, int64_t total_tokens);
 

@@ -209,6 +209,20 @@ __device__ __forceinline__ float row_update(LaneVec<DK> &s, const TokenCoeffs<DK
     return c;
 }
 
+// One u record on one state row: s = s diag(exp g) + u k^ (element by
+// element, s * alpha first, then one fused multiply-add).  No dot product:
+// u already holds beta (v - s' . k^).
+template <int DK>
+__device__ __forceinline__ void commit_u_row(LaneVec<DK> &s, const float *k_hat, const float *g, float u, int l) {
+    LaneVec<DK> kh, al;
+    load_lane_vec<DK, float>(k_hat, l, kh);
+    load_lane_vec<DK, float>(g, l, al);
+    exp_lane<DK>(al);
+    const float2 u2 = make_float2(u, u);
+#pragma unroll
+    for (int i = 0; i < DK / 16; ++i) s.v[i] = __ffma2_rn(u2, kh.v[i], __fmul2_rn(s.v[i], al.v[i]));
+}
+
 // o_i = scale * (S_t q^)_i computed as scale * (s'.q^ + u (k^.q^)).
 __device__ __forceinline__ float row_output(float c, float u, float kq, float scale) {
     return __fmul_rn(scale, __fmaf_rn(u, kq, c));

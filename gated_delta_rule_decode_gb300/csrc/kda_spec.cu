@@ -122,6 +122,8 @@ __global__ void __launch_bounds__(256, (DMAX <= 8 ? 2 : 1)) verify_kernel(const 
                         &sm.kt[0][0], &sm.qt[0][0], &sm.A[0][0], &sm.P[0][0], DMAX, store_kq);
     }
     __syncthreads();
+    float *urec = p.rec_u ? p.rec_u + ((int64_t)n * D * p.H + h) * p.dv : nullptr;
+    const int64_t ustride = (int64_t)p.H * p.dv;
     if (valid) {
         // the outcome is made CTA-uniform so that no thread skips a barrier
         if (__syncthreads_and(mbar_wait(&sm.bar, 0)) == 0) {
@@ -129,8 +131,38 @@ __global__ void __launch_bounds__(256, (DMAX <= 8 ? 2 : 1)) verify_kernel(const 
             mbar_wait_drain(&sm.bar, 0);  // the copy still in flight
             return;
         }
+        // fused commit of the previous window's accepted u records: each
+        // group updates its rows in shared memory and writes them back to
+        // the pool before the window reads them
+        if (p.prev_accepted) {
+            const int a = __ldg(p.prev_accepted + n);
+            if (a < 0 || a > p.prev_D) {
+                if (threadIdx.x == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_ACCEPTED);
+            } else if (a > 0) {
+                // (the fused call writes the committed state: its pool is not read-only)
+                float *Sp = const_cast<float *>(p.pool) + ((int64_t)slot * p.H + h) * (int64_t)p.dv * DK;
+#pragma unroll 1
+                for (int rr = 0; rr < kVerifyRows; ++rr) {
+                    const int row = gid + rr * ngroups;
+                    LaneVec<DK> sr;
+                    load_lane_vec_smem<DK>(st + row * DK, l, sr);
+#pragma unroll 1
+                    for (int j = 0; j < a; ++j) {
+                        const int64_t tk = ((int64_t)n * p.prev_D + j) * p.H + h;
+                        commit_u_row<DK>(sr, p.prev_k_hat + tk * DK, p.prev_g + tk * DK, __ldg(p.prev_u + tk * p.dv + row), l);
+                    }
+                    store_lane_vec<DK>(st + row * DK, l, sr);
+                    store_row<DK>(Sp + (int64_t)row * DK, l, sr);
+                }
+                __syncthreads();
+            }
+        }
         window_rows<DK, DMAX>(st, ngroups, gid, l, D, p.scale, &sm.kt[0][0], &sm.qt[0][0], &sm.A[0][0], &sm.P[0][0],
-                              sm.beta, &sm.v[0][0], &sm.rt[0][0], &sm.ct[0][0], &sm.o[0][0]);
+                              sm.beta, &sm.v[0][0], &sm.rt[0][0], &sm.ct[0][0], &sm.o[0][0], urec, ustride);
+    } else if (urec) {
+        // a skipped entry's u records are zero
+        for (int idx = threadIdx.x; idx < D * p.dv; idx += blockDim.x)
+            urec[(idx / p.dv) * ustride + idx % p.dv] = 0.f;
     }
     __syncthreads();
     window_store<T>(p, n, h, threadIdx.x, blockDim.x, &sm.o[0][0], valid);
@@ -224,6 +256,74 @@ __global__ void __launch_bounds__(kSpecWarps * 32) replay_kernel(const ReplayPar
     for (int rr = 0; rr < R; ++rr) store_row<DK>(S + (int64_t)(row0 + rr * kRowStride) * DK, l, s[rr]);
 }
 
+// Commit from u records (the ReplaySSM variant that stores u = beta (v - S'k^)):
+// per accepted token j, S <- S diag(exp g_j) + u_j k^_j^T.  The same tiles as
+// replay_kernel; no dot products.  The element arithmetic (one multiply by
+// alpha, then one fused multiply-add) is the fused commit's, bit for bit.
+template <int DK, int R>
+__global__ void __launch_bounds__(kSpecWarps * 32) replay_u_kernel(const ReplayParams p) {
+    constexpr int ROWS = kRowStride * R;
+    __shared__ __align__(16) SpecSmem<DK, ROWS> sm;
+    const int nblk = p.dv / ROWS;
+    const int64_t item = blockIdx.x;
+    const int blk = (int)(item % nblk);
+    const int64_t sh = item / nblk;
+    const int h = (int)(sh % p.H);
+    const int n = (int)(sh / p.H);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int grp = lane >> 3, l = lane & 7;
+    const int gid = warp * kGroupsPerWarp + grp;
+    const int row0 = blk * ROWS + gid;
+
+    const int a = __ldg(p.num_accepted + n);
+    const int slot = __ldg(p.slot_ids + n);
+    const bool report = (blk == 0 && h == 0 && threadIdx.x == 0 && p.err_flag);
+    if (a < 0 || a > p.D) {
+        if (report) atomicOr(p.err_flag, KDA_DEVERR_ACCEPTED);
+        return;
+    }
+    if (slot < 0) return;
+    if ((int64_t)slot >= p.num_slots) {
+        if (report) atomicOr(p.err_flag, KDA_DEVERR_SLOT);
+        return;
+    }
+    if (a == 0) return;  // nothing accepted: no memory access at all
+
+    float *S = p.pool + ((int64_t)slot * p.H + h) * (int64_t)p.dv * DK;
+    LaneVec<DK> s[R];
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) load_row<DK>(S + (int64_t)(row0 + rr * kRowStride) * DK, l, s[rr]);
+    // group gid stages record gid's k^ and alpha; the tile's u values
+    if (gid < a) {
+        const int64_t tk = ((int64_t)n * p.D + gid) * p.H + h;
+        LaneVec<DK> kh, al;
+        load_lane_vec<DK, float>(p.rec_k_hat + tk * DK, l, kh);
+        load_lane_vec<DK, float>(p.rec_g + tk * DK, l, al);
+        exp_lane<DK>(al);
+        store_lane_vec<DK>(sm.kh[gid], l, kh);
+        store_lane_vec<DK>(sm.al[gid], l, al);
+    }
+    for (int idx = threadIdx.x; idx < a * ROWS; idx += kSpecWarps * 32) {
+        const int j = idx / ROWS, c = idx % ROWS;
+        sm.v[j][c] = __ldg(p.rec_u + (((int64_t)n * p.D + j) * p.H + h) * p.dv + blk * ROWS + c);
+    }
+    __syncthreads();
+    for (int j = 0; j < a; ++j) {
+        LaneVec<DK> kh, al;
+        load_lane_vec_smem<DK>(sm.kh[j], l, kh);
+        load_lane_vec_smem<DK>(sm.al[j], l, al);
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            const float u = sm.v[j][gid + rr * kRowStride];
+            const float2 u2 = make_float2(u, u);
+#pragma unroll
+            for (int i = 0; i < DK / 16; ++i) s[rr].v[i] = __ffma2_rn(u2, kh.v[i], __fmul2_rn(s[rr].v[i], al.v[i]));
+        }
+    }
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) store_row<DK>(S + (int64_t)(row0 + rr * kRowStride) * DK, l, s[rr]);
+}
+
 template <int DK, typename T, int DMAX>
 static cudaError_t launch_verify_d(const VerifyParams &p, cudaStream_t st) {
     const size_t smem = verify_state_offset<DK, DMAX>() + (size_t)p.dv * DK * 4;
@@ -273,6 +373,26 @@ cudaError_t launch_verify(const VerifyParams &p, int dk, int dtype, cudaStream_t
     if (dk == 128) return launch_verify_t<128, float>(p, st);
     if (dk == 64) return launch_verify_t<64, float>(p, st);
     return launch_verify_t<32, float>(p, st);
+}
+
+template <int DK>
+static cudaError_t launch_replay_u_t(const ReplayParams &p, cudaStream_t st) {
+    if (p.dv % (kRowStride * 4) == 0) {
+        const int64_t grid = (int64_t)p.batch * p.H * (p.dv / (kRowStride * 4));
+        if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        replay_u_kernel<DK, 4><<<(unsigned)grid, kSpecWarps * 32, 0, st>>>(p);
+    } else {
+        const int64_t grid = (int64_t)p.batch * p.H * (p.dv / (kRowStride * 2));
+        if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+        replay_u_kernel<DK, 2><<<(unsigned)grid, kSpecWarps * 32, 0, st>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_replay_u(const ReplayParams &p, int dk, cudaStream_t st) {
+    if (dk == 128) return launch_replay_u_t<128>(p, st);
+    if (dk == 64) return launch_replay_u_t<64>(p, st);
+    return launch_replay_u_t<32>(p, st);
 }
 
 cudaError_t launch_replay(const ReplayParams &p, int dk, int dtype, cudaStream_t st) {

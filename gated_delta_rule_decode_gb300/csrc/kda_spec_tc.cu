@@ -35,6 +35,7 @@
 // below 1e-30 in some channel takes the running products instead (the window
 // kernel forms a_jm and p_jm itself and flags the record).
 #include <cudaTypedefs.h>
+#include <type_traits>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -85,6 +86,14 @@ static_assert(offsetof(StateSmem, A) - offsetof(StateSmem, kq) == kOffA, "record
 static_assert(offsetof(StateSmem, flag) - offsetof(StateSmem, kq) == kOffFlag, "record layout");
 static_assert(offsetof(StateSmem, rbar) - offsetof(StateSmem, kq) >= kCopyBytes, "record layout");
 constexpr size_t kStateSmemBytes = sizeof(StateSmem) + 1024;  // + alignment of the swizzled tiles
+
+// The fused commit's staging: alpha = exp(g) and k^ of the previous window's
+// accepted records (appended, so the record layout above is unchanged).
+struct StateSmemFused : StateSmem {
+    float pa[kDraft][DK];
+    float pk[kDraft][DK];
+};
+constexpr size_t kStateSmemFusedBytes = sizeof(StateSmemFused) + 1024;
 
 __device__ __forceinline__ uint64_t evict_first_policy() {
     uint64_t pol;
@@ -168,7 +177,7 @@ __global__ void __launch_bounds__(kWinThreads) window_kernel(const VerifyParams 
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int idx = tid + kWinThreads * u;
-            if (idx < D * per_row) {
+            if (idx < D * per_row && p.rec_v) {
                 const int j = idx / per_row, c = (idx - j * per_row) * E;
                 __stcs(reinterpret_cast<uint4 *>(static_cast<T *>(p.rec_v) + (((int64_t)n * D + j) * p.H + h) * p.dv + c),
                        x[u]);
@@ -214,7 +223,7 @@ __global__ void __launch_bounds__(kWinThreads) window_kernel(const VerifyParams 
             if (l == 0) {
                 const float bt = sigmoid_f(Elem<T>::to_f(br));
                 Bw[j] = bt;
-                __stcs(p.rec_beta + tk, bt);
+                if (p.rec_beta) __stcs(p.rec_beta + tk, bt);
             }
         }
         widen(qr, x);
@@ -275,12 +284,13 @@ __global__ void __launch_bounds__(kWinThreads) window_kernel(const VerifyParams 
     if (tid == 0) *reinterpret_cast<int *>(rec + kOffFlag) = slow ? 1 : 0;
 }
 
-template <typename T>
+template <typename T, bool FUSED>
 __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyParams p,
                                                                const __grid_constant__ CUtensorMap smap,
                                                                const unsigned char *ws) {
     extern __shared__ unsigned char smem_raw[];
-    StateSmem &sm = *reinterpret_cast<StateSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    using Smem = typename std::conditional<FUSED, StateSmemFused, StateSmem>::type;
+    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int sh = blockIdx.x;
     const int h = sh % p.H, n = sh / p.H;
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -338,6 +348,22 @@ __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyPar
             set_ones<DK>(kb[r]);
         }
     }
+    // fused commit: the previous window's accepted prefix (thread tid stages
+    // channel tid of each record's alpha and k^)
+    int ca = 0;
+    if constexpr (FUSED) {
+        ca = __ldg(p.prev_accepted + n);
+        if (ca < 0 || ca > p.prev_D) {
+            if (tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_ACCEPTED);
+            ca = 0;
+        }
+        if (!valid) ca = 0;
+        for (int j = 0; j < ca; ++j) {
+            const int64_t tk = ((int64_t)n * p.prev_D + j) * p.H + h;
+            sm.pa[j][tid] = expf(__ldg(p.prev_g + tk * DK + tid));
+            sm.pk[j][tid] = __ldg(p.prev_k_hat + tk * DK + tid);
+        }
+    }
     // this thread's state row: its value entries
     float vr[kDraft];
     {
@@ -352,9 +378,9 @@ __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyPar
 
     bool ok = true;
     bool issued = false;
-    float o[kDraft];
+    float o[kDraft], uu[kDraft];
 #pragma unroll
-    for (int j = 0; j < kDraft; ++j) o[j] = 0.f;
+    for (int j = 0; j < kDraft; ++j) o[j] = uu[j] = 0.f;
     if (valid) {
         ok = __syncthreads_and(mbar_wait(&sm.rbar, 0)) != 0;
         if (ok && sm.flag[0] == 0) {
@@ -380,6 +406,38 @@ __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyPar
             }
         }
         if (ok) ok = __syncthreads_and(mbar_wait(&sm.sbar, 0)) != 0;
+        if constexpr (FUSED) {
+            // thread tid = state row tid: S <- S diag(alpha_j) + u_j k^_j for
+            // the accepted records, in the swizzled tile, then back to the pool
+            if (ok && ca > 0) {
+                float uj[kDraft];
+#pragma unroll
+                for (int j = 0; j < kDraft; ++j)
+                    uj[j] = j < ca ? __ldg(p.prev_u + (((int64_t)n * p.prev_D + j) * p.H + h) * p.dv + tid) : 0.f;
+                // (the fused call writes the committed state: its pool is not read-only)
+                float *Sp = const_cast<float *>(p.pool) + (((int64_t)slot * p.H + h) * 128 + tid) * DK;
+#pragma unroll 4
+                for (int q = 0; q < DK / 4; ++q) {
+                    float4 *cell = reinterpret_cast<float4 *>(&sm.st[q >> 3][0] + tid * 128 + (((q & 7) ^ (tid & 7)) << 4));
+                    float4 x = *cell;
+#pragma unroll
+                    for (int j = 0; j < kDraft; ++j) {
+                        if (j < ca) {
+                            const float4 a4 = *reinterpret_cast<const float4 *>(&sm.pa[j][4 * q]);
+                            const float4 k4 = *reinterpret_cast<const float4 *>(&sm.pk[j][4 * q]);
+                            x.x = __fmaf_rn(uj[j], k4.x, __fmul_rn(x.x, a4.x));
+                            x.y = __fmaf_rn(uj[j], k4.y, __fmul_rn(x.y, a4.y));
+                            x.z = __fmaf_rn(uj[j], k4.z, __fmul_rn(x.z, a4.z));
+                            x.w = __fmaf_rn(uj[j], k4.w, __fmul_rn(x.w, a4.w));
+                        }
+                    }
+                    *cell = x;
+                    *reinterpret_cast<float4 *>(Sp + 4 * q) = x;
+                }
+                fence_proxy_async_smem();  // the product reads the committed tile
+            }
+            __syncthreads();
+        }
         // every read of the scratch record is complete: drop its lines from L2
         // without writing them back
         if (ok && warp == 1)
@@ -415,6 +473,7 @@ __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyPar
 #pragma unroll
                     for (int m = 0; m <= j; ++m) c = __fmaf_rn(sm.P[j][m], u[m], c);
                     o[j] = __fmul_rn(p.scale, c);
+                    uu[j] = u[j];
                 }
             }
         } else {
@@ -430,6 +489,13 @@ __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyPar
 #pragma unroll
         for (int j = 0; j < kDraft; ++j)
             if (j < D) Elem<T>::store1(ob + (int64_t)j * p.H * p.dv, (valid && ok) ? o[j] : 0.f);
+        // u records (zero for a skipped entry)
+        if (p.rec_u) {
+            float *ub = p.rec_u + ((int64_t)n * D * p.H + h) * p.dv + tid;
+#pragma unroll
+            for (int j = 0; j < kDraft; ++j)
+                if (j < D) __stcs(ub + (int64_t)j * p.H * p.dv, (valid && ok) ? uu[j] : 0.f);
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -462,6 +528,7 @@ size_t verify_workspace_bytes(int H, int dk, int dv, int dtype, int64_t batch, i
 
 bool verify_tc_supported(const VerifyParams &p, int dk, int dtype) {
     return verify_workspace_bytes(p.H, dk, p.dv, dtype, p.batch, p.D) > 0 && p.workspace != nullptr &&
+           (p.prev_accepted == nullptr || p.prev_D <= verify_tc::kDraft) &&
            p.num_slots > 0 && p.num_slots * (int64_t)p.H <= 0x7fffffffLL &&
            (int64_t)p.batch * p.H <= 0x7fffffffLL && tensor_map_encode_fn() != nullptr;
 }
@@ -479,8 +546,10 @@ cudaError_t launch_verify_tc(const VerifyParams &p, cudaStream_t st) {
                                    strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(state_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kStateSmemBytes);
+    const bool fused = p.prev_accepted != nullptr;
+    const size_t smem_bytes = fused ? kStateSmemFusedBytes : kStateSmemBytes;
+    auto kern = fused ? state_kernel<__nv_bfloat16, true> : state_kernel<__nv_bfloat16, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
     if (e != cudaSuccess) return e;
     window_kernel<__nv_bfloat16><<<(unsigned)items, kWinThreads, 0, st>>>(p, ws);
     e = cudaGetLastError();
@@ -490,7 +559,7 @@ cudaError_t launch_verify_tc(const VerifyParams &p, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)items);
     cfg.blockDim = dim3(kStateThreads);
-    cfg.dynamicSmemBytes = kStateSmemBytes;
+    cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -499,7 +568,7 @@ cudaError_t launch_verify_tc(const VerifyParams &p, cudaStream_t st) {
     cfg.numAttrs = 1;
     const VerifyParams pp = p;
     const unsigned char *wsc = ws;
-    return cudaLaunchKernelEx(&cfg, state_kernel<__nv_bfloat16>, pp, map, wsc);
+    return cudaLaunchKernelEx(&cfg, kern, pp, map, wsc);
 }
 
 }  // namespace kda

@@ -69,7 +69,7 @@ __device__ __forceinline__ void window_coeffs(const VerifyParams &p, int n, int 
         if (l == 0) {
             const float bt = sigmoid_f(Elem<T>::load1(static_cast<const T *>(p.b) + tk));
             beta[j] = bt;
-            p.rec_beta[tk] = bt;
+            if (p.rec_beta) p.rec_beta[tk] = bt;
         }
     } else if (kind == 1) {
         store_lane_vec<DK>(qh + j * DK, l, xn);
@@ -120,7 +120,8 @@ __device__ __forceinline__ void window_values_store(const VerifyParams &p, int n
     for (int u = 0; u < 2; ++u) {
         const int idx = tid + u * nthreads;
         if (idx < total) {
-            *reinterpret_cast<uint4 *>(static_cast<T *>(p.rec_v) + value_vec_offset<T>(p, n, h, idx)) = vv.x[u];
+            if (p.rec_v)
+                *reinterpret_cast<uint4 *>(static_cast<T *>(p.rec_v) + value_vec_offset<T>(p, n, h, idx)) = vv.x[u];
             const int j = idx >> sh, col = (idx & ((p.dv / E) - 1)) * E;
             const T *e = reinterpret_cast<const T *>(&vv.x[u]);
 #pragma unroll
@@ -196,7 +197,8 @@ __device__ __forceinline__ void window_pair(int t, bool act, int D, int l, const
 template <int DK, int DMAX>
 __device__ __forceinline__ void window_rows(const float *st, int ngroups, int gid, int l, int D, float scale,
                                             const float *kt, const float *qt, const float *A, const float *P,
-                                            const float *beta, const float *v, float *rt, float *ct, float *o) {
+                                            const float *beta, const float *v, float *rt, float *ct, float *o,
+                                            float *urec = nullptr, int64_t ustride = 0) {
     LaneVec<DK> s[kVerifyRows];
 #pragma unroll
     for (int rr = 0; rr < kVerifyRows; ++rr) load_lane_vec_smem<DK>(st + (gid + rr * ngroups) * DK, l, s[rr]);
@@ -249,6 +251,7 @@ __device__ __forceinline__ void window_rows(const float *st, int ngroups, int gi
 #pragma unroll
             for (int m = 0; m <= j; ++m) c = __fmaf_rn(P[j * DMAX + m], u[m], c);
             if (l < 4) o[j * kMaxDv + row] = __fmul_rn(scale, c);
+            if (urec && l < 4) urec[j * ustride + row] = u[j];  // u record of (token j, row)
         }
     }
 }

@@ -34,7 +34,9 @@ EXPORTED = ("kda_decode", "kda_verify_record", "kda_replay_commit",
             "kda_prefill_chunked", "kda_prefill_workspace_bytes",
             "kda_records_bytes", "kda_status_string", "kda_abi_version",
             "kda_prefill_chunked_static", "kda_static_scratch_bytes",
-            "kda_verify_workspace_bytes", "kda_prefill_chunked_snapshots")
+            "kda_verify_workspace_bytes", "kda_prefill_chunked_snapshots",
+            "kda_records_u_bytes", "kda_verify_record_u", "kda_replay_commit_u",
+            "kda_commit_verify_u")
 
 
 class KdaError(RuntimeError):
@@ -54,12 +56,17 @@ class KdaRecords(ctypes.Structure):
                 ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p)]
 
 
+class KdaRecordsU(ctypes.Structure):
+    _fields_ = [("k_hat", ctypes.c_void_p), ("g", ctypes.c_void_p), ("u", ctypes.c_void_p)]
+
+
 _VP = ctypes.c_void_p
 _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
 _SZ = ctypes.c_size_t
 _PD = ctypes.POINTER(KdaDims)
 _PR = ctypes.POINTER(KdaRecords)
+_PRU = ctypes.POINTER(KdaRecordsU)
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -80,6 +87,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kda_prefill_chunked.argtypes = [_PD, _I32, _VP, _I64, _VP, _VP, _VP,
                                         _VP, _VP, _VP, _VP, _I64, _I32, _VP,
                                         _VP, _SZ, _VP, _VP]
+    lib.kda_records_u_bytes.argtypes = [_PD, _I32, _I32]
+    lib.kda_records_u_bytes.restype = _SZ
+    lib.kda_verify_record_u.argtypes = [_PD, _I32, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64,
+                                        _VP, _PRU, _VP, _SZ, _VP, _VP]
+    lib.kda_verify_record_u.restype = ctypes.c_int
+    lib.kda_replay_commit_u.argtypes = [_PD, _I32, _I32, _PRU, _VP, _VP, _VP, _I64, _VP, _VP]
+    lib.kda_replay_commit_u.restype = ctypes.c_int
+    lib.kda_commit_verify_u.argtypes = [_PD, _I32, _I32, _PRU, _VP, _I32, _VP, _VP, _VP, _VP, _VP,
+                                        _VP, _VP, _I64, _VP, _PRU, _VP, _SZ, _VP, _VP]
+    lib.kda_commit_verify_u.restype = ctypes.c_int
     lib.kda_prefill_chunked_snapshots.argtypes = [_PD, _I32, _VP, _I64, _VP, _VP, _VP, _VP, _VP, _VP,
                                                   _VP, _I64, _I32, _VP, _I32, _VP, _VP, _VP, _VP, _SZ,
                                                   _VP, _VP]
@@ -274,6 +291,95 @@ def replay_commit(records, num_accepted, slot_ids, pool, *, err_flag=None,
     if _prepare:
         return _Prepared(_lib.kda_replay_commit, args, "kda_replay_commit", (dims, rs), None)
     _check(_lib.kda_replay_commit(*args), "kda_replay_commit")
+
+
+def alloc_records_u(B, D, H, dk, dv, device):
+    """Allocate a u-record set (dict of fp32 tensors) for (B, D)."""
+    return dict(k_hat=torch.empty((B, D, H, dk), dtype=torch.float32, device=device),
+                g=torch.empty((B, D, H, dk), dtype=torch.float32, device=device),
+                u=torch.empty((B, D, H, dv), dtype=torch.float32, device=device))
+
+
+def _records_u_struct(rec) -> KdaRecordsU:
+    return KdaRecordsU(rec["k_hat"].data_ptr(), rec["g"].data_ptr(), rec["u"].data_ptr())
+
+
+def _verify_u_args(q, k, v, g, b, slot_ids, pool, out, records, workspace, eps, scale, stream):
+    B, D, H, dk = k.shape
+    dv = v.shape[3]
+    dt = q.dtype
+    for name, t, shp, d in (("q", q, (B, D, H, dk), dt), ("k", k, (B, D, H, dk), dt),
+                            ("v", v, (B, D, H, dv), dt),
+                            ("g", g, (B, D, H, dk), torch.float32),
+                            ("b", b, (B, D, H), dt), ("slot_ids", slot_ids, (B,), torch.int32)):
+        _need(t, name, shp, d)
+    _need(pool, "pool", (pool.shape[0], H, dv, dk), torch.float32)
+    if out is None:
+        out = torch.empty((B, D, H, dv), dtype=dt, device=q.device)
+    _need(out, "out", (B, D, H, dv), dt)
+    if records is None:
+        records = alloc_records_u(B, D, H, dk, dv, q.device)
+    dims = make_dims(H, dk, dv, _dtype_code(q), eps, scale)
+    need = int(_lib.kda_verify_workspace_bytes(ctypes.byref(dims), B, D))
+    if workspace is None and need > 0:
+        workspace = _scratch(need, q.device, stream)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return B, D, dims, out, records, workspace, ws_bytes
+
+
+def verify_record_u(q, k, v, g, b, slot_ids, pool, out=None, records=None, *, workspace=None,
+                    eps=1e-6, scale=None, err_flag=None, stream=None, _prepare=False):
+    """ReplaySSM verify writing u records; pool is read only.  Returns (out, records)."""
+    B, D, dims, out, records, workspace, ws_bytes = _verify_u_args(
+        q, k, v, g, b, slot_ids, pool, out, records, workspace, eps, scale, stream)
+    rs = _records_u_struct(records)
+    args = (ctypes.byref(dims), B, D, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(slot_ids),
+            _ptr(pool), pool.shape[0], _ptr(out), ctypes.byref(rs), _ptr(workspace), ws_bytes,
+            _ptr(err_flag), _stream_handle(stream))
+    if _prepare:
+        return _Prepared(_lib.kda_verify_record_u, args, "kda_verify_record_u", (dims, rs, workspace),
+                         (out, records))
+    _check(_lib.kda_verify_record_u(*args), "kda_verify_record_u")
+    return out, records
+
+
+def replay_commit_u(records, num_accepted, slot_ids, pool, *, err_flag=None, stream=None,
+                    _prepare=False):
+    """Commit the accepted prefix of each sequence's u records onto ``pool``."""
+    B, D, H, dk = records["k_hat"].shape
+    dv = records["u"].shape[3]
+    _need(num_accepted, "num_accepted", (B,), torch.int32)
+    _need(slot_ids, "slot_ids", (B,), torch.int32)
+    _need(pool, "pool", (pool.shape[0], H, dv, dk), torch.float32)
+    rs = _records_u_struct(records)
+    dims = make_dims(H, dk, dv, KDA_DT_F32)
+    args = (ctypes.byref(dims), B, D, ctypes.byref(rs), _ptr(num_accepted), _ptr(slot_ids),
+            _ptr(pool), pool.shape[0], _ptr(err_flag), _stream_handle(stream))
+    if _prepare:
+        return _Prepared(_lib.kda_replay_commit_u, args, "kda_replay_commit_u", (dims, rs), None)
+    _check(_lib.kda_replay_commit_u(*args), "kda_replay_commit_u")
+
+
+def commit_verify_u(prev_records, prev_accepted, q, k, v, g, b, slot_ids, pool, out=None,
+                    records=None, *, workspace=None, eps=1e-6, scale=None, err_flag=None,
+                    stream=None, _prepare=False):
+    """Commit the previous window's accepted u records, then verify this
+    window, in one launch (the pool receives the committed state).
+    Returns (out, records)."""
+    B, D, dims, out, records, workspace, ws_bytes = _verify_u_args(
+        q, k, v, g, b, slot_ids, pool, out, records, workspace, eps, scale, stream)
+    Dp = prev_records["k_hat"].shape[1]
+    _need(prev_accepted, "prev_accepted", (B,), torch.int32)
+    prs = _records_u_struct(prev_records)
+    rs = _records_u_struct(records)
+    args = (ctypes.byref(dims), B, Dp, ctypes.byref(prs), _ptr(prev_accepted), D, _ptr(q), _ptr(k),
+            _ptr(v), _ptr(g), _ptr(b), _ptr(slot_ids), _ptr(pool), pool.shape[0], _ptr(out),
+            ctypes.byref(rs), _ptr(workspace), ws_bytes, _ptr(err_flag), _stream_handle(stream))
+    if _prepare:
+        return _Prepared(_lib.kda_commit_verify_u, args, "kda_commit_verify_u",
+                         (dims, prs, rs, workspace), (out, records))
+    _check(_lib.kda_commit_verify_u(*args), "kda_commit_verify_u")
+    return out, records
 
 
 def prefill_workspace_bytes(H, dk, dv, dtype_code, num_seqs, total_tokens) -> int:

@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 3
+#define KDA_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define KDA_API __attribute__((visibility("default")))
@@ -205,6 +205,78 @@ KDA_API int kda_replay_commit(const kda_dims *dims, int32_t batch, int32_t draft
                       const kda_records *rec, const int32_t *num_accepted,
                       const int32_t *slot_ids, float *pool, int64_t num_slots,
                       int32_t *err_flag, void *stream);
+
+/*
+ * ReplaySSM variant records ("2.8x faster Kimi K3 inference on CANN", section
+ * 04 "ReplaySSM": during verification only per-token update records are
+ * kept).  Here the record of (sequence n, draft token j, head h) holds the
+ * update itself instead of the value:
+ *   k_hat  float32 [B][D][H][dk]  normalised key
+ *   g      float32 [B][D][H][dk]  raw log-decay (bit copy of the input)
+ *   u      float32 [B][D][H][dv]  u_j = beta_j (v_j - S'_j k^_j), the delta
+ *                                 rule's correction along k^_j, where S'_j is
+ *                                 the decayed state before token j
+ * so that committing token j is S <- S diag(exp g_j) + u_j k^_j^T: no dot
+ * product, one multiply and one fused multiply-add per state element.  u
+ * comes from verify's window form, so a u-record commit equals a decode
+ * sequence up to rounding (not bit for bit; the value-record commit of
+ * kda_replay_commit keeps that contract).  A u-record commit and the fused
+ * commit of kda_commit_verify_u give the same bits.  1536 bytes per
+ * token-head at dk = dv = 128 (against 1284 for kda_records).
+ */
+typedef struct kda_records_u {
+    float *k_hat;
+    float *g;
+    float *u;
+} kda_records_u;
+
+/* Total bytes of the three u-record arrays for (batch, draft_len). */
+KDA_API size_t kda_records_u_bytes(const kda_dims *dims, int32_t batch, int32_t draft_len);
+
+/*
+ * kda_verify_record_u: kda_verify_record writing u records.  Arguments,
+ * workspace and outputs as kda_verify_record (the outputs are the same
+ * bits); rec->u of a padding or out-of-range entry is zero.
+ */
+KDA_API int kda_verify_record_u(const kda_dims *dims, int32_t batch, int32_t draft_len,
+                                const void *q, const void *k, const void *v,
+                                const float *g, const void *b, const int32_t *slot_ids,
+                                const float *pool, int64_t num_slots, void *out,
+                                const kda_records_u *rec, void *workspace,
+                                size_t workspace_bytes, int32_t *err_flag, void *stream);
+
+/*
+ * kda_replay_commit_u: commit from u records.  For each sequence n with
+ * a = num_accepted[n] (0..draft_len), applies records 0..a-1 in order:
+ * S = S diag(exp g_j) + u_j k_hat_j^T, and writes the state back.  a == 0
+ * leaves it untouched; a outside 0..draft_len sets KDA_DEVERR_ACCEPTED.
+ * The pool must hold the state verify read (precondition).
+ */
+KDA_API int kda_replay_commit_u(const kda_dims *dims, int32_t batch, int32_t draft_len,
+                                const kda_records_u *rec, const int32_t *num_accepted,
+                                const int32_t *slot_ids, float *pool, int64_t num_slots,
+                                int32_t *err_flag, void *stream);
+
+/*
+ * kda_commit_verify_u: the previous window's commit fused with this window's
+ * verify, for when the previous window's acceptance is already on the
+ * device.  Per (sequence, head) one launch reads the state once, applies
+ * the accepted prefix (prev_accepted[n] records, 0..prev_draft_len) of the
+ * previous window's u records `prev` exactly as kda_replay_commit_u does
+ * (same bits), writes the committed state back to the pool, and verifies
+ * the new draft window from it into `rec` (as kda_verify_record_u).  One
+ * state read and one write, against a read and a write for the commit plus
+ * a read for the verify.  prev and rec must not overlap.  prev_accepted
+ * outside 0..prev_draft_len sets KDA_DEVERR_ACCEPTED and that sequence is
+ * verified without a commit.
+ */
+KDA_API int kda_commit_verify_u(const kda_dims *dims, int32_t batch, int32_t prev_draft_len,
+                                const kda_records_u *prev, const int32_t *prev_accepted,
+                                int32_t draft_len, const void *q, const void *k, const void *v,
+                                const float *g, const void *b, const int32_t *slot_ids,
+                                float *pool, int64_t num_slots, void *out,
+                                const kda_records_u *rec, void *workspace,
+                                size_t workspace_bytes, int32_t *err_flag, void *stream);
 
 /*
  * kda_prefill_chunked: chunked prefill of a variable-length batch.
