@@ -55,10 +55,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t phase) {
     return ok != 0;
 }
 
-// Bounded wait on phase `phase`; false if the limit ran out.
+// Non-suspending probe of phase `phase`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t phase) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(phase)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on phase `phase`; false if the limit ran out.  A test build
+// (KDA_WAIT_NONBLOCKING, with a small KDA_WAIT_LIMIT) polls without the
+// hardware's suspend, so that the limit runs out on copies and products
+// that are merely in flight and the timeout path can be exercised.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t phase) {
-    for (uint32_t it = 0; it < kWaitLimit; ++it)
+    for (uint32_t it = 0; it < kWaitLimit; ++it) {
+#ifdef KDA_WAIT_NONBLOCKING
+        if (mbar_test_wait(bar, phase)) return true;
+#else
         if (mbar_try_wait(bar, phase)) return true;
+#endif
+    }
     return false;
 }
 
