@@ -110,6 +110,13 @@ __device__ __forceinline__ void tma_load_3d_ef(void *dst, const CUtensorMap *map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z, const void *src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(smem_addr(src))
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_g2s_ef(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
@@ -351,6 +358,7 @@ __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyPar
     // fused commit: the previous window's accepted prefix (thread tid stages
     // channel tid of each record's alpha and k^)
     int ca = 0;
+    float pg[kDraft], pkv[kDraft], uj[kDraft];
     if constexpr (FUSED) {
         ca = __ldg(p.prev_accepted + n);
         if (ca < 0 || ca > p.prev_D) {
@@ -358,10 +366,13 @@ __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyPar
             ca = 0;
         }
         if (!valid) ca = 0;
-        for (int j = 0; j < ca; ++j) {
+        // loads first; shared stores once the value loads below are out
+#pragma unroll
+        for (int j = 0; j < kDraft; ++j) {
             const int64_t tk = ((int64_t)n * p.prev_D + j) * p.H + h;
-            sm.pa[j][tid] = expf(__ldg(p.prev_g + tk * DK + tid));
-            sm.pk[j][tid] = __ldg(p.prev_k_hat + tk * DK + tid);
+            pg[j] = j < ca ? __ldg(p.prev_g + tk * DK + tid) : 0.f;
+            pkv[j] = j < ca ? __ldg(p.prev_k_hat + tk * DK + tid) : 0.f;
+            uj[j] = j < ca ? __ldg(p.prev_u + tk * p.dv + tid) : 0.f;
         }
     }
     // this thread's state row: its value entries
@@ -370,6 +381,12 @@ __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyPar
         const T *vb = static_cast<const T *>(p.v) + ((int64_t)n * D * p.H + h) * p.dv + tid;
 #pragma unroll
         for (int j = 0; j < kDraft; ++j) vr[j] = j < D ? Elem<T>::load1(vb + (int64_t)j * p.H * p.dv) : 0.f;
+    }
+    if constexpr (FUSED) {
+        for (int j = 0; j < ca; ++j) {
+            sm.pa[j][tid] = expf(pg[j]);
+            sm.pk[j][tid] = pkv[j];
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -410,12 +427,6 @@ __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyPar
             // thread tid = state row tid: S <- S diag(alpha_j) + u_j k^_j for
             // the accepted records, in the swizzled tile, then back to the pool
             if (ok && ca > 0) {
-                float uj[kDraft];
-#pragma unroll
-                for (int j = 0; j < kDraft; ++j)
-                    uj[j] = j < ca ? __ldg(p.prev_u + (((int64_t)n * p.prev_D + j) * p.H + h) * p.dv + tid) : 0.f;
-                // (the fused call writes the committed state: its pool is not read-only)
-                float *Sp = const_cast<float *>(p.pool) + (((int64_t)slot * p.H + h) * 128 + tid) * DK;
 #pragma unroll 4
                 for (int q = 0; q < DK / 4; ++q) {
                     float4 *cell = reinterpret_cast<float4 *>(&sm.st[q >> 3][0] + tid * 128 + (((q & 7) ^ (tid & 7)) << 4));
@@ -432,11 +443,17 @@ __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyPar
                         }
                     }
                     *cell = x;
-                    *reinterpret_cast<float4 *>(Sp + 4 * q) = x;
                 }
-                fence_proxy_async_smem();  // the product reads the committed tile
+                fence_proxy_async_smem();  // the product and the tensor stores read the committed tile
             }
             __syncthreads();
+            // the committed state back to the pool: four tensor stores through
+            // the load's map (the fused call's pool is written)
+            if (ok && ca > 0 && tid == 0) {
+#pragma unroll
+                for (int a4 = 0; a4 < 4; ++a4) tma_store_3d(&smap, 32 * a4, 0, slot * p.H + h, sm.st[a4]);
+                bulk_commit();
+            }
         }
         // every read of the scratch record is complete: drop its lines from L2
         // without writing them back
@@ -496,6 +513,9 @@ __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyPar
             for (int j = 0; j < kDraft; ++j)
                 if (j < D) __stcs(ub + (int64_t)j * p.H * p.dv, (valid && ok) ? uu[j] : 0.f);
         }
+    }
+    if constexpr (FUSED) {
+        if (tid == 0) bulk_wait_all();  // the committed state's stores are complete
     }
     tc::fence_before_sync();
     __syncthreads();
