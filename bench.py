@@ -7,13 +7,14 @@ One step = one kda_decode launch over one batch of synthetic inputs; the
 batch and its slot set rotate over 16 disjoint slot sets so that each step
 touches 512 MiB of state that the previous step did not (more than the
 129 MB L2).  Extra paths measured in the same run (``paths`` key):
-speculative verify + commit (128 x 7 draft tokens x 32 heads), chunked
+speculative verify + commit (128 x 7 draft tokens x 32 heads), the fused
+ShortConv + decode + RMS-norm-gate step at the decode workload's size, chunked
 prefill (T = 8192 x 32 heads) and the long-context mix (T = 102400 prefill,
 256 decode steps on its final state, 1024 x 64-head decode over a
 16384-slot pool).
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-        [--paths decode,spec,prefill,longmix] [--no-cpu-baseline]
+        [--paths decode,spec,fused,prefill,longmix] [--no-cpu-baseline]
 With N > 1 it must run under torchrun (one process per GPU); every rank runs
 an independent replica (the recurrence has no cross-GPU exchange) and rank 0
 prints one JSON line with the whole-job throughput.
@@ -468,6 +469,42 @@ def run_spec(kda, peaks):
     }
 
 
+# fused decode (ShortConv + decode step + RMS norm and gate), per token-head:
+# the decode bytes + z (dv * 2) + the conv state read and write
+# (2 * 3 * (2 dk + dv) * 2); per launch once: conv taps H * (2 dk + dv) * 16
+# and the norm weight dv * 4
+FUSED_BYTES_PER_TH = DECODE_BYTES_PER_TH + 128 * 2 + 2 * 3 * 384 * 2  # 137474
+
+
+def run_fused(kda, peaks, B=256, H=32, NS=4096, n=200):
+    """The fused decode at the decode workload's size, rotating over 16
+    disjoint slot sets like the main line, beside the plain decode launch."""
+    dk = dv = 128
+    x = inputs.decode_inputs(B, H, dk, dv, dtype="bf16", num_slots=NS, seed=0, device="cuda")
+    ex = inputs.fused_extras(B, H, dk, dv, dtype="bf16", num_slots=NS, seed=0, device="cuda")
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5)
+    perm = torch.randperm(NS, generator=gen, device="cuda").to(torch.int32)
+    sets = [perm[i * B:(i + 1) * B].contiguous() for i in range(NS // B)]
+    out = torch.empty((B, H, dv), dtype=torch.bfloat16, device="cuda")
+    fcalls = [kda.decode_fused(x.q, x.k, x.v, x.g, x.b, ex.z, ss, x.pool, ex.conv_state, ex.conv_w,
+                               ex.norm_w, out, _prepare=True) for ss in sets]
+    dcalls = [kda.decode(x.q, x.k, x.v, x.g, x.b, ss, x.pool, out, _prepare=True) for ss in sets]
+    tf = time_launches(lambda i: fcalls[i % len(sets)](), n) / 1e6
+    td = time_launches(lambda i: dcalls[i % len(sets)](), n) / 1e6
+    fbytes = B * H * FUSED_BYTES_PER_TH + H * (2 * dk + dv) * 16 + dv * 4
+    gbs = fbytes / tf / 1e9
+    return {
+        "workload": "fused_decode_b256_h32_d128_pool4096_bf16",
+        "us": round(tf * 1e6, 2), "GB/s": round(gbs, 1),
+        "frac_hbm": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": fbytes,
+        "token_heads_per_s": round(B * H / tf, 1),
+        "plain_decode_us": round(td * 1e6, 2),
+        "bytes_per_token_head": FUSED_BYTES_PER_TH,
+        "launches": 2 * n,
+    }
+
+
 def run_prefill(kda, peaks, T=8192, H=32, steps=10, key="prefill_t8192_h32_d128_bf16", x=None):
     if x is None:
         x = inputs.prefill_inputs([T], H, 128, 128, dtype="bf16", seed=0, device="cuda")
@@ -717,7 +754,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--paths", default="decode,spec,prefill,longmix")
+    ap.add_argument("--paths", default="decode,spec,fused,prefill,longmix")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ncu-case", default=None,
                     help="run one small profiling case (decode_small, spec_small, prefill_small)")
@@ -745,6 +782,8 @@ def main(argv=None):
     if rank == 0:
         if "spec" in wanted:
             paths["verify_commit"] = run_spec(kda, peaks)
+        if "fused" in wanted:
+            paths["fused_decode"] = run_fused(kda, peaks)
         if "prefill" in wanted:
             paths["prefill"] = run_prefill(kda, peaks)
         if "longmix" in wanted:

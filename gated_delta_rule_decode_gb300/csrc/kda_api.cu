@@ -84,6 +84,29 @@ int kda_decode(const kda_dims *dims, int32_t batch, const void *q, const void *k
     return from_cuda(kda::launch_decode(p, dims->dk, dims->dtype, (cudaStream_t)stream));
 }
 
+int kda_decode_fused(const kda_dims *dims, int32_t batch, const void *q, const void *k,
+                     const void *v, const float *g, const void *b, const int32_t *slot_ids,
+                     float *pool, int64_t num_slots, const kda_fused_io *io, void *out,
+                     int32_t *err_flag, void *stream) {
+    int st = check_dims(dims);
+    if (st != KDA_OK) return st;
+    if (batch < 0 || num_slots < 0 || io == nullptr) return KDA_ERR_INVALID_ARG;
+    if (!(io->eps_o >= 0.f) || isinf(io->eps_o)) return KDA_ERR_INVALID_ARG;
+    if (batch == 0) return KDA_OK;
+    if (!all_aligned({q, k, v, g, out, io->conv_w, io->z, io->norm_w}) || b == nullptr ||
+        slot_ids == nullptr)
+        return KDA_ERR_INVALID_ARG;
+    if (num_slots > 0 && !all_aligned({pool, io->conv_state})) return KDA_ERR_INVALID_ARG;
+    kda::DecodeFusedParams p{};
+    p.q = q; p.k = k; p.v = v; p.g = g; p.b = b;
+    p.slot_ids = slot_ids; p.pool = pool; p.num_slots = num_slots;
+    p.conv_state = io->conv_state; p.conv_w = io->conv_w; p.z = io->z; p.norm_w = io->norm_w;
+    p.out = out; p.err_flag = err_flag;
+    p.batch = batch; p.H = dims->num_heads; p.dv = dims->dv;
+    p.eps = dims->eps; p.scale = resolve_scale(dims); p.eps_o = io->eps_o;
+    return from_cuda(kda::launch_decode_fused(p, dims->dk, dims->dtype, (cudaStream_t)stream));
+}
+
 size_t kda_verify_workspace_bytes(const kda_dims *dims, int32_t batch, int32_t draft_len) {
     if (check_dims(dims) != KDA_OK || batch < 0 || draft_len < 1 || draft_len > 16) return 0;
     return kda::verify_workspace_bytes(dims->num_heads, dims->dk, dims->dv, dims->dtype, batch, draft_len);

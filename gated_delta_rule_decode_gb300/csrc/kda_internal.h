@@ -22,6 +22,24 @@ struct DecodeParams {
     float eps, scale;
 };
 
+// Fused decode (ShortConv + decode step + RMS norm and sigmoid gate).
+struct DecodeFusedParams {
+    const void *q, *k, *v;
+    const float *g;
+    const void *b;
+    const int32_t *slot_ids;
+    float *pool;
+    int64_t num_slots;
+    void *conv_state;     // dtype [num_slots][H][3][2 dk + dv]
+    const float *conv_w;  // f32 [H][2 dk + dv][4]
+    const void *z;        // dtype [batch][H][dv]
+    const float *norm_w;  // f32 [dv]
+    void *out;
+    int32_t *err_flag;
+    int32_t batch, H, dv;
+    float eps, scale, eps_o;
+};
+
 struct VerifyParams {
     const void *q, *k, *v;
     const float *g;
@@ -128,6 +146,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encode_fn();
 
 // Each launcher returns cudaSuccess or the launch error.
 cudaError_t launch_decode(const DecodeParams &p, int dk, int dtype, cudaStream_t s);
+cudaError_t launch_decode_fused(const DecodeFusedParams &p, int dk, int dtype, cudaStream_t s);
 cudaError_t launch_verify(const VerifyParams &p, int dk, int dtype, cudaStream_t s);
 // Verify for bf16, dk = dv = 128, D <= 8 (window kernel + tensor-core state
 // kernel): the scratch it needs (0 for every other shape), whether it applies

@@ -85,6 +85,31 @@ def decode_inputs(B, H, dk, dv, dtype="bf16", num_slots=None, seed=0,
 
 
 @dataclass
+class FusedExtras:
+    conv_state: torch.Tensor  # [num_slots, H, 3, 2 dk + dv] (input dtype)
+    conv_w: torch.Tensor      # [H, 2 dk + dv, 4] fp32
+    z: torch.Tensor           # [B, H, dv] (input dtype)
+    norm_w: torch.Tensor      # [dv] fp32
+
+
+def fused_extras(B, H, dk, dv, dtype="bf16", num_slots=None, seed=0, device="cpu"):
+    """The fused decode's extra inputs, drawn after (and independently of)
+    ``decode_inputs`` from their own generator: conv state ~ N(0, 1) (raw
+    q/k/v-like inputs), conv taps ~ N(0, 0.5^2) (so that a width-4 conv of
+    N(0, 1) inputs stays near unit variance), gate pre-activations
+    z ~ N(0, 1), norm weight ~ N(1, 0.1^2)."""
+    num_slots = B if num_slots is None else num_slots
+    gen = _gen(seed + 7919, device)
+    dt = torch_dtype(dtype)
+    nc = 2 * dk + dv
+    conv_state = _normal((num_slots, H, 3, nc), gen, device).to(dt)
+    conv_w = _normal((H, nc, 4), gen, device, std=0.5)
+    z = _normal((B, H, dv), gen, device).to(dt)
+    norm_w = _normal((dv,), gen, device, std=0.1, mean=1.0)
+    return FusedExtras(conv_state, conv_w, z, norm_w)
+
+
+@dataclass
 class VerifyInputs:
     q: torch.Tensor             # [B, D, H, dk]
     k: torch.Tensor             # [B, D, H, dk]

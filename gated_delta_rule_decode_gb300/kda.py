@@ -36,7 +36,7 @@ EXPORTED = ("kda_decode", "kda_verify_record", "kda_replay_commit",
             "kda_prefill_chunked_static", "kda_static_scratch_bytes",
             "kda_verify_workspace_bytes", "kda_prefill_chunked_snapshots",
             "kda_records_u_bytes", "kda_verify_record_u", "kda_replay_commit_u",
-            "kda_commit_verify_u")
+            "kda_commit_verify_u", "kda_decode_fused")
 
 
 class KdaError(RuntimeError):
@@ -56,6 +56,11 @@ class KdaRecords(ctypes.Structure):
                 ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p)]
 
 
+class KdaFusedIo(ctypes.Structure):
+    _fields_ = [("conv_state", ctypes.c_void_p), ("conv_w", ctypes.c_void_p),
+                ("z", ctypes.c_void_p), ("norm_w", ctypes.c_void_p), ("eps_o", ctypes.c_float)]
+
+
 class KdaRecordsU(ctypes.Structure):
     _fields_ = [("k_hat", ctypes.c_void_p), ("g", ctypes.c_void_p), ("u", ctypes.c_void_p)]
 
@@ -67,6 +72,7 @@ _SZ = ctypes.c_size_t
 _PD = ctypes.POINTER(KdaDims)
 _PR = ctypes.POINTER(KdaRecords)
 _PRU = ctypes.POINTER(KdaRecordsU)
+_PF = ctypes.POINTER(KdaFusedIo)
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -78,6 +84,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
     lib.kda_decode.argtypes = [_PD, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                _I64, _VP, _VP, _VP]
+    lib.kda_decode_fused.argtypes = [_PD, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                     _I64, _PF, _VP, _VP, _VP]
+    lib.kda_decode_fused.restype = ctypes.c_int
     lib.kda_verify_record.argtypes = [_PD, _I32, _I32, _VP, _VP, _VP, _VP, _VP,
                                       _VP, _VP, _I64, _VP, _PR, _VP, _SZ, _VP, _VP]
     lib.kda_verify_workspace_bytes.argtypes = [_PD, _I32, _I32]
@@ -213,6 +222,42 @@ def decode(q, k, v, g, b, slot_ids, pool, out=None, *, eps=1e-6, scale=None,
     if _prepare:
         return _Prepared(_lib.kda_decode, args, "kda_decode", (dims,), out)
     _check(_lib.kda_decode(*args), "kda_decode")
+    return out
+
+
+def decode_fused(q, k, v, g, b, z, slot_ids, pool, conv_state, conv_w, norm_w, out=None, *,
+                 eps=1e-6, eps_o=1e-6, scale=None, err_flag=None, stream=None, _prepare=False):
+    """MegaKDA-style fused decode: ShortConv of q, k, v (conv_state shifted in
+    place), the decode step on ``pool``, then RMS norm x norm_w x sigmoid(z).
+
+    q, k: [B, H, dk]; v, z: [B, H, dv]; g: [B, H, dk] fp32; b: [B, H];
+    conv_state: [num_slots, H, 3, 2 dk + dv] (input dtype);
+    conv_w: [H, 2 dk + dv, 4] fp32; norm_w: [dv] fp32.  Returns out.
+    """
+    B, H, dk = k.shape
+    dv = v.shape[2]
+    dt = q.dtype
+    S = pool.shape[0]
+    for name, t, shp, d in (("q", q, (B, H, dk), dt), ("k", k, (B, H, dk), dt),
+                            ("v", v, (B, H, dv), dt), ("g", g, (B, H, dk), torch.float32),
+                            ("b", b, (B, H), dt), ("z", z, (B, H, dv), dt),
+                            ("slot_ids", slot_ids, (B,), torch.int32),
+                            ("pool", pool, (S, H, dv, dk), torch.float32),
+                            ("conv_state", conv_state, (S, H, 3, 2 * dk + dv), dt),
+                            ("conv_w", conv_w, (H, 2 * dk + dv, 4), torch.float32),
+                            ("norm_w", norm_w, (dv,), torch.float32)):
+        _need(t, name, shp, d)
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=dt, device=q.device)
+    _need(out, "out", (B, H, dv), dt)
+    dims = make_dims(H, dk, dv, _dtype_code(q), eps, scale)
+    io = KdaFusedIo(conv_state.data_ptr(), conv_w.data_ptr(), z.data_ptr(), norm_w.data_ptr(),
+                    float(eps_o))
+    args = (ctypes.byref(dims), B, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(slot_ids),
+            _ptr(pool), S, ctypes.byref(io), _ptr(out), _ptr(err_flag), _stream_handle(stream))
+    if _prepare:
+        return _Prepared(_lib.kda_decode_fused, args, "kda_decode_fused", (dims, io), out)
+    _check(_lib.kda_decode_fused(*args), "kda_decode_fused")
     return out
 
 

@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 4
+#define KDA_ABI_VERSION 5
 
 #if defined(__GNUC__)
 #define KDA_API __attribute__((visibility("default")))
@@ -140,6 +140,46 @@ KDA_API int kda_decode(const kda_dims *dims, int32_t batch, const void *q,
                const void *k, const void *v, const float *g, const void *b,
                const int32_t *slot_ids, float *pool, int64_t num_slots,
                void *out, int32_t *err_flag, void *stream);
+
+/*
+ * Inputs of kda_decode_fused besides the token's q, k, v, g, b:
+ *   conv_state  dtype [num_slots][H][3][2 dk + dv]  the last three RAW inputs
+ *               of each (slot, head), oldest first, channels ordered q | k | v;
+ *               read and shifted in place (same slots as the state pool)
+ *   conv_w      f32   [H][2 dk + dv][4]  depthwise conv taps per channel; tap 0
+ *               multiplies the oldest input, tap 3 the current one
+ *   z           dtype [batch][H][dv]     output-gate pre-activation
+ *   norm_w      f32   [dv]               RMS-norm weight (shared by the heads)
+ *   eps_o       RMS-norm epsilon inside the sqrt, >= 0
+ * All arrays are owned by the caller.
+ */
+typedef struct kda_fused_io {
+    void *conv_state;
+    const float *conv_w;
+    const void *z;
+    const float *norm_w;
+    float eps_o;
+} kda_fused_io;
+
+/*
+ * kda_decode_fused: one MegaKDA-style fused decode step ("2.8x faster Kimi K3
+ * inference on CANN", section 03 "MegaKDA": ShortConv and the output-side
+ * compute fused with the KDA recurrence in one operator).  For every
+ * (sequence n, head h), in one launch:
+ *   x~_c = silu(w_c0 x_{t-3,c} + w_c1 x_{t-2,c} + w_c2 x_{t-1,c} + w_c3 x_c)
+ *          for each channel c of q, k and v, with x_{t-3..t-1} from conv_state,
+ *          which is then shifted to hold x_{t-2}, x_{t-1}, x (raw inputs)
+ *   o    = the kda_decode step on (q~, k~, v~, g, b), held in fp32 (the
+ *          convolved values are never rounded to dtype), state written back
+ *   out  = o / sqrt(mean_i o_i^2 + eps_o) * norm_w * sigmoid(z)
+ * The input projections are not part of it.  Arguments as for kda_decode,
+ * plus `io`; supported shapes as for kda_decode.  Padding and out-of-range
+ * slots leave the state pool and the conv state untouched and output zero.
+ */
+KDA_API int kda_decode_fused(const kda_dims *dims, int32_t batch, const void *q,
+               const void *k, const void *v, const float *g, const void *b,
+               const int32_t *slot_ids, float *pool, int64_t num_slots,
+               const kda_fused_io *io, void *out, int32_t *err_flag, void *stream);
 
 /*
  * kda_verify_record: ReplaySSM verification of `draft_len` (1..16) draft
