@@ -149,6 +149,12 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (bulk copy) reads of the same memory.
+// Orders this thread's earlier generic-proxy accesses to global memory before
+// later async-proxy (bulk copy) accesses to the same locations.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -59,12 +59,14 @@ constexpr int D = 128;  // dk = dv
 constexpr float kSpanLimit = 80.f;
 
 // Operand image of one (chunk, head) in the workspace (bytes).
-constexpr uint32_t IMG_BW = 0;                         // [W; Q~] fp16, 128 rows x K 128
-constexpr uint32_t IMG_P = IMG_BW + 128 * 128 * 2;     // P       fp16, 64 rows x K 64
-constexpr uint32_t IMG_KT = IMG_P + 64 * 64 * 2;       // K^^T    fp16, 128 rows x K 64
-constexpr uint32_t IMG_EGC = IMG_KT + 128 * 64 * 2;    // e^{gamma_C}, 128 fp32
-constexpr uint32_t IMG_UP = IMG_EGC + 1024;            // U'^T [128 value rows][64 tokens] fp32, unit-swizzled rows
-constexpr uint32_t IMG_BYTES = IMG_UP + 64 * 128 * 4;  // 89 KiB
+// Every tile is fp16, K-major and 128B-swizzled, in the layout the chain's
+// products read it; row counts are those of the stacked tiles.
+constexpr uint32_t IMG_BQ = 0;                         // [-G^T; Q']: 128 key rows + 64 token rows, K = 128 keys
+constexpr uint32_t IMG_UPT = IMG_BQ + 192 * 128 * 2;   // U'^T: 128 value rows, K = 64 tokens
+constexpr uint32_t IMG_KP = IMG_UPT + 128 * 64 * 2;    // [K^^T; P]: 128 key rows + 64 token rows, K = 64 tokens
+constexpr uint32_t IMG_EGC = IMG_KP + 192 * 64 * 2;    // e^{gamma_C}, 128 fp32
+constexpr uint32_t IMG_TILES = IMG_EGC;                // the tiles, copied to the chain as one block
+constexpr uint32_t IMG_BYTES = IMG_EGC + 1024;         // 89 KiB
 constexpr float kHalfMax = 65504.f;                    // largest finite fp16
 
 __host__ __device__ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -84,6 +86,14 @@ __device__ __forceinline__ void st_h(unsigned char *tile, int rows, int row, int
 // two fp16 values in one 32-bit word: a in the low half, b in the high half
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// pack_h2 that also folds |a|, |b| (as fp16) into a running maximum: the
+// maximum is infinite once a value overflowed fp16 (NaNs are ignored)
+__device__ __forceinline__ uint32_t pack_h2_track(float a, float b, __half2 &hmax) {
+    const __half2 h = __floats2half2_rn(a, b);
+    hmax = __hmax2(hmax, __habs2(h));
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
@@ -174,7 +184,7 @@ struct PrepSmem {
     float gC[D];          // gamma at the chunk's last token
     float eref[D];        // e^{ref}
     float xs[32][33];     // partial products of the UT inverse
-    uint64_t bar_in, bar_v, bar_mma;
+    uint64_t bar_in, bar_v, bar_mma, bar_q, bar_kp;
     uint32_t tmem_base;
 };
 constexpr size_t kPrepSmem = sizeof(PrepSmem) + 1024;
@@ -220,6 +230,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
     if (tid == 0) {
         mbar_init(&sm.bar_in, 1);
         mbar_init(&sm.bar_v, 1);
+        mbar_init(&sm.bar_q, 1);
+        mbar_init(&sm.bar_kp, 1);
         mbar_init(&sm.bar_mma, 1);
         fence_barrier_init();
         mbar_arrive_expect_tx(&sm.bar_in, 2 * (C * D * 2) + C * D * 4);  // k, q (bf16) and g (fp32)
@@ -238,7 +250,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
     const uint32_t tm = sm.tmem_base;
     uint32_t phase = 0;
     // outstanding asynchronous work, for the drain after a timeout
-    bool in_pend = true, v_pend = false, mma_pend = false;
+    bool in_pend = true, v_pend = false, mma_pend = false, q_pend = false, kp_pend = false;
     bool ok = __syncthreads_and(tid == 0 ? mbar_wait(&sm.bar_in, 0) : true) != 0;
     if (ok) {
         in_pend = false;
@@ -246,7 +258,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
     } else if (tid == 0 && p.err_flag) {
         atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
     }
-    bool big = false;  // a W entry beyond the fp16 range of the chain's operands
+    __half2 hmax = __float2half2_rn(0.f);  // largest |entry| of the chain's fp16 operands written here
+    bool bulk_out = false;  // thread 0: bulk stores of staged image tiles issued
     bool unsafe = false;
     auto issue_v = [&]() {  // thread 0, once q has been read
         mbar_arrive_expect_tx(&sm.bar_v, C * D * 2);
@@ -389,11 +402,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                             make_float4(mi[4], mi[5], mi[6], mi[7]);
                     }
                 }
-                if (isq)  // Q~ = q^ e^{gamma}: row 64 + tok of [W; Q~], one 16-byte unit
-                    *reinterpret_cast<uint4 *>(img + IMG_BW + tc::sw128_off16(C + tok, c0, 128)) =
+                if (isq)  // Q~ = q^ e^{gamma}: row 128 + tok of [-G^T; Q'] until Q' replaces it
+                    *reinterpret_cast<uint4 *>(img + IMG_BQ + tc::sw128_off16(128 + tok, c0, 192)) =
                         make_uint4(pack_h2(qt[0], qt[1]), pack_h2(qt[2], qt[3]), pack_h2(qt[4], qt[5]),
                                    pack_h2(qt[6], qt[7]));
             }
+            // the Q~ rows come back by bulk copy in step 9
+            fence_proxy_async_global();
         }
         tc::wait_st();
         fence_proxy_async_smem();
@@ -440,7 +455,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             tc::st16(tc::lane_addr(tm, warp, PT_BK + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(&bk[16]));
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                *reinterpret_cast<uint4 *>(img + IMG_KT + tc::sw128_off16(lr, 32 * hf + 8 * j, 128)) =
+                *reinterpret_cast<uint4 *>(img + IMG_KP + tc::sw128_off16(lr, 32 * hf + 8 * j, 192)) =
                     make_uint4(kw[4 * j], kw[4 * j + 1], kw[4 * j + 2], kw[4 * j + 3]);
         }
 
@@ -473,7 +488,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                             const int j = 32 * hf + 8 * j8 + 2 * e;
                             w[e] = pack_h2(j <= r ? g32[8 * j8 + 2 * e] : 0.f, j + 1 <= r ? g32[8 * j8 + 2 * e + 1] : 0.f);
                         }
-                        *reinterpret_cast<uint4 *>(img + IMG_P + tc::sw128_off16(r, 32 * hf + 8 * j8, 64)) =
+                        *reinterpret_cast<uint4 *>(img + IMG_KP + tc::sw128_off16(128 + r, 32 * hf + 8 * j8, 192)) =
                             make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
@@ -496,7 +511,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                     }
                 }
                 areg[it] = (j < r) ? sm.beta[r] * a : 0.f;
-                st_h(img + IMG_P, 64, r, j, (j <= r) ? pp : 0.f);
+                st_h(img + IMG_KP, 192, 128 + r, j, (j <= r) ? pp : 0.f);
             }
             __syncthreads();
 #pragma unroll
@@ -507,6 +522,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             if (tid == 0) issue_v();
             v_pend = true;
         }
+        // the image rows of K^^T and P are read back by a bulk copy later
+        fence_proxy_async_global();
         __syncthreads();
     }
 
@@ -588,6 +605,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         }
         // ---- 7. beta V^T into TMEM (thread = value row lr, tokens 32 hf ..)
         ok = __syncthreads_and(tid == 0 ? mbar_wait(&sm.bar_v, 0) : true) != 0;
+        if (ok && tid == 0) {
+            // [K^^T; P] (this CTA's image rows) back into u1 behind the
+            // coming W^T tile, for the products of step 9; the inverse's
+            // scratch there has been read
+            mbar_arrive_expect_tx(&sm.bar_kp, 192 * 64 * 2);
+            bulk_g2s(reinterpret_cast<unsigned char *>(&sm.u1) + 128 * 64 * 2, img + IMG_KP, 192 * 64 * 2, &sm.bar_kp);
+        }
+        kp_pend = ok;
         if (ok) {
             v_pend = false;
             mbar_try_wait(&sm.bar_v, 0);
@@ -625,53 +650,163 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         ok = wait_mma(&sm.bar_mma, phase, p.err_flag);
         if (ok) {
             mma_pend = false;
-            // ---- 8. lane lr: W[r][lr] (column lr of the W rows of [W; Q~])
-            // and U'[r][lr] (row lr of U'^T, 16-byte units of four tokens at
-            // (u & 8) | ((u & 7) ^ (lr & 7))), tokens 32 hf .. + 31
-            // W rows go to a shared copy of their part of the [W; Q~] tile
-            // (over the inverse's scratch), which two bulk copies then store
-            unsigned char *up = img + IMG_UP + (size_t)lr * C * 4;
+            // ---- 8. lane lr, tokens 32 hf .. + 31: row lr of W^T into a
+            // shared tile (over the inverse's scratch; the B operand of the
+            // two products of step 9) and row lr of U'^T into a shared copy
+            // of its image tile (over T, which the finished products have
+            // read), stored by one bulk copy
             unsigned char *wt = reinterpret_cast<unsigned char *>(&sm.u1);
+            unsigned char *ut = sm.u2.t;
 #pragma unroll
             for (int r0 = 0; r0 < 32; r0 += 16) {
-                float w16[16];
+                float w16[16], u16[16];
                 tc::ld16(tc::lane_addr(tm, warp, PT_WT + 32 * hf + r0), w16);
+                tc::ld16(tc::lane_addr(tm, warp, PT_UPT + 32 * hf + r0), u16);
                 tc::wait_ld();
 #pragma unroll
-                for (int rr = 0; rr < 16; ++rr) {
-                    big |= !(fabsf(w16[rr]) <= kHalfMax) && w16[rr] == w16[rr];
-                    st_h(wt, 64, 32 * hf + r0 + rr, lr, w16[rr]);
-                }
-                tc::ld16(tc::lane_addr(tm, warp, PT_UPT + 32 * hf + r0), w16);
-                tc::wait_ld();
+                for (int q8 = 0; q8 < 16; q8 += 8) {
+                    uint32_t pw[4], pu[4];
 #pragma unroll
-                for (int rr = 0; rr < 16; rr += 4) {
-                    const int u = (32 * hf + r0 + rr) >> 2;
-                    *reinterpret_cast<float4 *>(up + (((u & 8) | ((u & 7) ^ (lr & 7))) << 4)) =
-                        make_float4(w16[rr], w16[rr + 1], w16[rr + 2], w16[rr + 3]);
+                    for (int e = 0; e < 4; ++e) {
+                        const float a0 = w16[q8 + 2 * e], a1 = w16[q8 + 2 * e + 1];
+                        const float b0 = u16[q8 + 2 * e], b1 = u16[q8 + 2 * e + 1];
+                        pw[e] = pack_h2_track(a0, a1, hmax);
+                        pu[e] = pack_h2_track(b0, b1, hmax);
+                    }
+                    const int t = 32 * hf + r0 + q8;
+                    *reinterpret_cast<uint4 *>(wt + tc::sw128_off16(lr, t, 128)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                    *reinterpret_cast<uint4 *>(ut + tc::sw128_off16(lr, t, 128)) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
                 }
             }
         }
     }
     if (ok) {
-        // the W rows: rows 0..63 of each 64-channel column of [W; Q~]
-        fence_proxy_async_smem();
+        // ---- 9. the state-independent products of the chain step:
+        // G^T = K^^T W (M = 128 key rows, N = 128 keys) and P W (M = 128, of
+        // which rows 0..63 are P's; N = 128 keys), kind::f16, K = 64 tokens.
+        // [K^^T; P] came back from the image (this CTA's own writes) into
+        // the shared memory behind the W^T tile by a bulk copy issued in
+        // step 7; the A tile of P W spans
+        // 64 rows past P, whose products land in TMEM lanes nobody reads.
+        unsigned char *wt = reinterpret_cast<unsigned char *>(&sm.u1);
+        unsigned char *kp = wt + 128 * 64 * 2;
+        static_assert(128 * 64 * 2 + 2 * 128 * 64 * 2 <= sizeof(sm.u1), "W^T and the [K^^T; P] A tiles fit u1");
+        static_assert(192 * 128 * 2 <= sizeof(sm.u1) && 128 * 64 * 2 <= sizeof(sm.u2.t), "staged image tiles fit");
+        fence_proxy_async_smem();  // the W^T and U'^T tiles, for the products and the bulk store
+        tc::fence_before_sync();   // step 8's TMEM reads, before the products overwrite those columns
         __syncthreads();
+        // the Q~ rows of the [-G^T; Q'] tile (one 8 KB run per 64-key
+        // column block) into the upper half of u2, for the Q' epilogue
+        unsigned char *qs = sm.u2.gam + 128 * 64 * 2;
+        static_assert(2 * 128 * 64 * 2 <= sizeof(sm.u2), "U'^T and Q~ fit u2");
         if (tid == 0) {
-            const unsigned char *wt = reinterpret_cast<const unsigned char *>(&sm.u1);
-            bulk_s2g(img + IMG_BW, wt, C * 128);
-            bulk_s2g(img + IMG_BW + 128 * 128, wt + C * 128, C * 128);
+            bulk_s2g(img + IMG_UPT, sm.u2.t, 128 * 64 * 2);
             bulk_commit();
-            bulk_wait_all();
+            bulk_out = true;
+            mbar_arrive_expect_tx(&sm.bar_q, 2 * C * 128);
+            bulk_g2s(qs, img + IMG_BQ + 128 * 128, C * 128, &sm.bar_q);
+            bulk_g2s(qs + C * 128, img + IMG_BQ + 192 * 128 + 128 * 128, C * 128, &sm.bar_q);
+        }
+        q_pend = true;
+        ok = __syncthreads_and(tid == 0 ? mbar_wait(&sm.bar_kp, 0) : true) != 0;
+        if (ok) {
+            kp_pend = false;
+            mbar_try_wait(&sm.bar_kp, 0);
+        } else if (tid == 0 && p.err_flag) {
+            atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
+        }
+        tc::fence_after_sync();
+        if (ok && tid == 0) {
+            constexpr uint32_t id = tc::idesc_f16(128, 128);
+            const uint32_t ak = tc::smem_u32(kp), ap = tc::smem_u32(kp + 128 * 128), bw = tc::smem_u32(wt);
+#pragma unroll
+            for (int ks = 0; ks < C / 16; ++ks) {
+                const uint64_t bd = tc::desc_tf32_kstep(bw, 128, ks);
+                tc::mma_f16_ss(tm + 0, tc::desc_tf32_kstep(ak, 128, ks), bd, id, ks > 0);
+                tc::mma_f16_ss(tm + 128, tc::desc_tf32_kstep(ap, 128, ks), bd, id, ks > 0);
+            }
+            tc::commit(&sm.bar_mma);
+        }
+        mma_pend = ok;
+        if (ok) ok = wait_mma(&sm.bar_mma, phase, p.err_flag);
+        if (ok) {
+            mma_pend = false;
+            // [-G^T; Q'] goes to a shared copy of its image tile over u1 (the
+            // products that read W^T and [K^^T; P] there are done), then out
+            // by one bulk copy.
+            unsigned char *bq = reinterpret_cast<unsigned char *>(&sm.u1);
+            // -G^T row lr (key channel lr), keys 64 hf .. + 63
+#pragma unroll
+            for (int j0 = 0; j0 < 64; j0 += 16) {
+                float g16[16];
+                tc::ld16(tc::lane_addr(tm, warp, 64 * hf + j0), g16);
+                tc::wait_ld();
+#pragma unroll
+                for (int q8 = 0; q8 < 16; q8 += 8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float a0 = g16[q8 + 2 * e], a1 = g16[q8 + 2 * e + 1];
+                        w[e] = pack_h2_track(-a0, -a1, hmax);
+                    }
+                    *reinterpret_cast<uint4 *>(bq + tc::sw128_off16(lr, 64 * hf + j0 + q8, 192)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            // Q' = Q~ - P W: row 128 + lr of the tile, lanes 0..63 (Q~ from
+            // its staged copy: row lr of the 64-row run of column block hf)
+            ok = __syncthreads_and(tid == 0 ? mbar_wait(&sm.bar_q, 0) : true) != 0;
+            if (ok) {
+                q_pend = false;
+                mbar_try_wait(&sm.bar_q, 0);
+            } else if (tid == 0 && p.err_flag) {
+                atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
+            }
+            if (ok && lr < C) {
+#pragma unroll
+                for (int j0 = 0; j0 < 64; j0 += 16) {
+                    float pw16[16];
+                    tc::ld16(tc::lane_addr(tm, warp, 128 + 64 * hf + j0), pw16);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int q8 = 0; q8 < 16; q8 += 8) {
+                        const int u = (j0 + q8) >> 3;
+                        const uint4 qt = *reinterpret_cast<const uint4 *>(qs + hf * C * 128 + lr * 128 +
+                                                                          ((u ^ (lr & 7)) << 4));
+                        const uint32_t qw[4] = {qt.x, qt.y, qt.z, qt.w};
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 qf = __half22float2(*reinterpret_cast<const __half2 *>(&qw[e]));
+                            const float a0 = qf.x - pw16[q8 + 2 * e], a1 = qf.y - pw16[q8 + 2 * e + 1];
+                            w[e] = pack_h2_track(a0, a1, hmax);
+                        }
+                        *reinterpret_cast<uint4 *>(bq + tc::sw128_off16(128 + lr, 64 * hf + j0 + q8, 192)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (ok && tid == 0) {
+                bulk_s2g(img + IMG_BQ, bq, 192 * 128 * 2);
+                bulk_commit();
+            }
         }
     }
+    // the staged tiles have been read out of shared memory before the CTA ends
+    // (their global writes complete with the kernel)
+    if (tid == 0 && bulk_out) bulk_wait_read_all();
     if (!ok && tid == 0) {
         // let every copy and product still in flight finish before the CTA
         // releases its memory
         if (in_pend) mbar_wait_drain(&sm.bar_in, 0);
         if (v_pend) mbar_wait_drain(&sm.bar_v, 0);
+        if (q_pend) mbar_wait_drain(&sm.bar_q, 0);
+        if (kp_pend) mbar_wait_drain(&sm.bar_kp, 0);
         if (mma_pend) mbar_wait_drain(&sm.bar_mma, phase & 1);
     }
+    const bool big = !(__low2float(hmax) <= kHalfMax) || !(__high2float(hmax) <= kHalfMax);
     if (__syncthreads_or(big) && tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_RANGE);
     tc::fence_before_sync();
     __syncthreads();
@@ -685,36 +820,43 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
 // serve the same 32 lanes and take one quarter of the columns each.  The fp32
 // state lives in the data warps' registers (thread (i, quarter q) holds
 // S[i][32 q .. 32 q + 31]); its fp16 copy S16 in TMEM is the A operand of the
-// first product.  Per chunk c:
-//   X  = S16 [W; Q~]^T        kind::f16, N = 128 (tokens of W, then of Q~), K = 128
-//   U^T = U'^T - X[:, 0:64]   data warps, written as fp16 into TMEM
-//   Z  = U^T K^               kind::f16, N = 128 channels, K = 64 tokens
-//   O^T = X[:, 64:] + U^T P^T kind::f16, N = 64 tokens, K = 64
-//   S = S diag(e^{gamma_C}) + Z, S16 = fp16(S)   data warps
-// The issuing warp (one thread) waits on "S16 ready" and "U16 ready"
-// barriers that the data warps arrive on, issues the products and the bulk
-// copies of the operand images (one per chunk, two buffers, the chunk after
-// next prefetched into L2).  The data warps observe the products' completion
-// barriers themselves, one lane per warp polling, so no CTA-wide barrier
-// sits in the chunk loop.  Only X -> U -> Z -> S16 is on the serial path: a
-// chunk's outputs go out (one tensor store per full chunk) while the next
-// chunk's X runs.
+// one product that needs it.  With G = W^T K^ and Q' = Q~ - P W formed by
+// the prep kernel, chunk c is (accumulator ACC = [D | O^T], 192 columns)
+//   ACC  = U'^T [K^^T; P]^T            kind::f16, N = 192, K = 64 tokens
+//   ACC += S16 [-G^T; Q']^T            kind::f16, N = 192, K = 128 keys
+//   S = S diag(e^{gamma_C}) + D, S16 = fp16(S)     data warps
+//   outputs = scale * O^T                          data warps
+// The first product does not depend on the state: it is issued for chunk
+// c + 1 while the data warps update the state of chunk c, so the serial path
+// is only S16 -> the second product -> the state update -> S16.  The issuing
+// warp (one thread) waits on the "S16 ready" barrier and on "accumulator
+// free" barriers that the data warps arrive on, issues the products and the
+// bulk copies of the operand images (two buffers; the chunk after next
+// prefetched into L2; e^{gamma_C} into a ring of four with barriers of its
+// own, so that an image buffer can be refilled as soon as its products are
+// done and only the issuing thread ever waits on an image barrier).  The data warps observe
+// the products' completion barriers themselves, one lane per warp polling,
+// so no CTA-wide barrier sits in the chunk loop.  A full chunk's outputs
+// leave through a shared tile and one TMA tensor store.
 constexpr int kDataWarps = 16;
 constexpr int kDataThreads = 32 * kDataWarps;
 constexpr int kChainThreads = kDataThreads + 32;  // + the issuing warp
-constexpr uint32_t CT_D1 = 0;     // X (64 columns) then O (64), two buffers of 128
-constexpr uint32_t CT_Z = 256;    // U^T K^, 128 columns
-constexpr uint32_t CT_S16 = 384;  // fp16 state, two per column: 64 columns
-constexpr uint32_t CT_U16 = 448;  // fp16 U^T: two buffers of 32 columns
+constexpr uint32_t CT_ACC = 0;      // accumulators [D (128) | O^T (64)] at columns 0 and 256
+constexpr uint32_t CT_ACC_STRIDE = 256;
+constexpr uint32_t CT_S16 = 448;    // fp16 state, two per column: 64 columns
 constexpr uint32_t CT_COLS = 512;
-static_assert(IMG_BYTES % 1024 == 0, "image buffers stay 1024-aligned");
+constexpr uint32_t kAccN = 192;
+static_assert(IMG_TILES % 1024 == 0, "image buffers stay 1024-aligned");
 
 struct ChainSmem {
-    unsigned char img[2][IMG_BYTES];  // a chunk's operand image, as laid out in the workspace
+    unsigned char img[2][IMG_TILES];  // a chunk's operand tiles, as laid out in the workspace
     unsigned char ot[2][C * D * 2];   // a full chunk's outputs [64 tokens][128 value rows], for the TMA store
+    float egc[4][D];                  // e^{gamma_C} of chunk c in egc[c & 3]
     uint64_t full[2];                 // chunk images landed
-    uint64_t mma1, mma2s, mma2o;      // X, Z, output product done
-    uint64_t s16_ready, u16_ready;    // the data warps' hand-offs (one arrival per data warp)
+    uint64_t egc_full[4];             // e^{gamma_C} of chunk c landed in egc[c & 3]
+    uint64_t acc_done[2];             // both products of the chunk using this accumulator done
+    uint64_t acc_free[2];             // the data warps have read this accumulator (one arrival per data warp)
+    uint64_t s16_ready;               // S16 written (one arrival per data warp)
     uint64_t tile_full;               // an output tile written (one arrival per data warp)
     uint64_t tile_free[2];            // an output tile's tensor store has read it (thread 0)
     uint32_t tmem_base;
@@ -732,8 +874,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
     return okw;
 }
 
-// The data warp's hand-off: its TMEM stores are complete and ordered before
-// lane 0's arrival.
+// The data warp's hand-off: its TMEM accesses are complete and ordered
+// before lane 0's arrival.
 __device__ __forceinline__ void warp_arrive(uint64_t *bar) {
     tc::wait_st();
     tc::fence_before_sync();
@@ -768,16 +910,15 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
 
     if (warp == 0) tc::tmem_alloc(&sm.tmem_base, CT_COLS);
     if (tid == 0) {
-        mbar_init(&sm.full[0], 1);
-        mbar_init(&sm.full[1], 1);
-        mbar_init(&sm.mma1, 1);
-        mbar_init(&sm.mma2s, 1);
-        mbar_init(&sm.mma2o, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.full[b], 1);
+            mbar_init(&sm.acc_done[b], 1);
+            mbar_init(&sm.acc_free[b], kDataWarps);
+            mbar_init(&sm.tile_free[b], 1);
+        }
+        for (int r = 0; r < 4; ++r) mbar_init(&sm.egc_full[r], 1);
         mbar_init(&sm.s16_ready, kDataWarps);
-        mbar_init(&sm.u16_ready, kDataWarps);
         mbar_init(&sm.tile_full, kDataWarps);
-        mbar_init(&sm.tile_free[0], 1);
-        mbar_init(&sm.tile_free[1], 1);
         fence_barrier_init();
     }
     tc::fence_before_sync();
@@ -791,77 +932,97 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
     if (warp == kDataWarps) {
         // ================= issuing warp (lane 0)
         if ((tid & 31) == 0) {
-            int last_issue[2] = {-1, -1};
+            int last_issue[2] = {-1, -1}, last_egc[4] = {-1, -1, -1, -1};
+            int ndone[2] = {0, 0};  // commits on acc_done[b]
+            int open_b = -1;        // an accumulator with products issued after its last commit
             auto issue = [&](int ci) {
                 const int b = ci & 1;
-                mbar_arrive_expect_tx(&sm.full[b], IMG_BYTES);
-                bulk_g2s(sm.img[b], image(ci), IMG_BYTES, &sm.full[b]);
+                mbar_arrive_expect_tx(&sm.full[b], IMG_TILES);
+                bulk_g2s(sm.img[b], image(ci), IMG_TILES, &sm.full[b]);
+                mbar_arrive_expect_tx(&sm.egc_full[ci & 3], D * 4);
+                bulk_g2s(sm.egc[ci & 3], image(ci) + IMG_EGC, D * 4, &sm.egc_full[ci & 3]);
                 last_issue[b] = ci;
+                last_egc[ci & 3] = ci;
                 if (ci + 2 < nchunks) bulk_prefetch_l2(image(ci + 2), IMG_BYTES);
+            };
+            constexpr uint32_t id = tc::idesc_f16(128, kAccN);
+            // ACC[b] = U'^T [K^^T; P]^T (chunk ci's image in buffer b = ci & 1)
+            auto mma_u = [&](int ci) {
+                const int b = ci & 1;
+                const uint32_t a0 = tc::smem_u32(sm.img[b] + IMG_UPT), b0 = tc::smem_u32(sm.img[b] + IMG_KP);
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks)
+                    tc::mma_f16_ss(tm + CT_ACC + b * CT_ACC_STRIDE, tc::desc_tf32_kstep(a0, 128, ks),
+                                   tc::desc_tf32_kstep(b0, 192, ks), id, ks > 0);
+                open_b = b;
+            };
+            // ACC[b] += S16 [-G^T; Q']^T, then the commit that releases both
+            auto mma_s = [&](int ci) {
+                const int b = ci & 1;
+                const uint32_t b0 = tc::smem_u32(sm.img[b] + IMG_BQ);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                    tc::mma_f16_ts(tm + CT_ACC + b * CT_ACC_STRIDE, tm + CT_S16 + 8 * ks,
+                                   tc::desc_tf32_kstep(b0, 192, ks), id, 1);
+                tc::commit(&sm.acc_done[b]);
+                ++ndone[b];
+                open_b = -1;
             };
             if (nchunks > 0) issue(0);
             if (nchunks > 1) issue(1);
-            int nx = 0, nz = 0;  // products committed so far (X; Z and O)
+            if (nchunks > 0) {
+                ok = mbar_wait(&sm.full[0], 0);
+                if (ok) {
+                    tc::fence_after_sync();
+                    mma_u(0);
+                    ok = mbar_wait(&sm.s16_ready, 0);
+                }
+            }
             for (int c = 0; c < nchunks && ok; ++c) {
                 const int b = c & 1;
-                // ---- X of chunk c: S16 (its hand-off) and the image
-                ok = mbar_wait(&sm.s16_ready, c & 1) && mbar_wait(&sm.full[b], (c >> 1) & 1);
-                if (!ok) break;
+                // ---- the serial product of chunk c (S16 of chunk c is ready)
                 tc::fence_after_sync();
-                {
-                    constexpr uint32_t id = tc::idesc_f16(128, 128);
-                    const uint32_t b0 = tc::smem_u32(sm.img[b] + IMG_BW), d1 = CT_D1 + b * 128;
-#pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks)
-                        tc::mma_f16_ts(tm + d1, tm + CT_S16 + 8 * ks, tc::desc_tf32_kstep(b0, 128, ks), id, ks > 0);
-                    tc::commit(&sm.mma1);
-                    ++nx;
-                }
-                // ---- chunk c - 1's buffer is free once its products are done
-                // (and its readers, the data warps, handed over S16 of chunk c)
-                if (c >= 1 && c + 1 < nchunks) {
-                    ok = mbar_wait(&sm.mma2o, (c - 1) & 1);
+                mma_s(c);
+                // ---- the state-independent product of chunk c + 1: its image
+                // has landed and the data warps have read chunk c - 1's
+                // accumulator, which it reuses
+                if (c + 1 < nchunks) {
+                    ok = mbar_wait(&sm.full[b ^ 1], ((c + 1) >> 1) & 1) &&
+                         (c == 0 || mbar_wait(&sm.acc_free[b ^ 1], ((c - 1) >> 1) & 1));
                     if (!ok) break;
-                    issue(c + 1);
+                    tc::fence_after_sync();
+                    mma_u(c + 1);
                 }
-                // ---- Z, then O, of chunk c: U16 (its hand-off)
-                ok = mbar_wait(&sm.u16_ready, c & 1);
-                if (!ok) break;
-                tc::fence_after_sync();
-                {
-                    const uint32_t u16 = CT_U16 + b * 32, d1 = CT_D1 + b * 128;
-                    const uint32_t kt = tc::smem_u32(sm.img[b] + IMG_KT), pp = tc::smem_u32(sm.img[b] + IMG_P);
-#pragma unroll
-                    for (int ks = 0; ks < C / 16; ++ks)
-                        tc::mma_f16_ts(tm + CT_Z, tm + u16 + 8 * ks, tc::desc_tf32_kstep(kt, 128, ks),
-                                       tc::idesc_f16(128, 128), ks > 0);
-                    tc::commit(&sm.mma2s);
-#pragma unroll
-                    for (int ks = 0; ks < C / 16; ++ks)
-                        tc::mma_f16_ts(tm + d1 + 64, tm + u16 + 8 * ks, tc::desc_tf32_kstep(pp, 64, ks),
-                                       tc::idesc_f16(128, 64), 1);
-                    tc::commit(&sm.mma2o);
-                    ++nz;
+                // ---- chunk c's products have read image buffer b: refill it
+                if (c + 2 < nchunks) {
+                    ok = mbar_wait(&sm.acc_done[b], (c >> 1) & 1);
+                    if (!ok) break;
+                    issue(c + 2);
                 }
+                if (c + 1 < nchunks) ok = mbar_wait(&sm.s16_ready, (c + 1) & 1);
             }
             if (!ok && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
             // no product or copy may still be writing when the CTA releases its
-            // memory: the last commit of each barrier and the last copy into
-            // each buffer (a phase already complete passes at once)
-            if (nx > 0) mbar_wait_drain(&sm.mma1, (nx - 1) & 1);
-            if (nz > 0) {
-                mbar_wait_drain(&sm.mma2s, (nz - 1) & 1);
-                mbar_wait_drain(&sm.mma2o, (nz - 1) & 1);
+            // memory: products issued after the last commit get one of their
+            // own, then the last commit of each barrier and the last copy into
+            // each buffer are waited for (a phase already complete passes at once)
+            if (open_b >= 0) {
+                tc::commit(&sm.acc_done[open_b]);
+                ++ndone[open_b];
             }
-            for (int b = 0; b < 2; ++b)
+            for (int b = 0; b < 2; ++b) {
+                if (ndone[b] > 0) mbar_wait_drain(&sm.acc_done[b], (ndone[b] - 1) & 1);
                 if (last_issue[b] >= 0) mbar_wait_drain(&sm.full[b], (last_issue[b] >> 1) & 1);
+            }
+            for (int r = 0; r < 4; ++r)
+                if (last_egc[r] >= 0) mbar_wait_drain(&sm.egc_full[r], (last_egc[r] >> 2) & 1);
         }
     } else {
         // ================= data warps
         const int lr = ((warp & 3) << 5) | (tid & 31);  // value row = TMEM lane
         const int cq = warp >> 2;                        // quarter of the columns this thread takes
         auto taddr = [&](uint32_t col) { return tc::lane_addr(tm, warp, (int)col); };
-        bool bad = false;  // a U entry beyond the fp16 range (or not a number)
+        __half2 s16max = __float2half2_rn(0.f);  // running max of |S16|: inf or NaN once S16 overflowed
         Sg = p.pool + ((int64_t)slot * H + h) * (int64_t)D * D + (int64_t)lr * D + cq * 32;
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
@@ -872,22 +1033,27 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
         auto store_s16 = [&]() {
             uint32_t w[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) w[e] = pack_h2(S[2 * e], S[2 * e + 1]);
+            for (int e = 0; e < 16; ++e) {
+                const __half2 h2 = __floats2half2_rn(S[2 * e], S[2 * e + 1]);
+                s16max = __hmax2_nan(s16max, __habs2(h2));
+                w[e] = *reinterpret_cast<const uint32_t *>(&h2);
+            }
             tc::st16u(taddr(CT_S16 + cq * 16), w);
         };
-        // outputs of chunk cj (tokens cq * 16 .. + 15 of value row lr): a full
+        // outputs of chunk cj (tokens cq * 16 .. + 15 of value row lr), read
+        // from its accumulator (complete: acc_done was observed): a full
         // chunk through its tile and one tensor store, a partial one straight
         // to global memory.  Tile hand-offs go through mbarriers (bounded
         // waits): the data warps arrive on tile_full once their part is
         // written, thread 0 then issues the store and, once the previous
         // store has read its tile, arrives on that tile's tile_free.
         auto output = [&](int cj) {
-            if (!warp_wait(&sm.mma2o, cj & 1)) return false;
             const int64_t tj = (int64_t)cs + (int64_t)cj * C;
             const int Lj = (int)((int64_t)ce - tj < C ? (int64_t)ce - tj : C);
             float o[16];
-            tc::ld16(taddr(CT_D1 + (cj & 1) * 128 + 64 + cq * 16), o);
+            tc::ld16(taddr(CT_ACC + (cj & 1) * CT_ACC_STRIDE + 128 + cq * 16), o);
             tc::wait_ld();
+            warp_arrive(&sm.acc_free[cj & 1]);  // the accumulator has been read
             if (Lj == C) {
                 const int t = cj & 1, use = cj >> 1;  // the tile and its use count
                 if (use > 0 && !warp_wait(&sm.tile_free[t], (use - 1) & 1)) return false;
@@ -934,68 +1100,42 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
         };
         for (int c = 0; c < nchunks && ok; ++c) {
             const int b = c & 1;
-            const unsigned char *im = sm.img[b];
-            // ---- the previous chunk's outputs while X runs
-            if (c > 0) {
-                ok = output(c - 1);
-                if (!ok) break;
-            }
-            // ---- U^T = U'^T - X[:, 0:64], fp16 into TMEM (each warp also
-            // observes chunk c's image barrier before reading U'^T and e^gamma)
-            ok = warp_wait(&sm.mma1, c & 1) && warp_wait(&sm.full[b], (c >> 1) & 1);
+            // ---- S = S diag(e^{gamma_C}) + D, and its fp16 copy (each warp
+            // observes the barrier of chunk c's e^{gamma_C} before reading it;
+            // its slot is refilled only after every data warp has handed
+            // over S16 of chunk c + 1)
+            ok = warp_wait(&sm.acc_done[b], (c >> 1) & 1) && warp_wait(&sm.egc_full[c & 3], (c >> 2) & 1);
             if (!ok) break;
             {
-                float x[16];
-                tc::ld16(taddr(CT_D1 + b * 128 + cq * 16), x);
-                const unsigned char *urow = im + IMG_UP + lr * (C * 4);
-                float up[16];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int u = cq * 4 + j;
-                    const float4 v4 =
-                        *reinterpret_cast<const float4 *>(urow + (((u & 8) | ((u & 7) ^ (lr & 7))) << 4));
-                    up[4 * j] = v4.x; up[4 * j + 1] = v4.y; up[4 * j + 2] = v4.z; up[4 * j + 3] = v4.w;
-                }
-                tc::wait_ld();
-                uint32_t w[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float u0 = up[2 * e] - x[2 * e], u1 = up[2 * e + 1] - x[2 * e + 1];
-                    bad |= !(fabsf(u0) <= kHalfMax) || !(fabsf(u1) <= kHalfMax);
-                    w[e] = pack_h2(u0, u1);
-                }
-                tc::st8u(taddr(CT_U16 + b * 32 + cq * 8), w);
-            }
-            warp_arrive(&sm.u16_ready);
-            // ---- S = S diag(e^{gamma_C}) + Z, and its fp16 copy
-            ok = warp_wait(&sm.mma2s, c & 1);
-            if (!ok) break;
-            {
-                float z[32];
-                tc::ld32(taddr(CT_Z + cq * 32), z);
-                const float4 *e4 = reinterpret_cast<const float4 *>(im + IMG_EGC) + cq * 8;
+                float d[32];
+                tc::ld32(taddr(CT_ACC + b * CT_ACC_STRIDE + cq * 32), d);
+                const float4 *e4 = reinterpret_cast<const float4 *>(sm.egc[c & 3]) + cq * 8;
                 tc::wait_ld();
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const float4 g4 = e4[j];
-                    S[4 * j] = fmaf(S[4 * j], g4.x, z[4 * j]);
-                    S[4 * j + 1] = fmaf(S[4 * j + 1], g4.y, z[4 * j + 1]);
-                    S[4 * j + 2] = fmaf(S[4 * j + 2], g4.z, z[4 * j + 2]);
-                    S[4 * j + 3] = fmaf(S[4 * j + 3], g4.w, z[4 * j + 3]);
+                    const float2 lo = __ffma2_rn(make_float2(S[4 * j], S[4 * j + 1]), make_float2(g4.x, g4.y),
+                                                 make_float2(d[4 * j], d[4 * j + 1]));
+                    const float2 hi = __ffma2_rn(make_float2(S[4 * j + 2], S[4 * j + 3]), make_float2(g4.z, g4.w),
+                                                 make_float2(d[4 * j + 2], d[4 * j + 3]));
+                    S[4 * j] = lo.x; S[4 * j + 1] = lo.y; S[4 * j + 2] = hi.x; S[4 * j + 3] = hi.y;
                 }
                 store_s16();
             }
             warp_arrive(&sm.s16_ready);
+            // ---- chunk c's outputs, off the serial path
+            ok = output(c);
+            if (!ok) break;
             // the state after c + 1 chunks, where a snapshot asks for it
             if (snap_ptr < snap_hi)
                 snap_ptr = snap_due(p, snap_ptr, snap_hi, min((int64_t)(c + 1) * C, (int64_t)ce - cs), C, snap_bad,
                                     store_snapshot);
         }
-        if (ok && nchunks > 0) ok = output(nchunks - 1);
         // requests past the sequence's last whole chunk can never be met
         if (ok && snap_ptr < snap_hi) snap_bad = true;
         if (snap_bad && h == 0 && tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_SNAPSHOT);
         if (tid == 0) bulk_wait_all();  // every tensor store complete before shared memory goes
+        const bool bad = !(__low2float(s16max) <= kHalfMax) || !(__high2float(s16max) <= kHalfMax);
         if (bad && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_RANGE);
         if (!ok && (tid & 31) == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
     }

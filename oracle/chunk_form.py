@@ -93,6 +93,22 @@ def chunk_step(S0, inter, scale: float):
     return O, S_C
 
 
+def chunk_step_split(S0, inter, scale: float):
+    """The same chunk step with every state-independent product formed first.
+
+    Substituting U = U' - W S0^T into the two uses of U gives
+      S_C = S0 diag(e^{gamma_C}) + U'^T K^ - S0 G,   G = W^T K^  (dk x dk)
+      O   = scale (Q' S0^T + P U'),                   Q' = Q~ - P W
+    so that the only product that needs the incoming state is S0 [G; Q']
+    (exact algebra: the result differs from chunk_step by rounding only).
+    """
+    G = inter["W"].T @ inter["K_hat_end"]
+    Qp = inter["Q_tilde"] - inter["P"] @ inter["W"]
+    O = scale * (Qp @ S0.T + inter["P"] @ inter["U_prime"])
+    S_C = S0 * np.exp(inter["gamma"][-1])[None, :] + inter["U_prime"].T @ inter["K_hat_end"] - S0 @ G
+    return O, S_C
+
+
 def prefill(q, k, v, g, b, S0=None, chunk: int = 64, eps: float = 1e-6,
             scale=None):
     """Chunked prefill of one (sequence, head); the last chunk may be partial.

@@ -367,6 +367,25 @@ def test_chunk_form_equals_recurrence(T):
     np.testing.assert_allclose(S_c, S_ref, rtol=1e-9, atol=1e-11)
 
 
+@pytest.mark.parametrize("L", [64, 37])
+def test_chunk_step_split_equals_chunk_step(L):
+    """The state-independent split of the chunk step (G = W^T K^, Q' = Q~ - P W)
+    is the same map as the U form, on a full and a partial chunk."""
+    rng = np.random.default_rng(100 + L)
+    dk, dv = 32, 24
+    q, k, v, g, b = _random_tokens(rng, L, dk, dv, g_mean=3.0)
+    S0 = 0.3 * rng.standard_normal((dv, dk))
+    inter = chunk_form.chunk_intermediates(q, k, v, g, b)
+    o1, s1 = chunk_form.chunk_step(S0, inter, dk ** -0.5)
+    o2, s2 = chunk_form.chunk_step_split(S0, inter, dk ** -0.5)
+    np.testing.assert_allclose(o2, o1, rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(s2, s1, rtol=1e-11, atol=1e-13)
+    # and both are the token loop
+    o_ref, s_ref = oracle.recurrence(q, k, v, g, b, S0=S0)
+    np.testing.assert_allclose(o2, o_ref, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(s2, s_ref, rtol=1e-9, atol=1e-11)
+
+
 def test_chunk_form_strong_decay():
     """Large per-token decay (alpha ~ e^-3) stays finite and equal to the loop."""
     rng = np.random.default_rng(99)
