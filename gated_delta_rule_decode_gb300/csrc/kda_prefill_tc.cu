@@ -45,6 +45,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <climits>
+
 #include "kda.h"
 #include "kda_bulk.cuh"
 #include "kda_internal.h"
@@ -204,19 +206,43 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                                                                    const __grid_constant__ CUtensorMap kmap,
                                                                    const __grid_constant__ CUtensorMap qmap,
                                                                    const __grid_constant__ CUtensorMap vmap,
-                                                                   const __grid_constant__ CUtensorMap gmap) {
+                                                                   const __grid_constant__ CUtensorMap gmap,
+                                                                   const int seg_lo, const int seg_len,
+                                                                   const int pdl_wait) {
     extern __shared__ unsigned char smem_raw[];
     PrepSmem &sm =
         *reinterpret_cast<PrepSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int32_t *plan = static_cast<const int32_t *>(p.workspace);
     const int n = p.num_seqs;
-    if (plan[n + 1] == 0) return;
-    const int32_t chunk = blockIdx.x;
-    if (chunk >= plan[n]) return;
+    // A segment launched behind the previous segment's chain (pdl_wait) may
+    // run beside it; one CTA waits for that chain to complete before it
+    // exits, so the next chain, an ordinary launch behind this grid, starts
+    // from the state the previous one wrote.
+    const bool waiter = pdl_wait && blockIdx.x == 0 && blockIdx.y == 0;
+    auto leave = [&]() {
+        if (waiter) asm volatile("griddepcontrol.wait;" ::: "memory");
+    };
+    if (plan[n + 1] == 0) return leave();
+    // the chunk: seg_len > 0 maps CTA x to local chunk seg_lo + x % seg_len
+    // of sequence x / seg_len; seg_len = 0 maps it to global chunk x, taken
+    // only from local chunk seg_lo on
+    int32_t chunk;
+    int s;
+    if (seg_len > 0) {
+        s = (int)(blockIdx.x / seg_len);
+        if (s >= n) return leave();
+        const int32_t local = seg_lo + (int32_t)(blockIdx.x % seg_len);
+        if (local >= plan[s + 1] - plan[s]) return leave();
+        chunk = plan[s] + local;
+    } else {
+        chunk = blockIdx.x;
+        if (chunk >= plan[n]) return leave();
+        s = find_seq(plan, n, chunk);
+        if (chunk - plan[s] < seg_lo) return leave();
+    }
     const int h = blockIdx.y, H = p.H;
-    const int s = find_seq(plan, n, chunk);
     const int slot = p.slot_ids[s];
-    if (slot < 0 || (int64_t)slot >= p.num_slots) return;  // the chain writes zeros
+    if (slot < 0 || (int64_t)slot >= p.num_slots) return leave();  // the chain writes zeros
     const int t0 = p.cu_seqlens[s] + (chunk - plan[s]) * C;
     const int L = p.cu_seqlens[s + 1] - t0 < C ? p.cu_seqlens[s + 1] - t0 : C;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -811,6 +837,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tm, PT_COLS);
+    leave();
 }
 
 // ================================================================== chain
@@ -885,7 +912,10 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar) {
 
 template <typename T>
 __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillParams p,
-                                                                  const __grid_constant__ CUtensorMap omap) {
+                                                                  const __grid_constant__ CUtensorMap omap,
+                                                                  const int seg_lo, const int seg_hi) {
+    // the next segment's prep kernel may start beside this grid
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ unsigned char smem_raw[];
     ChainSmem &sm =
         *reinterpret_cast<ChainSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -898,15 +928,21 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
     const int slot = p.slot_ids[s];
     T *out = static_cast<T *>(p.out);
     const int64_t tok_stride = (int64_t)H * D, hoff = (int64_t)h * D;
+    // this launch walks the sequence's local chunks [c_lo, c_hi); a later
+    // segment starts from the state the previous one wrote to the pool
+    const int nchunks_all = plan[s + 1] - plan[s];
+    const int c_lo = seg_lo, c_hi = seg_hi < nchunks_all ? seg_hi : nchunks_all;
+    if (seg_lo > 0 && c_lo >= c_hi) return;
+    const int nchunks = c_hi > c_lo ? c_hi - c_lo : 0;  // chunks of this launch; loop index i is c_lo + i
     if (slot < 0 || (int64_t)slot >= p.num_slots) {
-        for (int64_t t = cs + (tid >> 7); t < ce; t += kChainThreads / D)
+        const int64_t t_end = seg_hi < nchunks_all ? (int64_t)cs + (int64_t)c_hi * C : (int64_t)ce;
+        for (int64_t t = cs + (int64_t)c_lo * C + (tid >> 7); t < t_end; t += kChainThreads / D)
             Elem<T>::store1(out + t * tok_stride + hoff + (tid & 127), 0.f);
-        if (slot >= 0 && h == 0 && tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_SLOT);
+        if (slot >= 0 && seg_lo == 0 && h == 0 && tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_SLOT);
         return;
     }
-    const int nchunks = plan[s + 1] - plan[s];
     const unsigned char *ws = static_cast<const unsigned char *>(p.workspace) + plan_bytes(n);
-    auto image = [&](int ci) { return ws + ((size_t)(plan[s] + ci) * H + h) * (size_t)IMG_BYTES; };
+    auto image = [&](int ci) { return ws + ((size_t)(plan[s] + c_lo + ci) * H + h) * (size_t)IMG_BYTES; };
 
     if (warp == 0) tc::tmem_alloc(&sm.tmem_base, CT_COLS);
     if (tid == 0) {
@@ -1026,8 +1062,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
         Sg = p.pool + ((int64_t)slot * H + h) * (int64_t)D * D + (int64_t)lr * D + cq * 32;
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-            const float4 v4 = p.init_from_pool ? *reinterpret_cast<const float4 *>(Sg + e)
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 v4 = (p.init_from_pool || seg_lo > 0) ? *reinterpret_cast<const float4 *>(Sg + e)
+                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
             S[e] = v4.x; S[e + 1] = v4.y; S[e + 2] = v4.z; S[e + 3] = v4.w;
         }
         auto store_s16 = [&]() {
@@ -1048,7 +1084,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
         // written, thread 0 then issues the store and, once the previous
         // store has read its tile, arrives on that tile's tile_free.
         auto output = [&](int cj) {
-            const int64_t tj = (int64_t)cs + (int64_t)cj * C;
+            const int64_t tj = (int64_t)cs + (int64_t)(c_lo + cj) * C;
             const int Lj = (int)((int64_t)ce - tj < C ? (int64_t)ce - tj : C);
             float o[16];
             tc::ld16(taddr(CT_ACC + (cj & 1) * CT_ACC_STRIDE + 128 + cq * 16), o);
@@ -1068,7 +1104,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
                     if (tid == 0) {
                         stored = mbar_wait(&sm.tile_full, cj & 1);
                         if (stored) {
-                            tma_store_2d(&omap, h * D, cs + cj * C, sm.ot[t]);
+                            tma_store_2d(&omap, h * D, (int)tj, sm.ot[t]);
                             bulk_commit();
                             if (cj > 0) {
                                 bulk_wait_read_le1();
@@ -1091,7 +1127,12 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
         // snapshot requests of this sequence (the same for every thread)
         int snap_ptr = 0, snap_hi = 0;
         bool snap_bad = false;
-        if (p.num_snaps > 0) snap_range(p, s, snap_ptr, snap_hi);
+        if (p.num_snaps > 0) {
+            snap_range(p, s, snap_ptr, snap_hi);
+            // requests up to this segment's first chunk were an earlier launch's
+            if (seg_lo > 0)
+                while (snap_ptr < snap_hi && (int64_t)p.snap_tokens[snap_ptr] <= (int64_t)c_lo * C) ++snap_ptr;
+        }
         auto store_snapshot = [&](int sl) {
             float *dst = p.pool + ((int64_t)sl * H + h) * (int64_t)D * D + (int64_t)lr * D + cq * 32;
 #pragma unroll
@@ -1128,11 +1169,11 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
             if (!ok) break;
             // the state after c + 1 chunks, where a snapshot asks for it
             if (snap_ptr < snap_hi)
-                snap_ptr = snap_due(p, snap_ptr, snap_hi, min((int64_t)(c + 1) * C, (int64_t)ce - cs), C, snap_bad,
-                                    store_snapshot);
+                snap_ptr = snap_due(p, snap_ptr, snap_hi, min((int64_t)(c_lo + c + 1) * C, (int64_t)ce - cs), C,
+                                    snap_bad, store_snapshot);
         }
         // requests past the sequence's last whole chunk can never be met
-        if (ok && snap_ptr < snap_hi) snap_bad = true;
+        if (ok && snap_ptr < snap_hi && c_hi == nchunks_all) snap_bad = true;
         if (snap_bad && h == 0 && tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_SNAPSHOT);
         if (tid == 0) bulk_wait_all();  // every tensor store complete before shared memory goes
         const bool bad = !(__low2float(s16max) <= kHalfMax) || !(__high2float(s16max) <= kHalfMax);
@@ -1166,6 +1207,11 @@ size_t prefill_tc_workspace_bytes(int H, int32_t num_seqs, int64_t total_tokens)
     return plan_bytes(num_seqs) + (size_t)max_chunks(num_seqs, total_tokens) * (size_t)H * IMG_BYTES;
 }
 
+// Chunks per segment when a long prefill is pipelined (see launch_prefill_tc):
+// a prep CTA lives tens of microseconds, so a segment's prep grid must span
+// many waves for its tail to stay small; 128 chunks x 32 heads is about 13.
+constexpr int kSegChunks = 128;
+
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
     using namespace prefill_tc;
     cudaError_t e = cudaFuncSetAttribute(prep_tc_kernel<__nv_bfloat16>,
@@ -1175,10 +1221,11 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
                              (int)kChainSmem);
     if (e != cudaSuccess) return e;
     const int64_t mc = max_chunks(p.num_seqs, p.total_tokens);
-    if (mc > 0 && p.total_tokens > 0) {
-        // the token inputs as [total_tokens][H * 128] tensors, boxes of 64
-        // tokens x 64 channels (bf16) or 32 channels (g, fp32), 128B-swizzled
-        CUtensorMap kmap, qmap, vmap, gmap;
+    // the token inputs as [total_tokens][H * 128] tensors, boxes of 64
+    // tokens x 64 channels (bf16) or 32 channels (g, fp32), 128B-swizzled
+    CUtensorMap kmap, qmap, vmap, gmap;
+    const bool any = mc > 0 && p.total_tokens > 0;
+    if (any) {
         const cuuint64_t dims[2] = {(cuuint64_t)p.H * D, (cuuint64_t)p.total_tokens};
         const cuuint64_t sb[1] = {(cuuint64_t)p.H * D * 2}, sf[1] = {(cuuint64_t)p.H * D * 4};
         const cuuint32_t boxb[2] = {64, (cuuint32_t)C}, boxf[2] = {32, (cuuint32_t)C};
@@ -1195,24 +1242,65 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
                                    elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        prep_tc_kernel<__nv_bfloat16>
-            <<<dim3((unsigned)mc, (unsigned)p.H), kPrepThreads, kPrepSmem, st>>>(p, kmap, qmap, vmap, gmap);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
     }
     // the output tensor as [total_tokens][H * 128] bf16, boxes of 64 tokens x
     // one head's 128 values (the chain's full-chunk tensor stores)
     CUtensorMap omap;
-    const cuuint64_t dims[2] = {(cuuint64_t)p.H * D, (cuuint64_t)(p.total_tokens > 0 ? p.total_tokens : 1)};
-    const cuuint64_t strides[1] = {(cuuint64_t)p.H * D * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)C};
-    const cuuint32_t elem[2] = {1, 1};
-    const CUresult r = tensor_map_encode_fn()(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.out, dims, strides, box,
-                                              elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                                              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    chain_kernel<__nv_bfloat16><<<dim3((unsigned)p.num_seqs, (unsigned)p.H), kChainThreads, kChainSmem, st>>>(p, omap);
-    return cudaGetLastError();
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)p.H * D, (cuuint64_t)(p.total_tokens > 0 ? p.total_tokens : 1)};
+        const cuuint64_t strides[1] = {(cuuint64_t)p.H * D * 2};
+        const cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)C};
+        const cuuint32_t elem[2] = {1, 1};
+        const CUresult r = tensor_map_encode_fn()(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.out, dims, strides,
+                                                  box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    // Pipelining: when few (sequence, head) chains would walk many chunks
+    // each, the chunks are cut into segments of kSegChunks local chunks.
+    // Segment k's prep runs beside segment k - 1's chain (programmatic
+    // dependent launch: the chain lets it start at once; one of its CTAs
+    // waits for that chain before the grid ends), and segment k's chain, an
+    // ordinary launch, follows its prep and so the previous chain.  The last
+    // segment takes every remaining chunk.  Only the last chain is exposed.
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+        sms = 1;
+    int nseg = 1;
+    if (any && p.num_seqs > 0 && (int64_t)p.num_seqs * p.H <= (int64_t)sms) {
+        const int64_t per_seq = (p.total_tokens + C - 1) / C / p.num_seqs;  // mean chunks per sequence
+        const int64_t k = per_seq / kSegChunks;
+        nseg = k < 2 ? 1 : (k > 128 ? 128 : (int)k);
+    }
+    const dim3 cgrid((unsigned)p.num_seqs, (unsigned)p.H);
+    for (int k = 0; k < nseg; ++k) {
+        const bool last = k == nseg - 1;
+        const int lo = k * kSegChunks;
+        if (any) {
+            const int seg_len = last ? 0 : kSegChunks;
+            const int64_t gx = last ? mc : (int64_t)p.num_seqs * kSegChunks;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)gx, (unsigned)p.H);
+            cfg.blockDim = dim3(kPrepThreads);
+            cfg.dynamicSmemBytes = kPrepSmem;
+            cfg.stream = st;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = k > 0 ? 1 : 0;
+            const PrefillParams pp = p;
+            e = cudaLaunchKernelEx(&cfg, prep_tc_kernel<__nv_bfloat16>, pp, kmap, qmap, vmap, gmap, lo, seg_len,
+                                   k > 0 ? 1 : 0);
+            if (e != cudaSuccess) return e;
+        }
+        chain_kernel<__nv_bfloat16><<<cgrid, kChainThreads, kChainSmem, st>>>(p, omap, lo,
+                                                                             last ? INT_MAX : lo + kSegChunks);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace kda
