@@ -1207,10 +1207,12 @@ size_t prefill_tc_workspace_bytes(int H, int32_t num_seqs, int64_t total_tokens)
     return plan_bytes(num_seqs) + (size_t)max_chunks(num_seqs, total_tokens) * (size_t)H * IMG_BYTES;
 }
 
-// Chunks per segment when a long prefill is pipelined (see launch_prefill_tc):
-// a prep CTA lives tens of microseconds, so a segment's prep grid must span
-// many waves for its tail to stay small; 128 chunks x 32 heads is about 13.
-constexpr int kSegChunks = 128;
+// Segments of a pipelined prefill (see launch_prefill_tc): a prep CTA lives
+// tens of microseconds, so a segment's prep grid must span several waves
+// (at least kSegMinCtas CTAs) for its tail to stay small, and a segment holds
+// at least kSegMinChunks chunks of each sequence.
+constexpr int kSegMinCtas = 2048;
+constexpr int kSegMinChunks = 64;
 
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
     using namespace prefill_tc;
@@ -1257,7 +1259,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
     // Pipelining: when few (sequence, head) chains would walk many chunks
-    // each, the chunks are cut into segments of kSegChunks local chunks.
+    // each, the chunks are cut into segments of seg_chunks local chunks.
     // Segment k's prep runs beside segment k - 1's chain (programmatic
     // dependent launch: the chain lets it start at once; one of its CTAs
     // waits for that chain before the grid ends), and segment k's chain, an
@@ -1267,19 +1269,30 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                   cudaSuccess)
         sms = 1;
-    int nseg = 1;
+    int nseg = 1, seg_chunks = 0;
     if (any && p.num_seqs > 0 && (int64_t)p.num_seqs * p.H <= (int64_t)sms) {
         const int64_t per_seq = (p.total_tokens + C - 1) / C / p.num_seqs;  // mean chunks per sequence
-        const int64_t k = per_seq / kSegChunks;
-        nseg = k < 2 ? 1 : (k > 128 ? 128 : (int)k);
+        // about sqrt(per_seq / 10) segments balance the exposed last chain
+        // (per_seq / K chunks at ~1.7 us) against the K prep tails (~17 us)
+        int64_t kopt = 1;
+        while ((kopt + 1) * (kopt + 1) * 10 <= per_seq) ++kopt;
+        const int64_t ctas_per_chunk = (int64_t)p.num_seqs * p.H;
+        int64_t len = (kSegMinCtas + ctas_per_chunk - 1) / ctas_per_chunk;
+        if (len < kSegMinChunks) len = kSegMinChunks;
+        if (len < (per_seq + kopt - 1) / kopt) len = (per_seq + kopt - 1) / kopt;
+        const int64_t k = per_seq / len;
+        if (k >= 2) {
+            nseg = k > 256 ? 256 : (int)k;
+            seg_chunks = (int)len;
+        }
     }
     const dim3 cgrid((unsigned)p.num_seqs, (unsigned)p.H);
     for (int k = 0; k < nseg; ++k) {
         const bool last = k == nseg - 1;
-        const int lo = k * kSegChunks;
+        const int lo = k * seg_chunks;
         if (any) {
-            const int seg_len = last ? 0 : kSegChunks;
-            const int64_t gx = last ? mc : (int64_t)p.num_seqs * kSegChunks;
+            const int seg_len = last ? 0 : seg_chunks;
+            const int64_t gx = last ? mc : (int64_t)p.num_seqs * seg_chunks;
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)gx, (unsigned)p.H);
             cfg.blockDim = dim3(kPrepThreads);
@@ -1296,7 +1309,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
             if (e != cudaSuccess) return e;
         }
         chain_kernel<__nv_bfloat16><<<cgrid, kChainThreads, kChainSmem, st>>>(p, omap, lo,
-                                                                             last ? INT_MAX : lo + kSegChunks);
+                                                                             last ? INT_MAX : lo + seg_chunks);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

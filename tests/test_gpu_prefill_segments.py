@@ -1,9 +1,11 @@
 """GPU parity of the pipelined tensor-core prefill: when a few (sequence,
-head) chains each walk many chunks, the chunks are cut into segments of 128
-and segment k's prep runs beside segment k - 1's chain.  These batches are
-long enough per sequence to take that path (2 and 3 segments); outputs, final
-states and snapshots on both sides of a segment boundary are compared with
-the fp64 oracle."""
+head) chains each walk many chunks, the chunks are cut into segments and
+segment k's prep runs beside segment k - 1's chain.  The library takes about
+sqrt(mean chunks per sequence / 10) segments, each of at least 64 chunks and
+at least 2048 prep CTAs, when (sequences x heads) is at most the SM count.
+These batches take that path (4 and 3 segments); outputs, final states and
+snapshots on both sides of segment boundaries are compared with the fp64
+oracle."""
 import pytest
 import torch
 
@@ -13,7 +15,7 @@ from kda_testutil import assert_close, err_flag, round_to, to_np64, tol_for
 
 pytestmark = pytest.mark.gpu
 
-SEG_TOKENS = 128 * 64
+
 
 
 def _kda():
@@ -52,23 +54,27 @@ def _run(lens, slots, H, reqs, num_slots, seed):
     return x, pool, out
 
 
-def test_two_segments_mixed_batch():
+def test_four_segments_mixed_batch():
     """Five sequences (60000, 26000, 100, 0 and 300 tokens; the third is
-    padding) x 2 heads: 1350 chunks, 270 per sequence on average, so two
-    segments; the short sequences lie in the first only.  Snapshots at the
-    segment boundary (8192 tokens), one chunk past it and deep in the second."""
+    padding) x 8 heads: 1350 chunks, 270 per sequence on average, so four
+    segments of 64 chunks (the last takes the rest); the short sequences lie
+    in the first only.  Snapshots at a segment boundary (4096 tokens), one
+    chunk past it and deep in the last segment."""
+    seg = 64 * 64
     lens = [60000, 26000, 100, 0, 300]
     slots = [0, 1, -1, 2, 3]
-    reqs = [(0, SEG_TOKENS, 4), (0, SEG_TOKENS + 64, 5), (1, 25600, 6), (4, 256, 7)]
-    x, pool, out = _run(lens, slots, 2, reqs, num_slots=9, seed=41)
+    reqs = [(0, seg, 4), (0, seg + 64, 5), (1, 25600, 6), (4, 256, 7)]
+    x, pool, out = _run(lens, slots, 8, reqs, num_slots=9, seed=41)
     cu = x.cu_seqlens.tolist()
     assert torch.all(out[cu[2]:cu[3]] == 0)          # padding sequence: zero outputs
     assert torch.equal(pool[8].cpu(), x.pool[8])     # a slot nobody names keeps its bits
 
 
 def test_three_segments_one_sequence():
-    """One sequence of 3 x 8192 + 337 tokens, one head: three segments, the
-    last with a partial chunk; snapshots at both segment boundaries."""
-    T = 3 * SEG_TOKENS + 337
-    reqs = [(0, SEG_TOKENS, 1), (0, 2 * SEG_TOKENS, 2), (0, 3 * SEG_TOKENS, 3)]
-    _run([T], [0], 1, reqs, num_slots=4, seed=42)
+    """One sequence of 3 x 8192 + 337 tokens x 16 heads: three segments of
+    128 chunks, the last with a partial chunk; snapshots at both segment
+    boundaries and at the last whole chunk."""
+    seg = 128 * 64
+    T = 3 * seg + 337
+    reqs = [(0, seg, 1), (0, 2 * seg, 2), (0, 3 * seg + 320, 3)]
+    _run([T], [0], 16, reqs, num_slots=4, seed=42)
