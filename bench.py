@@ -735,6 +735,17 @@ def run_ncu_case(name, steps, kda):
         for i in range(steps):
             out, rec = kda.verify_record(x.q, x.k, x.v, x.g, x.b, x.slot_ids, x.pool, out, rec)
             kda.replay_commit(rec, x.num_accepted, x.slot_ids, x.pool)
+    elif name == "fused_small":
+        # the fused decode at 256 x 32 heads over a 512-slot pool, two
+        # disjoint slot sets alternating (512 MiB of state per launch)
+        x = inputs.decode_inputs(256, 32, 128, 128, dtype="bf16", num_slots=512, seed=0,
+                                 device="cuda")
+        ex = inputs.fused_extras(256, 32, 128, 128, dtype="bf16", num_slots=512, seed=0, device="cuda")
+        sets = [x.slot_ids, torch.arange(512, dtype=torch.int32, device="cuda")[
+            ~torch.isin(torch.arange(512, device="cuda"), x.slot_ids.long())].contiguous()]
+        for i in range(steps):
+            kda.decode_fused(x.q, x.k, x.v, x.g, x.b, ex.z, sets[i % 2], x.pool, ex.conv_state,
+                             ex.conv_w, ex.norm_w)
     elif name == "prefill_small":
         x = inputs.prefill_inputs([8192], 32, 128, 128, dtype="bf16", seed=0, device="cuda")
         for i in range(steps):
@@ -757,7 +768,7 @@ def main(argv=None):
     ap.add_argument("--paths", default="decode,spec,fused,prefill,longmix")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ncu-case", default=None,
-                    help="run one small profiling case (decode_small, spec_small, prefill_small)")
+                    help="run one small profiling case (decode_small, spec_small, fused_small, prefill_small)")
     args = ap.parse_args(argv)
     if args.ncu_case:
         from gated_delta_rule_decode_gb300 import kda

@@ -41,8 +41,15 @@ __device__ __forceinline__ uint32_t cluster_rank() {
     return r;
 }
 
+// Arrive with release semantics: this thread's earlier memory accesses are
+// performed first (cheap while no global stores are outstanding).
 __device__ __forceinline__ void cluster_arrive() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+// Arrive without ordering memory: execution order only.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_wait() {
@@ -161,7 +168,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 3)
         const float c = row_update<DK, true>(s[rr], tc, xc[2 * DK + lrow], &u);
         o[rr] = row_output(c, u, tc.kq, p.scale);
         ss = __fmaf_rn(o[rr], o[rr], ss);
-        store_row<DK>(S + (int64_t)lrow * DK, l, s[rr]);
     }
 
     // sum of o_i^2: the 4 groups of a warp, the 4 warps in order, then the
@@ -176,7 +182,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 3)
         for (int w = 1; w < kFusedWarps; ++w) t = __fadd_rn(t, red[w]);
         part = t;
     }
-    cluster_arrive();  // publishes `part`; every read of the old conv state is done
+    // publishes `part` (its release is cheap: the state stores come after
+    // it); every read of the old conv state has been consumed
+    cluster_arrive();
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) store_row<DK>(S + (int64_t)(lrow0 + rr * kFusedGroups) * DK, l, s[rr]);
     cluster_wait();
 
     // shift the conv state: CTA 0 writes the q channels, CTA 1 the k
@@ -194,8 +204,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 3)
 
     const float p0 = rank == 0 ? part : ld_peer_f32(&part, 0);
     const float p1 = rank == 1 ? part : ld_peer_f32(&part, 1);
-    cluster_arrive();  // the peer's `part` has been read: it may exit after the wait
     const float inv = rsqrtf(__fadd_rn(__fmul_rn(__fadd_rn(p0, p1), 1.0f / DV), p.eps_o));
+    // the peer's `part` has been read (inv depends on it): the peer may exit
+    // once it has seen this arrival
+    cluster_arrive_relaxed();
 
     if (l < R) {
         // lane l of the group writes its row rr = l (R <= 8 lanes)
