@@ -22,6 +22,7 @@
 // in the same order, so the state equals what kda_decode produces from the
 // same convolved inputs held in fp32.
 #include "kda.h"
+#include "kda_bulk.cuh"
 #include "kda_internal.h"
 #include "kda_rowmath.cuh"
 
@@ -41,12 +42,6 @@ __device__ __forceinline__ uint32_t cluster_rank() {
     return r;
 }
 
-// Arrive with release semantics: this thread's earlier memory accesses are
-// performed first (cheap while no global stores are outstanding).
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-
 // Arrive without ordering memory: execution order only.
 __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
@@ -56,21 +51,33 @@ __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Reads a float at the same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ float ld_peer_f32(const float *p, uint32_t rank) {
+// The shared::cluster address of `p`'s counterpart in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t rank) {
     const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
     uint32_t pa;
-    float v;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(pa) : "r"(a), "r"(rank));
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(pa) : "memory");
-    return v;
+    return pa;
+}
+
+// Writes `v` into CTA `rank`'s copy of `dst` and completes 4 bytes of the
+// transaction count of that CTA's copy of `bar`.
+__device__ __forceinline__ void st_async_peer(float *dst, uint64_t *bar, float v, uint32_t rank) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                     peer_addr(dst, rank)),
+                 "r"(__float_as_uint(v)), "r"(peer_addr(bar, rank))
+                 : "memory");
 }
 
 // A cluster of two CTAs owns one (sequence, head): CTA r of the pair holds
 // value rows [r dv/2, (r+1) dv/2), the same 64-row grain per CTA as kda_decode.
 // Both CTAs convolve all q and k channels (each needs the whole k^ and q^)
-// and their own half of the v channels; the RMS norm's sum of squares is
-// exchanged through distributed shared memory.
+// and their own half of the v channels.  The RMS norm's sum of squares is
+// exchanged through distributed shared memory: each CTA stores its partial
+// sum into the other's `peer_part` with st.async, which completes the
+// other's `xbar`.  A CTA writes its conv-state channels only after it has
+// received the other's partial, which the other sent after its reads of the
+// old conv state; and it exits only after that receipt, so neither CTA's
+// shared memory is written after it has gone.
 template <int DK, typename T, int R>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 3)
     decode_fused_kernel(const DecodeFusedParams p) {
@@ -81,7 +88,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 3)
     constexpr int PER = (NL + kFusedThreads - 1) / kFusedThreads;
     __shared__ __align__(16) float xc[NL];  // q~ | k~ | this CTA's v~ rows
     __shared__ float red[kFusedWarps];
-    __shared__ float part;                  // this CTA's sum of o_i^2
+    __shared__ float peer_part;             // the other CTA's sum of o_i^2
+    __shared__ __align__(8) uint64_t xbar;  // peer_part received
 
     const uint32_t rank = cluster_rank();
     const int64_t sh = blockIdx.x >> 1;  // (sequence, head) flattened = token index
@@ -115,6 +123,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 3)
     const int orow_l = lrow0 + (l < R ? l : 0) * kFusedGroups;  // the row lane l < R writes
     const float zraw = Elem<T>::load1(static_cast<const T *>(p.z) + sh * DV + vbase + orow_l);
     const float nw = __ldg(p.norm_w + vbase + orow_l);
+
+    // the exchange barrier, initialised before the other CTA can send to it
+    // (the cluster wait below comes before this CTA's own send)
+    if (tid == 0) {
+        mbar_init(&xbar, 1);
+        fence_barrier_init();
+        mbar_arrive_expect_tx(&xbar, 4);
+    }
+    cluster_arrive_relaxed();
 
     T *cs = static_cast<T *>(p.conv_state) + ((int64_t)slot * p.H + h) * (3 * NC);
     const float4 *cw = reinterpret_cast<const float4 *>(p.conv_w) + (int64_t)h * NC;
@@ -176,18 +193,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 3)
     ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, 16));
     if (lane == 0) red[warp] = ss;
     __syncthreads();
-    if (tid == 0) {
-        float t = red[0];
+    float mine = red[0];
 #pragma unroll
-        for (int w = 1; w < kFusedWarps; ++w) t = __fadd_rn(t, red[w]);
-        part = t;
-    }
-    // publishes `part` (its release is cheap: the state stores come after
-    // it); every read of the old conv state has been consumed
-    cluster_arrive();
+    for (int w = 1; w < kFusedWarps; ++w) mine = __fadd_rn(mine, red[w]);
+    cluster_wait();  // the other CTA's exchange barrier is initialised
+    // every read of the old conv state has been consumed (the partial sum
+    // depends on it) when the partial leaves
+    if (tid == 0) st_async_peer(&peer_part, &xbar, mine, rank ^ 1u);
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) store_row<DK>(S + (int64_t)(lrow0 + rr * kFusedGroups) * DK, l, s[rr]);
-    cluster_wait();
+    // the other CTA's partial (thread 0 polls, bounded)
+    const bool got = __syncthreads_and(tid == 0 ? mbar_wait(&xbar, 0) : true) != 0;
+    if (got) {
+        mbar_try_wait(&xbar, 0);
+    } else if (tid == 0) {
+        if (p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
+        mbar_wait_drain(&xbar, 0);  // its write must land before this CTA's memory is released
+    }
+    const float theirs = got ? peer_part : 0.f;
 
     // shift the conv state: CTA 0 writes the q channels, CTA 1 the k
     // channels, each its own v channels
@@ -202,12 +225,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 3)
         }
     }
 
-    const float p0 = rank == 0 ? part : ld_peer_f32(&part, 0);
-    const float p1 = rank == 1 ? part : ld_peer_f32(&part, 1);
+    // rank 0's half first on both CTAs: the same bits
+    const float p0 = rank == 0 ? mine : theirs, p1 = rank == 0 ? theirs : mine;
     const float inv = rsqrtf(__fadd_rn(__fmul_rn(__fadd_rn(p0, p1), 1.0f / DV), p.eps_o));
-    // the peer's `part` has been read (inv depends on it): the peer may exit
-    // once it has seen this arrival
-    cluster_arrive_relaxed();
 
     if (l < R) {
         // lane l of the group writes its row rr = l (R <= 8 lanes)
@@ -217,7 +237,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 3)
         const float y = __fmul_rn(__fmul_rn(__fmul_rn(ol, inv), nw), sigmoid_f(zraw));
         Elem<T>::store1(orow + orow_l, y);
     }
-    cluster_wait();
 }
 
 template <int DK, typename T>
