@@ -1280,7 +1280,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
         int64_t len = (kSegMinCtas + ctas_per_chunk - 1) / ctas_per_chunk;
         if (len < kSegMinChunks) len = kSegMinChunks;
         if (len < (per_seq + kopt - 1) / kopt) len = (per_seq + kopt - 1) / kopt;
-        const int64_t k = per_seq / len;
+        const int64_t k = (per_seq + len - 1) / len;
         if (k >= 2) {
             nseg = k > 256 ? 256 : (int)k;
             seg_chunks = (int)len;

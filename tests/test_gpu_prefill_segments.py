@@ -1,11 +1,12 @@
 """GPU parity of the pipelined tensor-core prefill: when a few (sequence,
 head) chains each walk many chunks, the chunks are cut into segments and
 segment k's prep runs beside segment k - 1's chain.  The library takes about
-sqrt(mean chunks per sequence / 10) segments, each of at least 64 chunks and
-at least 2048 prep CTAs, when (sequences x heads) is at most the SM count.
-These batches take that path (4 and 3 segments); outputs, final states and
-snapshots on both sides of segment boundaries are compared with the fp64
-oracle."""
+sqrt(mean chunks per sequence / 10) segments (rounded up after the length
+is fixed), each of at least 64 chunks and at least 2048 prep CTAs, when
+(sequences x heads) is at most the SM count; the last segment takes the
+rest.  These batches take that path (5 and 4 segments); outputs, final
+states and snapshots on both sides of segment boundaries are compared with
+the fp64 oracle."""
 import pytest
 import torch
 
@@ -54,9 +55,9 @@ def _run(lens, slots, H, reqs, num_slots, seed):
     return x, pool, out
 
 
-def test_four_segments_mixed_batch():
+def test_five_segments_mixed_batch():
     """Five sequences (60000, 26000, 100, 0 and 300 tokens; the third is
-    padding) x 8 heads: 1350 chunks, 270 per sequence on average, so four
+    padding) x 8 heads: 1350 chunks, 270 per sequence on average, so five
     segments of 64 chunks (the last takes the rest); the short sequences lie
     in the first only.  Snapshots at a segment boundary (4096 tokens), one
     chunk past it and deep in the last segment."""
@@ -70,10 +71,10 @@ def test_four_segments_mixed_batch():
     assert torch.equal(pool[8].cpu(), x.pool[8])     # a slot nobody names keeps its bits
 
 
-def test_three_segments_one_sequence():
-    """One sequence of 3 x 8192 + 337 tokens x 16 heads: three segments of
-    128 chunks, the last with a partial chunk; snapshots at both segment
-    boundaries and at the last whole chunk."""
+def test_four_segments_one_sequence():
+    """One sequence of 3 x 8192 + 337 tokens x 16 heads (390 chunks): three
+    segments of 128 chunks and a last one of 6 ending in a partial chunk;
+    snapshots at two segment boundaries and at the last whole chunk."""
     seg = 128 * 64
     T = 3 * seg + 337
     reqs = [(0, seg, 1), (0, 2 * seg, 2), (0, 3 * seg + 320, 3)]
