@@ -1212,6 +1212,9 @@ size_t prefill_tc_workspace_bytes(int H, int32_t num_seqs, int64_t total_tokens)
 // (at least kSegMinCtas CTAs) for its tail to stay small, and a segment holds
 // at least kSegMinChunks chunks of each sequence.
 constexpr int kSegMinCtas = 2048;
+#ifndef KDA_SEG_FIRST_PCT
+#define KDA_SEG_FIRST_PCT 72
+#endif
 constexpr int kSegMinChunks = 64;
 
 cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
@@ -1286,13 +1289,25 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
             seg_chunks = (int)len;
         }
     }
+    // With two segments the first is made larger (KDA_SEG_FIRST_PCT percent
+    // of the mean chunks per sequence): the second prep then runs on the SMs
+    // the first chain leaves free for about as long as that chain, and the
+    // exposed second chain is shorter.  72 % measured best at 8192 tokens x 32
+    // heads (507 us, against 550 us for halves and 521 us for 66 % or 78 %).
+    int first_len = seg_chunks;
+    if (nseg == 2) {
+        const int64_t per_seq = (p.total_tokens + C - 1) / C / p.num_seqs;
+        const int64_t f = per_seq * KDA_SEG_FIRST_PCT / 100;
+        if (f > first_len && f < per_seq) first_len = (int)f;
+    }
     const dim3 cgrid((unsigned)p.num_seqs, (unsigned)p.H);
     for (int k = 0; k < nseg; ++k) {
         const bool last = k == nseg - 1;
-        const int lo = k * seg_chunks;
+        const int lo = k == 0 ? 0 : first_len + (k - 1) * seg_chunks;
+        const int len = k == 0 ? first_len : seg_chunks;
         if (any) {
-            const int seg_len = last ? 0 : seg_chunks;
-            const int64_t gx = last ? mc : (int64_t)p.num_seqs * seg_chunks;
+            const int seg_len = last ? 0 : len;
+            const int64_t gx = last ? mc : (int64_t)p.num_seqs * len;
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)gx, (unsigned)p.H);
             cfg.blockDim = dim3(kPrepThreads);
@@ -1309,7 +1324,7 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
             if (e != cudaSuccess) return e;
         }
         chain_kernel<__nv_bfloat16><<<cgrid, kChainThreads, kChainSmem, st>>>(p, omap, lo,
-                                                                             last ? INT_MAX : lo + seg_chunks);
+                                                                             last ? INT_MAX : lo + len);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

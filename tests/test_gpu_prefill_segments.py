@@ -79,3 +79,11 @@ def test_four_segments_one_sequence():
     T = 3 * seg + 337
     reqs = [(0, seg, 1), (0, 2 * seg, 2), (0, 3 * seg + 320, 3)]
     _run([T], [0], 16, reqs, num_slots=4, seed=42)
+
+
+def test_two_uneven_segments_one_sequence():
+    """One sequence of 8172 tokens x 32 heads (128 chunks, the last partial):
+    two segments, the first holding 72 % of the chunks (92).  Snapshots at
+    the boundary, one chunk past it and at the last whole chunk."""
+    reqs = [(0, 92 * 64, 1), (0, 93 * 64, 2), (0, 127 * 64, 3)]
+    _run([8172], [0], 32, reqs, num_slots=4, seed=43)
