@@ -20,12 +20,17 @@ with the KDA recurrence.  The page gives no formulas; the readings taken:
 
 The projections are not part of it (they need trained weights): the conv
 weights, w_o and z are inputs.  The recurrence itself is the C oracle's.
+
+For a prefill the same ShortConv runs along each sequence: the history of
+its first token is the slot's conv state when the prefill starts from the
+pool, else zero, and the slot's conv state afterwards holds the last three
+raw inputs of that history followed by the sequence.
 """
 from __future__ import annotations
 
 import numpy as np
 
-from . import _f64, _i32, decode as _decode
+from . import _f64, _i32, decode as _decode, prefill as _prefill
 
 CONV_WIDTH = 4
 
@@ -95,4 +100,43 @@ def decode_fused(q, k, v, g, b, z, wq, wk, wv, w_o, slot_ids, pool, conv_pool,
         sl = int(slots[n])
         if sl < 0 or sl >= cpool.shape[0]:
             out[n] = 0.0
+    return out, P, cpool, err
+
+
+def prefill_fused(q, k, v, g, b, z, wq, wk, wv, w_o, cu_seqlens, slot_ids, pool, conv_pool,
+                  init_from_pool=False, eps: float = 1e-6, eps_o: float = 1e-6, scale=None):
+    """Fused prefill of a variable-length batch.
+
+    q, k, g: [T, H, dk]; v, z: [T, H, dv]; b: [T, H]; cu_seqlens: [n+1];
+    conv_pool: [S, H, 3, 2 dk + dv].  Returns (out [T, H, dv], new pool,
+    new conv_pool, errors).  Padding and out-of-range sequences output zero
+    and leave both pools alone.
+    """
+    q, k, v, g, b, z = (_f64(t) for t in (q, k, v, g, b, z))
+    wq, wk, wv, w_o = (_f64(t) for t in (wq, wk, wv, w_o))
+    cu = [int(x) for x in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist") else cu_seqlens)]
+    slots = _i32(slot_ids)
+    cpool = _f64(conv_pool).copy()
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    qc, kc, vc = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for s in range(len(cu) - 1):
+        sl = int(slots[s])
+        if sl < 0 or sl >= cpool.shape[0]:
+            continue
+        for h in range(H):
+            hist = cpool[sl, h].copy() if init_from_pool else np.zeros((3, 2 * dk + dv))
+            for t in range(cu[s], cu[s + 1]):
+                qc[t, h], hq = short_conv_step(hist[:, :dk], q[t, h], wq[h])
+                kc[t, h], hk = short_conv_step(hist[:, dk:2 * dk], k[t, h], wk[h])
+                vc[t, h], hv = short_conv_step(hist[:, 2 * dk:], v[t, h], wv[h])
+                hist = np.concatenate([hq, hk, hv], axis=1)
+            cpool[sl, h] = hist
+    o, P, err = _prefill(qc, kc, vc, g, b, cu, slots, pool, init_from_pool=init_from_pool,
+                         eps=eps, scale=scale)
+    out = rms_norm_gate(o, z, w_o, eps_o)
+    for s in range(len(cu) - 1):
+        sl = int(slots[s])
+        if sl < 0 or sl >= cpool.shape[0]:
+            out[cu[s]:cu[s + 1]] = 0.0
     return out, P, cpool, err

@@ -117,3 +117,66 @@ def test_decode_fused_matches_brute_force():
     # slot 1 is named by nobody: both pools keep it
     np.testing.assert_array_equal(P[1], pool[1])
     np.testing.assert_array_equal(C[1], cpool[1])
+
+
+def test_prefill_fused_equals_sequential_fused_decodes():
+    """A fused prefill of a sequence equals its tokens fed one by one to the
+    fused decode (the conv history carried through the conv state, the KDA
+    state through the pool): outputs, final state and final conv state.
+    Sequences of 5, 2 (shorter than the conv history), 0 and 4 tokens, one
+    of them padding; the prefill starts from the pools."""
+    rng = np.random.default_rng(7)
+    H, dk, dv, S = 2, 4, 3, 5
+    lens = [5, 2, 0, 4]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T = int(cu[-1])
+    q, k = rng.standard_normal((T, H, dk)), rng.standard_normal((T, H, dk))
+    v, z = rng.standard_normal((T, H, dv)), rng.standard_normal((T, H, dv))
+    g = -np.abs(rng.standard_normal((T, H, dk))) * 0.3
+    b = rng.standard_normal((T, H))
+    wq, wk = rng.standard_normal((H, dk, 4)), rng.standard_normal((H, dk, 4))
+    wv, wo = rng.standard_normal((H, dv, 4)), rng.standard_normal(dv)
+    pool = rng.standard_normal((S, H, dv, dk)) * 0.3
+    cpool = rng.standard_normal((S, H, 3, 2 * dk + dv))
+    slots = np.array([3, 0, 4, -1], dtype=np.int32)
+    out, P, C, err = megakda.prefill_fused(q, k, v, g, b, z, wq, wk, wv, wo, cu, slots, pool, cpool,
+                                           init_from_pool=True, eps_o=1e-5)
+    assert err == 0
+    P2, C2 = pool.copy(), cpool.copy()
+    for s, L in enumerate(lens):
+        for t in range(cu[s], cu[s] + L):
+            sel = lambda a: a[t:t + 1]  # noqa: E731
+            o1, P2, C2, e = megakda.decode_fused(sel(q), sel(k), sel(v), sel(g), sel(b), sel(z),
+                                                 wq, wk, wv, wo, slots[s:s + 1], P2, C2, eps_o=1e-5)
+            np.testing.assert_allclose(out[t], o1[0], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(P, P2, rtol=1e-10, atol=1e-12)
+    np.testing.assert_array_equal(C, C2)
+    assert np.all(out[cu[3]:cu[4]] == 0)
+
+
+def test_prefill_fused_from_zero_history():
+    """Without init_from_pool the conv history and the state start at zero:
+    the first token's conv output is silu(w3 x) and the new conv state of a
+    two-token sequence is [0, x0, x1]."""
+    rng = np.random.default_rng(8)
+    H, dk, dv = 1, 4, 3
+    q, k = rng.standard_normal((2, H, dk)), rng.standard_normal((2, H, dk))
+    v, z = rng.standard_normal((2, H, dv)), rng.standard_normal((2, H, dv))
+    g = -np.abs(rng.standard_normal((2, H, dk)))
+    b = rng.standard_normal((2, H))
+    wq, wk = rng.standard_normal((H, dk, 4)), rng.standard_normal((H, dk, 4))
+    wv, wo = rng.standard_normal((H, dv, 4)), np.ones(dv)
+    cpool = rng.standard_normal((1, H, 3, 2 * dk + dv))
+    out, P, C, err = megakda.prefill_fused(q, k, v, g, b, z, wq, wk, wv, wo, [0, 2],
+                                           np.array([0], np.int32), np.zeros((1, H, dv, dk)), cpool)
+    raw = np.concatenate([q[:, 0], k[:, 0], v[:, 0]], axis=1)
+    np.testing.assert_array_equal(C[0, 0], np.stack([np.zeros(2 * dk + dv), raw[0], raw[1]]))
+    # token 0 alone: the zero state makes o = scale beta (k^.q^) v~ with the
+    # convolved inputs silu(w3 x)
+    qc = megakda.silu(wq[0, :, 3] * q[0, 0])
+    kc = megakda.silu(wk[0, :, 3] * k[0, 0])
+    vc = megakda.silu(wv[0, :, 3] * v[0, 0])
+    qh = qc / np.sqrt(qc @ qc + 1e-6)
+    kh = kc / np.sqrt(kc @ kc + 1e-6)
+    o = dk ** -0.5 * (1 / (1 + np.exp(-b[0, 0]))) * (kh @ qh) * vc
+    np.testing.assert_allclose(out[0, 0], megakda.rms_norm_gate(o, z[0, 0], wo, 1e-6), rtol=1e-12)
