@@ -546,6 +546,28 @@ def run_prefill(kda, peaks, T=8192, H=32, steps=10, key="prefill_t8192_h32_d128_
             "algorithmic_flop": flops, "with_snapshots": snap}
 
 
+def run_prefill_fused(kda, peaks, T=8192, H=32, steps=10):
+    """The fused ShortConv + prefill + gated RMS norm at the prefill
+    workload's size, beside the plain prefill's figure."""
+    x = inputs.prefill_inputs([T], H, 128, 128, dtype="bf16", seed=0, device="cuda")
+    ex = inputs.fused_prefill_extras(T, 1, H, 128, 128, dtype="bf16", seed=0, device="cuda")
+    out = torch.empty((T, H, 128), dtype=torch.bfloat16, device="cuda")
+    ws_bytes = kda.prefill_workspace_bytes(H, 128, 128, kda.KDA_DT_BF16, 1, T)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+    try:
+        call = kda.prefill_fused(x.q, x.k, x.v, x.g, x.b, ex.z, x.cu_seqlens, x.slot_ids, x.pool,
+                                 ex.conv_state, ex.conv_w, ex.norm_w, out, workspace=ws, _prepare=True)
+        t = time_launches(lambda i: call(), steps, warmup=2) / 1e6
+    except kda.KdaError as e:
+        return {"workload": "prefill_fused_t8192_h32_d128_bf16", "unavailable": str(e)}
+    # the plain prefill's bytes plus z (dv x 2 per token-head) and the conv
+    # state read and written (2 x 3 x 384 x 2 per head)
+    bytes_ = T * H * (PREFILL_BYTES_PER_TH + 128 * 2) + H * 128 * 128 * 4 + H * 2 * 3 * 384 * 2
+    return {"workload": "prefill_fused_t8192_h32_d128_bf16", "us": round(t * 1e6, 1),
+            "tokens_per_s": round(T / t, 1), "GB/s": round(bytes_ / t / 1e9, 1),
+            "frac_hbm": round(bytes_ / t / 1e9 / peaks["hbm_gbs"], 4), "algorithmic_bytes": bytes_}
+
+
 def run_longmix(kda, peaks):
     res = {"workload": "longmix_prefill_t102400_h32_decode256_b1024_h64_pool16384"}
     T, H = 102400, 32
@@ -746,6 +768,12 @@ def run_ncu_case(name, steps, kda):
         for i in range(steps):
             kda.decode_fused(x.q, x.k, x.v, x.g, x.b, ex.z, sets[i % 2], x.pool, ex.conv_state,
                              ex.conv_w, ex.norm_w)
+    elif name == "prefill_fused_small":
+        x = inputs.prefill_inputs([8192], 32, 128, 128, dtype="bf16", seed=0, device="cuda")
+        ex = inputs.fused_prefill_extras(8192, 1, 32, 128, 128, dtype="bf16", seed=0, device="cuda")
+        for i in range(steps):
+            kda.prefill_fused(x.q, x.k, x.v, x.g, x.b, ex.z, x.cu_seqlens, x.slot_ids, x.pool, ex.conv_state,
+                              ex.conv_w, ex.norm_w)
     elif name == "prefill_small":
         x = inputs.prefill_inputs([8192], 32, 128, 128, dtype="bf16", seed=0, device="cuda")
         for i in range(steps):
@@ -768,7 +796,8 @@ def main(argv=None):
     ap.add_argument("--paths", default="decode,spec,fused,prefill,longmix")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ncu-case", default=None,
-                    help="run one small profiling case (decode_small, spec_small, fused_small, prefill_small)")
+                    help="run one small profiling case (decode_small, spec_small, fused_small, prefill_small, "
+                         "prefill_fused_small)")
     args = ap.parse_args(argv)
     if args.ncu_case:
         from gated_delta_rule_decode_gb300 import kda
@@ -797,6 +826,7 @@ def main(argv=None):
             paths["fused_decode"] = run_fused(kda, peaks)
         if "prefill" in wanted:
             paths["prefill"] = run_prefill(kda, peaks)
+            paths["prefill_fused"] = run_prefill_fused(kda, peaks)
         if "longmix" in wanted:
             paths["longmix"] = run_longmix(kda, peaks)
     barrier(world)

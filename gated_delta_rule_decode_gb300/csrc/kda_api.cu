@@ -255,7 +255,8 @@ static int prefill_impl(const kda_dims *dims, int32_t num_seqs, const int32_t *c
                         const float *g, const void *b, const int32_t *slot_ids, float *pool,
                         int64_t num_slots, int32_t init_from_pool, void *out, int32_t num_snaps,
                         const int32_t *snap_seq, const int32_t *snap_tokens, const int32_t *snap_slot,
-                        void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream) {
+                        void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream,
+                        const kda_fused_io *io = nullptr) {
     if (num_snaps < 0) return KDA_ERR_INVALID_ARG;
     if (num_snaps > 0 && (snap_seq == nullptr || snap_tokens == nullptr || snap_slot == nullptr))
         return KDA_ERR_INVALID_ARG;
@@ -268,6 +269,14 @@ static int prefill_impl(const kda_dims *dims, int32_t num_seqs, const int32_t *c
         return KDA_ERR_INVALID_ARG;
     if (num_slots > 0 && !all_aligned({pool})) return KDA_ERR_INVALID_ARG;
     if (total_tokens > (int64_t)0x7fffffff) return KDA_ERR_INVALID_ARG;
+    if (io != nullptr) {
+        // the fused prefill exists on the tensor-core path only
+        if (!kda::prefill_tc_supported(dims->dk, dims->dv, dims->dtype)) return KDA_ERR_UNSUPPORTED;
+        if (!(io->eps_o >= 0.f) || isinf(io->eps_o)) return KDA_ERR_INVALID_ARG;
+        if (!all_aligned({io->conv_w, io->norm_w})) return KDA_ERR_INVALID_ARG;
+        if (total_tokens > 0 && !all_aligned({io->z})) return KDA_ERR_INVALID_ARG;
+        if (num_slots > 0 && !all_aligned({io->conv_state})) return KDA_ERR_INVALID_ARG;
+    }
     const size_t need = kda::prefill_workspace_bytes(dims->num_heads, dims->dk, dims->dv, dims->dtype,
                                                      num_seqs, total_tokens);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
@@ -282,6 +291,10 @@ static int prefill_impl(const kda_dims *dims, int32_t num_seqs, const int32_t *c
     p.num_seqs = num_seqs; p.H = dims->num_heads; p.dk = dims->dk; p.dv = dims->dv;
     p.eps = dims->eps; p.scale = resolve_scale(dims);
     p.num_snaps = num_snaps; p.snap_seq = snap_seq; p.snap_tokens = snap_tokens; p.snap_slot = snap_slot;
+    if (io != nullptr) {
+        p.conv_state = io->conv_state; p.conv_w = io->conv_w; p.z = io->z; p.norm_w = io->norm_w;
+        p.eps_o = io->eps_o;
+    }
     return from_cuda(kda::launch_prefill(p, dims->dtype, (cudaStream_t)stream));
 }
 
@@ -305,6 +318,17 @@ int kda_prefill_chunked_snapshots(const kda_dims *dims, int32_t num_seqs, const 
     return prefill_impl(dims, num_seqs, cu_seqlens, total_tokens, q, k, v, g, b, slot_ids, pool, num_slots,
                         init_from_pool, out, num_snaps, snap_seq, snap_tokens, snap_slot, workspace,
                         workspace_bytes, err_flag, stream);
+}
+
+int kda_prefill_fused(const kda_dims *dims, int32_t num_seqs, const int32_t *cu_seqlens, int64_t total_tokens,
+                      const void *q, const void *k, const void *v, const float *g, const void *b,
+                      const int32_t *slot_ids, float *pool, int64_t num_slots, int32_t init_from_pool,
+                      const kda_fused_io *io, void *out, void *workspace, size_t workspace_bytes,
+                      int32_t *err_flag, void *stream) {
+    if (io == nullptr) return KDA_ERR_INVALID_ARG;
+    return prefill_impl(dims, num_seqs, cu_seqlens, total_tokens, q, k, v, g, b, slot_ids, pool, num_slots,
+                        init_from_pool, out, 0, nullptr, nullptr, nullptr, workspace, workspace_bytes, err_flag,
+                        stream, io);
 }
 
 }  // extern "C"

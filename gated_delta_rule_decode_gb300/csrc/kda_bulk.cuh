@@ -123,6 +123,15 @@ __device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *map, int
         : "memory");
 }
 
+// Prefetch of the box of a 2-D tensor map at (x, y) into L2 (no completion
+// to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const void *map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // Shared -> global 2-D tensor store (box of the tensor map at (x, y)) in the
 // thread's bulk group.
 __device__ __forceinline__ void tma_store_2d(const void *map, int x, int y, const void *src_smem) {

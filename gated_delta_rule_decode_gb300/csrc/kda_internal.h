@@ -101,6 +101,13 @@ struct PrefillParams {
     // sorted by sequence, then by token count
     int32_t num_snaps;
     const int32_t *snap_seq, *snap_tokens, *snap_slot;
+    // fused ShortConv + gated RMS norm (conv_w null: the plain prefill);
+    // tensor-core path only
+    void *conv_state;     // dtype [num_slots][H][3][2 dk + dv]
+    const float *conv_w;  // f32 [H][2 dk + dv][4]
+    const void *z;        // dtype [total_tokens][H][dv]
+    const float *norm_w;  // f32 [dv]
+    float eps_o;
 };
 
 // Snapshot requests of sequence s: [lo, hi) of the sorted request list.

@@ -186,12 +186,36 @@ struct PrepSmem {
     float gC[D];          // gamma at the chunk's last token
     float eref[D];        // e^{ref}
     float xs[32][33];     // partial products of the UT inverse
+    float vhist[3][D];    // fused: the three value inputs before the chunk
     uint64_t bar_in, bar_v, bar_mma, bar_q, bar_kp;
     uint32_t tmem_base;
 };
 constexpr size_t kPrepSmem = sizeof(PrepSmem) + 1024;
 static_assert(sizeof(InvScratch) <= C * D * 6, "inverse scratch must fit the k staging and the K- tile");
 static_assert(offsetof(PrepSmem, qv) % 1024 == 0 && offsetof(PrepSmem, u2) % 1024 == 0, "TMA boxes");
+
+// The staged k and q boxes hold the bf16 inputs; the fused prefill
+// overwrites them with the convolved values as fp16 (10-bit mantissa, so the
+// rounding stays below the later fp16 operands').  A 32-bit word of a box
+// holds two consecutive channels.
+template <bool F16>
+__device__ __forceinline__ float2 box_pair(uint32_t w) {
+    if constexpr (F16) {
+        return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+    } else {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+}
+
+template <bool F16>
+__device__ __forceinline__ float box_elem(const unsigned char *box, int r, int c) {
+    const unsigned char *e = box + tc::sw128_off16(r, c, C);
+    if constexpr (F16) {
+        return __half2float(*reinterpret_cast<const __half *>(e));
+    } else {
+        return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(e));
+    }
+}
 
 // staged bf16 element (row r, channel c) and fp32 element of a 64-row tile
 __device__ __forceinline__ float st_bf16(const unsigned char *box, int r, int c) {
@@ -201,7 +225,48 @@ __device__ __forceinline__ float &st_f32(unsigned char *tile, int r, int c) {
     return *reinterpret_cast<float *>(tile + tc::sw128_off(r, c, C));
 }
 
+// ---- fused ShortConv (the MegaKDA-style prefill)
+
+constexpr int kConvChannels = 3 * D;  // q | k | v channels of a head
+
+// SiLU and the sigmoid gate with the fast exponential and reciprocal (a few
+// ulp; the prefill's operands are rounded to fp16 right after)
+__device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
+// sigmoid(z), the output gate
+__device__ __forceinline__ float sigmoid_gate(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
+
+// The three raw inputs before token t0 of conv channel ch (q | k | v order)
+// of head h, oldest first: from the sequence itself after its first chunk,
+// else from the slot's conv state (init_from_pool) or zero.
 template <typename T>
+__device__ __forceinline__ void conv_history(const PrefillParams &p, bool first, int slot, int h, int t0, int ch,
+                                             float (&hist)[3]) {
+    if (!first) {
+        const T *src = ch < D ? static_cast<const T *>(p.q) : ch < 2 * D ? static_cast<const T *>(p.k)
+                                                                       : static_cast<const T *>(p.v);
+        const int c = ch % D;
+#pragma unroll
+        for (int j = 0; j < 3; ++j) hist[j] = Elem<T>::load1(src + ((int64_t)(t0 - 3 + j) * p.H + h) * D + c);
+    } else if (p.init_from_pool) {
+        const T *cs = static_cast<const T *>(p.conv_state) + ((int64_t)slot * p.H + h) * (3 * kConvChannels);
+#pragma unroll
+        for (int j = 0; j < 3; ++j) hist[j] = Elem<T>::load1(cs + j * kConvChannels + ch);
+    } else {
+        hist[0] = hist[1] = hist[2] = 0.f;
+    }
+}
+
+// silu(w . (x_{t-3}, x_{t-2}, x_{t-1}, x_t)) in the fused decode's order
+__device__ __forceinline__ float conv_tap(float4 w, float x0, float x1, float x2, float x3) {
+    float acc = __fmul_rn(w.x, x0);
+    acc = __fmaf_rn(w.y, x1, acc);
+    acc = __fmaf_rn(w.z, x2, acc);
+    acc = __fmaf_rn(w.w, x3, acc);
+    return silu_f(acc);
+}
+
+template <typename T, bool FUSED>
 __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillParams p,
                                                                    const __grid_constant__ CUtensorMap kmap,
                                                                    const __grid_constant__ CUtensorMap qmap,
@@ -250,6 +315,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
     const int hf = warp >> 2;                 // half of the columns or tokens
     unsigned char *__restrict__ img = static_cast<unsigned char *>(p.workspace) + plan_bytes(n) +
                                       ((size_t)chunk * H + h) * (size_t)IMG_BYTES;
+    // fused: the conv histories are requested first, so that they arrive
+    // with the staged inputs (k and q per thread; v's through shared memory)
+    float khist[3];
+    if constexpr (FUSED) {
+        conv_history<T>(p, chunk == plan[s], slot, h, t0, (tid >= 128 ? 0 : D) + (tid & 127), khist);
+        if (tid < D) {
+            float vh[3];
+            conv_history<T>(p, chunk == plan[s], slot, h, t0, 2 * D + tid, vh);
+#pragma unroll
+            for (int j = 0; j < 3; ++j) sm.vhist[j][tid] = vh[j];
+        }
+    }
     unsigned char *kst = sm.u1.a.kst, *km = sm.u1.a.km, *qv = sm.qv, *gam = sm.u2.gam;
 
     if (warp == 0) tc::tmem_alloc(&sm.tmem_base, PT_COLS);
@@ -293,6 +370,51 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         tma_load_2d(qv + C * 128, &vmap, h * D + 64, t0, &sm.bar_v);
     };
 
+    if (FUSED && ok) {
+        // ---- 0. ShortConv of k (threads 0..127: channel tid) and q (128..255),
+        // in place in the staged boxes as fp16, tokens in descending order so
+        // that every step still reads raw (bf16) inputs
+        const int ch = tid & 127;
+        const bool isq = tid >= 128;
+        const int cch = (isq ? 0 : D) + ch;  // conv channel (q | k | v)
+        unsigned char *box = (isq ? qv : kst) + (ch >> 6) * C * 128;
+        const int cc = ch & 63;
+        const float4 w = __ldg(reinterpret_cast<const float4 *>(p.conv_w) + (int64_t)h * kConvChannels + cch);
+        const float(&hist)[3] = khist;
+        // row r of the channel sits at r * 128 + ((u ^ (r & 7)) << 4) + e in
+        // its box; the unrolled 16-row blocks make r & 7 a constant
+        const int u = cc >> 3, e = (cc & 7) << 1;
+        auto at = [&](int r) { return box + r * 128 + ((u ^ (r & 7)) << 4) + e; };
+        auto x_at = [&](int r) {
+            return r >= 0 ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(at(r))) : hist[3 + r];
+        };
+        // blocks of 16 rows from the top: the block's 16 inputs and the three
+        // below it are loaded first (those rows are still raw: only rows
+        // above have been overwritten), then its 16 outputs are stored
+        float ymax = 0.f;
+#pragma unroll 1
+        for (int blk = (L - 1) >> 4; blk >= 0; --blk) {
+            float x[19];  // x[i] = input of row 16 blk - 3 + i
+#pragma unroll
+            for (int i = 0; i < 19; ++i) {
+                const int r = 16 * blk - 3 + i;
+                x[i] = r < L ? x_at(r) : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int r = 16 * blk + j;
+                if (r < L) {
+                    const float y = conv_tap(w, x[j], x[j + 1], x[j + 2], x[j + 3]);
+                    ymax = fmaxf(ymax, fabsf(y));
+                    *reinterpret_cast<__half *>(at(r)) = __float2half_rn(y);
+                }
+            }
+        }
+        // an overflow of the fp16 values shows as infinity in the running maximum
+        const __half ym = __float2half_rn(ymax);
+        hmax = __hmax2(hmax, __halves2half2(ym, ym));
+        __syncthreads();
+    }
     if (ok) {
         // ---- 1. L2Norm sums of squares (thread = row of k (0..63) or q, one
         // 64-channel half; the 16-byte units of a row are read in its swizzled
@@ -309,9 +431,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                     const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float a = __uint_as_float(w4[e] << 16), b = __uint_as_float(w4[e] & 0xffff0000u);
-                        ss = fmaf(a, a, ss);
-                        ss = fmaf(b, b, ss);
+                        const float2 ab = box_pair<FUSED>(w4[e]);
+                        ss = fmaf(ab.x, ab.x, ss);
+                        ss = fmaf(ab.y, ab.y, ss);
                     }
                 }
             }
@@ -385,8 +507,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                 float x[8], gm[8];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    x[2 * e] = __uint_as_float(w4[e] << 16) * inv;
-                    x[2 * e + 1] = __uint_as_float(w4[e] & 0xffff0000u) * inv;
+                    const float2 ab = box_pair<FUSED>(w4[e]);
+                    x[2 * e] = ab.x * inv;
+                    x[2 * e + 1] = ab.y * inv;
                 }
                 {
                     const float4 g0 = *reinterpret_cast<const float4 *>(gam + tc::sw128_off(tok, c0, C));
@@ -470,7 +593,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int r = 32 * hf + i + e;
-                    const float kx = st_bf16(kst, r, lr) * sm.invk[r];
+                    const float kx = box_elem<FUSED>(kst, r, lr) * sm.invk[r];
                     const float g = st_f32(gam, r, lr);
                     bk[i + e] = sm.beta[r] * kx * __expf(g);
                     kh2[e] = !unsafe ? st_f32(km, r, lr) * egcref : (r < L ? kx * expf(gCv - g) : 0.f);
@@ -531,9 +654,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                 if (j <= r) {
                     for (int cc = 0; cc < D; ++cc) {
                         const float gr = st_f32(gam, r, cc), gj = st_f32(gam, j, cc);
-                        const float m = st_bf16(kst, j, cc) * sm.invk[j] * expf(gr - gj);
-                        a = fmaf(st_bf16(kst, r, cc) * sm.invk[r], m, a);
-                        pp = fmaf(st_bf16(qv, r, cc) * sm.invq[r], m, pp);
+                        const float m = box_elem<FUSED>(kst, j, cc) * sm.invk[j] * expf(gr - gj);
+                        a = fmaf(box_elem<FUSED>(kst, r, cc) * sm.invk[r], m, a);
+                        pp = fmaf(box_elem<FUSED>(qv, r, cc) * sm.invq[r], m, pp);
                     }
                 }
                 areg[it] = (j < r) ? sm.beta[r] * a : 0.f;
@@ -643,10 +766,35 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             v_pend = false;
             mbar_try_wait(&sm.bar_v, 0);
             float bv[32];
+            if constexpr (!FUSED) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int r = 32 * hf + i;
-                bv[i] = r < L ? sm.beta[r] * st_bf16(qv, r, lr) : 0.f;
+                for (int i = 0; i < 32; ++i) {
+                    const int r = 32 * hf + i;
+                    bv[i] = r < L ? sm.beta[r] * st_bf16(qv, r, lr) : 0.f;
+                }
+            } else {
+                // ShortConv of value channel lr on the fly (fp32), the three
+                // inputs before token 32 hf from the box or the history
+                const float4 w =
+                    __ldg(reinterpret_cast<const float4 *>(p.conv_w) + (int64_t)h * kConvChannels + 2 * D + lr);
+                float hist[3];
+                if (hf == 0) {
+#pragma unroll
+                    for (int j = 0; j < 3; ++j) hist[j] = sm.vhist[j][lr];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 3; ++j) hist[j] = st_bf16(qv, 29 + j, lr);
+                }
+                float x0 = hist[0], x1 = hist[1], x2 = hist[2];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int r = 32 * hf + i;
+                    const float x3 = st_bf16(qv, r, lr);
+                    bv[i] = r < L ? sm.beta[r] * conv_tap(w, x0, x1, x2, x3) : 0.f;
+                    x0 = x1;
+                    x1 = x2;
+                    x2 = x3;
+                }
             }
             tc::st16(tc::lane_addr(tm, warp, PT_BV + 32 * hf), *reinterpret_cast<float(*)[16]>(&bv[0]));
             tc::st16(tc::lane_addr(tm, warp, PT_BV + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(&bv[16]));
@@ -910,7 +1058,7 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar) {
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
-template <typename T>
+template <typename T, bool FUSED>
 __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillParams p,
                                                                   const __grid_constant__ CUtensorMap omap,
                                                                   const int seg_lo, const int seg_hi) {
@@ -1083,6 +1231,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
         // waits): the data warps arrive on tile_full once their part is
         // written, thread 0 then issues the store and, once the previous
         // store has read its tile, arrives on that tile's tile_free.
+        constexpr bool fused = FUSED;
         auto output = [&](int cj) {
             const int64_t tj = (int64_t)cs + (int64_t)(c_lo + cj) * C;
             const int Lj = (int)((int64_t)ce - tj < C ? (int64_t)ce - tj : C);
@@ -1090,12 +1239,14 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
             tc::ld16(taddr(CT_ACC + (cj & 1) * CT_ACC_STRIDE + 128 + cq * 16), o);
             tc::wait_ld();
             warp_arrive(&sm.acc_free[cj & 1]);  // the accumulator has been read
+#pragma unroll
+            for (int r = 0; r < 16; ++r) o[r] = p.scale * o[r];
             if (Lj == C) {
                 const int t = cj & 1, use = cj >> 1;  // the tile and its use count
                 if (use > 0 && !warp_wait(&sm.tile_free[t], (use - 1) & 1)) return false;
                 T *tile = reinterpret_cast<T *>(sm.ot[t]) + (cq * 16) * D + lr;
 #pragma unroll
-                for (int r = 0; r < 16; ++r) Elem<T>::store1(tile + r * D, p.scale * o[r]);
+                for (int r = 0; r < 16; ++r) Elem<T>::store1(tile + r * D, o[r]);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if ((tid & 31) == 0) mbar_arrive(&sm.tile_full);
@@ -1118,7 +1269,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
                 T *dst = out + (tj + cq * 16) * tok_stride + hoff + lr;
 #pragma unroll
                 for (int r = 0; r < 16; ++r)
-                    if (cq * 16 + r < Lj) Elem<T>::store1(dst + (int64_t)r * tok_stride, p.scale * o[r]);
+                    if (cq * 16 + r < Lj) Elem<T>::store1(dst + (int64_t)r * tok_stride, o[r]);
             }
             return true;
         };
@@ -1174,6 +1325,29 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
         }
         // requests past the sequence's last whole chunk can never be met
         if (ok && snap_ptr < snap_hi && c_hi == nchunks_all) snap_bad = true;
+        if (fused && c_hi == nchunks_all) {
+            // the slot's conv state: the last three raw inputs of the
+            // sequence, preceded by its old history (or zeros) when the
+            // sequence is shorter; the prep kernel read the old one before
+            // this launch (the first chunk's segment runs first)
+            const int Ls = ce - cs;
+            T *cst = static_cast<T *>(p.conv_state) + ((int64_t)slot * H + h) * (3 * kConvChannels);
+            for (int ch = tid; ch < kConvChannels; ch += kDataThreads) {
+                const T *src = ch < D ? static_cast<const T *>(p.q) : ch < 2 * D ? static_cast<const T *>(p.k)
+                                                                               : static_cast<const T *>(p.v);
+                const int c = ch % D;
+                T old[3], nv[3];
+#pragma unroll
+                for (int j = 0; j < 3; ++j) old[j] = p.init_from_pool ? cst[j * kConvChannels + ch] : T(0.f);
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    const int pos = Ls - 3 + j;
+                    nv[j] = pos >= 0 ? src[((int64_t)cs + pos) * tok_stride + hoff + c] : old[3 + pos];
+                }
+#pragma unroll
+                for (int j = 0; j < 3; ++j) cst[j * kConvChannels + ch] = nv[j];
+            }
+        }
         if (snap_bad && h == 0 && tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_SNAPSHOT);
         if (tid == 0) bulk_wait_all();  // every tensor store complete before shared memory goes
         const bool bad = !(__low2float(s16max) <= kHalfMax) || !(__high2float(s16max) <= kHalfMax);
@@ -1190,6 +1364,36 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tm, CT_COLS);
+}
+
+// The fused prefill's output side: out = o / sqrt(mean(o^2) + eps_o) * norm_w
+// * sigmoid(z) per (token, head), in place over the chain's outputs.  One
+// warp per (token, head), four values per lane; the sum of squares is a
+// butterfly over the warp (the same bits on every lane).  Padding sequences'
+// zero outputs stay zero.
+constexpr int kGateWarps = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(kGateWarps * 32) norm_gate_kernel(const PrefillParams p) {
+    const int64_t row = (int64_t)blockIdx.x * kGateWarps + (threadIdx.x >> 5);  // token x head
+    if (row >= p.total_tokens * p.H) return;
+    const int lane = threadIdx.x & 31;
+    T *o = static_cast<T *>(p.out) + row * D + 4 * lane;
+    const T *z = static_cast<const T *>(p.z) + row * D + 4 * lane;
+    float x[4], zz[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[e] = Elem<T>::to_f(o[e]);
+        zz[e] = Elem<T>::to_f(z[e]);
+    }
+    const float4 w = __ldg(reinterpret_cast<const float4 *>(p.norm_w) + lane);
+    float ss = __fmaf_rn(x[3], x[3], __fmaf_rn(x[2], x[2], __fmaf_rn(x[1], x[1], __fmul_rn(x[0], x[0]))));
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, m));
+    const float inv = rsqrtf(__fadd_rn(__fmul_rn(ss, 1.0f / D), p.eps_o));
+    const float wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = T(__fmul_rn(__fmul_rn(__fmul_rn(x[e], inv), wv[e]), sigmoid_gate(zz[e])));
 }
 
 }  // namespace prefill_tc
@@ -1217,12 +1421,13 @@ constexpr int kSegMinCtas = 2048;
 #endif
 constexpr int kSegMinChunks = 64;
 
-cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
+template <bool FUSED>
+static cudaError_t launch_tc(const PrefillParams &p, cudaStream_t st) {
     using namespace prefill_tc;
-    cudaError_t e = cudaFuncSetAttribute(prep_tc_kernel<__nv_bfloat16>,
+    cudaError_t e = cudaFuncSetAttribute(prep_tc_kernel<__nv_bfloat16, FUSED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(chain_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(chain_kernel<__nv_bfloat16, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kChainSmem);
     if (e != cudaSuccess) return e;
     const int64_t mc = max_chunks(p.num_seqs, p.total_tokens);
@@ -1319,16 +1524,27 @@ cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
             cfg.attrs = attr;
             cfg.numAttrs = k > 0 ? 1 : 0;
             const PrefillParams pp = p;
-            e = cudaLaunchKernelEx(&cfg, prep_tc_kernel<__nv_bfloat16>, pp, kmap, qmap, vmap, gmap, lo, seg_len,
+            e = cudaLaunchKernelEx(&cfg, prep_tc_kernel<__nv_bfloat16, FUSED>, pp, kmap, qmap, vmap, gmap, lo, seg_len,
                                    k > 0 ? 1 : 0);
             if (e != cudaSuccess) return e;
         }
-        chain_kernel<__nv_bfloat16><<<cgrid, kChainThreads, kChainSmem, st>>>(p, omap, lo,
+        chain_kernel<__nv_bfloat16, FUSED><<<cgrid, kChainThreads, kChainSmem, st>>>(p, omap, lo,
                                                                              last ? INT_MAX : lo + len);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
+    if (FUSED && p.total_tokens > 0) {
+        const int64_t rows = p.total_tokens * p.H;
+        norm_gate_kernel<__nv_bfloat16>
+            <<<(unsigned)((rows + kGateWarps - 1) / kGateWarps), kGateWarps * 32, 0, st>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     return cudaSuccess;
+}
+
+cudaError_t launch_prefill_tc(const PrefillParams &p, cudaStream_t st) {
+    return p.conv_w != nullptr ? launch_tc<true>(p, st) : launch_tc<false>(p, st);
 }
 
 }  // namespace kda

@@ -109,6 +109,20 @@ def fused_extras(B, H, dk, dv, dtype="bf16", num_slots=None, seed=0, device="cpu
     return FusedExtras(conv_state, conv_w, z, norm_w)
 
 
+def fused_prefill_extras(T, n_seqs, H, dk, dv, dtype="bf16", num_slots=None, seed=0, device="cpu"):
+    """The fused prefill's extra inputs: as ``fused_extras``, with z drawn per
+    token ([T, H, dv])."""
+    num_slots = n_seqs if num_slots is None else num_slots
+    gen = _gen(seed + 7919, device)
+    dt = torch_dtype(dtype)
+    nc = 2 * dk + dv
+    conv_state = _normal((num_slots, H, 3, nc), gen, device).to(dt)
+    conv_w = _normal((H, nc, 4), gen, device, std=0.5)
+    z = _normal((T, H, dv), gen, device).to(dt)
+    norm_w = _normal((dv,), gen, device, std=0.1, mean=1.0)
+    return FusedExtras(conv_state, conv_w, z, norm_w)
+
+
 @dataclass
 class VerifyInputs:
     q: torch.Tensor             # [B, D, H, dk]

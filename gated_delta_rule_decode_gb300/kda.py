@@ -36,7 +36,7 @@ EXPORTED = ("kda_decode", "kda_verify_record", "kda_replay_commit",
             "kda_prefill_chunked_static", "kda_static_scratch_bytes",
             "kda_verify_workspace_bytes", "kda_prefill_chunked_snapshots",
             "kda_records_u_bytes", "kda_verify_record_u", "kda_replay_commit_u",
-            "kda_commit_verify_u", "kda_decode_fused")
+            "kda_commit_verify_u", "kda_decode_fused", "kda_prefill_fused")
 
 
 class KdaError(RuntimeError):
@@ -87,6 +87,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kda_decode_fused.argtypes = [_PD, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                      _I64, _PF, _VP, _VP, _VP]
     lib.kda_decode_fused.restype = ctypes.c_int
+    lib.kda_prefill_fused.argtypes = [_PD, _I32, _VP, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I64,
+                                      _I32, _PF, _VP, _VP, _SZ, _VP, _VP]
+    lib.kda_prefill_fused.restype = ctypes.c_int
     lib.kda_verify_record.argtypes = [_PD, _I32, _I32, _VP, _VP, _VP, _VP, _VP,
                                       _VP, _VP, _I64, _VP, _PR, _VP, _SZ, _VP, _VP]
     lib.kda_verify_workspace_bytes.argtypes = [_PD, _I32, _I32]
@@ -258,6 +261,53 @@ def decode_fused(q, k, v, g, b, z, slot_ids, pool, conv_state, conv_w, norm_w, o
     if _prepare:
         return _Prepared(_lib.kda_decode_fused, args, "kda_decode_fused", (dims, io), out)
     _check(_lib.kda_decode_fused(*args), "kda_decode_fused")
+    return out
+
+
+def prefill_fused(q, k, v, g, b, z, cu_seqlens, slot_ids, pool, conv_state, conv_w, norm_w, out=None, *,
+                  init_from_pool=False, workspace=None, eps=1e-6, eps_o=1e-6, scale=None, err_flag=None,
+                  stream=None, _prepare=False):
+    """MegaKDA-style fused prefill: ShortConv of q, k, v along each sequence
+    (history from ``conv_state`` when ``init_from_pool``, else zero; the conv
+    state is updated), the chunked prefill on ``pool``, then RMS norm x
+    norm_w x sigmoid(z) per token.  bf16 with dk = dv = 128 only.
+
+    q, k: [T, H, dk]; v, z: [T, H, dv]; g: [T, H, dk] fp32; b: [T, H];
+    cu_seqlens: [n+1] int32; slot_ids: [n] int32; conv_state:
+    [num_slots, H, 3, 2 dk + dv]; conv_w: [H, 2 dk + dv, 4] fp32;
+    norm_w: [dv] fp32.  Returns out [T, H, dv].
+    """
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    n = slot_ids.shape[0]
+    dt = q.dtype
+    S = pool.shape[0]
+    for name, t, shp, d in (("q", q, (T, H, dk), dt), ("k", k, (T, H, dk), dt),
+                            ("v", v, (T, H, dv), dt), ("g", g, (T, H, dk), torch.float32),
+                            ("b", b, (T, H), dt), ("z", z, (T, H, dv), dt),
+                            ("cu_seqlens", cu_seqlens, (n + 1,), torch.int32),
+                            ("slot_ids", slot_ids, (n,), torch.int32),
+                            ("pool", pool, (S, H, dv, dk), torch.float32),
+                            ("conv_state", conv_state, (S, H, 3, 2 * dk + dv), dt),
+                            ("conv_w", conv_w, (H, 2 * dk + dv, 4), torch.float32),
+                            ("norm_w", norm_w, (dv,), torch.float32)):
+        _need(t, name, shp, d)
+    if out is None:
+        out = torch.empty((T, H, dv), dtype=dt, device=q.device)
+    _need(out, "out", (T, H, dv), dt)
+    code = _dtype_code(q)
+    need = prefill_workspace_bytes(H, dk, dv, code, n, T)
+    if workspace is None and need > 0:
+        workspace = _scratch(need, q.device, stream)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    dims = make_dims(H, dk, dv, code, eps, scale)
+    io = KdaFusedIo(conv_state.data_ptr(), conv_w.data_ptr(), z.data_ptr(), norm_w.data_ptr(), float(eps_o))
+    args = (ctypes.byref(dims), n, _ptr(cu_seqlens), T, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b),
+            _ptr(slot_ids), _ptr(pool), S, 1 if init_from_pool else 0, ctypes.byref(io), _ptr(out),
+            _ptr(workspace), ws_bytes, _ptr(err_flag), _stream_handle(stream))
+    if _prepare:
+        return _Prepared(_lib.kda_prefill_fused, args, "kda_prefill_fused", (dims, io, workspace), out)
+    _check(_lib.kda_prefill_fused(*args), "kda_prefill_fused")
     return out
 
 

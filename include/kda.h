@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 5
+#define KDA_ABI_VERSION 6
 
 #if defined(__GNUC__)
 #define KDA_API __attribute__((visibility("default")))
@@ -393,6 +393,32 @@ KDA_API int kda_prefill_chunked_snapshots(const kda_dims *dims, int32_t num_seqs
                                           const int32_t *snap_tokens, const int32_t *snap_slot,
                                           void *workspace, size_t workspace_bytes,
                                           int32_t *err_flag, void *stream);
+
+/*
+ * kda_prefill_fused: the MegaKDA-style fused prefill ("2.8x faster Kimi K3
+ * inference on CANN", section 03 "MegaKDA"), the prefill counterpart of
+ * kda_decode_fused.  For each sequence and head:
+ *   - the ShortConv of kda_decode_fused runs along the sequence: the three
+ *     inputs before its first token are the slot's conv state when
+ *     init_from_pool is set, else zero; the convolved k and q are rounded to
+ *     dtype (bf16), the convolved v stays fp32;
+ *   - the chunked prefill of kda_prefill_chunked runs on the convolved
+ *     inputs (init_from_pool selects the KDA state's start as there);
+ *   - out = o / sqrt(mean_i o_i^2 + eps_o) * norm_w * sigmoid(z) per token;
+ *   - the slot's conv state afterwards holds the last three raw inputs of the
+ *     history followed by the sequence (so a decode continues from it).
+ * Arguments as for kda_prefill_chunked, plus `io` (kda_fused_io, with z of
+ * shape dtype [total_tokens][H][dv]).  Only the tensor-core shape (bf16,
+ * dk = dv = 128) is built; every other shape returns KDA_ERR_UNSUPPORTED.
+ * Padding and out-of-range sequences output zero and leave both pools alone.
+ */
+KDA_API int kda_prefill_fused(const kda_dims *dims, int32_t num_seqs,
+                      const int32_t *cu_seqlens, int64_t total_tokens,
+                      const void *q, const void *k, const void *v, const float *g,
+                      const void *b, const int32_t *slot_ids, float *pool,
+                      int64_t num_slots, int32_t init_from_pool,
+                      const kda_fused_io *io, void *out, void *workspace,
+                      size_t workspace_bytes, int32_t *err_flag, void *stream);
 
 /*
  * kda_prefill_chunked_static: kda_prefill_chunked without a caller-provided

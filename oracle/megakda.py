@@ -124,14 +124,17 @@ def prefill_fused(q, k, v, g, b, z, wq, wk, wv, w_o, cu_seqlens, slot_ids, pool,
         sl = int(slots[s])
         if sl < 0 or sl >= cpool.shape[0]:
             continue
+        a, e = cu[s], cu[s + 1]
         for h in range(H):
             hist = cpool[sl, h].copy() if init_from_pool else np.zeros((3, 2 * dk + dv))
-            for t in range(cu[s], cu[s + 1]):
-                qc[t, h], hq = short_conv_step(hist[:, :dk], q[t, h], wq[h])
-                kc[t, h], hk = short_conv_step(hist[:, dk:2 * dk], k[t, h], wk[h])
-                vc[t, h], hv = short_conv_step(hist[:, 2 * dk:], v[t, h], wv[h])
-                hist = np.concatenate([hq, hk, hv], axis=1)
-            cpool[sl, h] = hist
+            # the raw inputs of the sequence after its three-token history
+            x = np.concatenate([hist, np.concatenate([q[a:e, h], k[a:e, h], v[a:e, h]], axis=1)])
+            w = np.concatenate([wq[h], wk[h], wv[h]])          # [2 dk + dv, 4]
+            L = e - a
+            # y_t = silu(sum_i w[:, i] x_{t-3+i}): window i of x starts at row i
+            y = silu(sum(w[:, i] * x[i:i + L] for i in range(4)))
+            qc[a:e, h], kc[a:e, h], vc[a:e, h] = y[:, :dk], y[:, dk:2 * dk], y[:, 2 * dk:]
+            cpool[sl, h] = x[-3:]
     o, P, err = _prefill(qc, kc, vc, g, b, cu, slots, pool, init_from_pool=init_from_pool,
                          eps=eps, scale=scale)
     out = rms_norm_gate(o, z, w_o, eps_o)

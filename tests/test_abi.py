@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(kda):
     for name in declared_functions():
         assert hasattr(lib, name), name
     assert set(kda.EXPORTED) <= set(declared_functions())
-    assert lib.kda_abi_version() == 5
+    assert lib.kda_abi_version() == 6
 
 
 def test_status_strings(kda):
