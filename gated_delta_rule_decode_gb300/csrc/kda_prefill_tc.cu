@@ -1380,11 +1380,14 @@ __global__ void __launch_bounds__(kGateWarps * 32) norm_gate_kernel(const Prefil
     const int lane = threadIdx.x & 31;
     T *o = static_cast<T *>(p.out) + row * D + 4 * lane;
     const T *z = static_cast<const T *>(p.z) + row * D + 4 * lane;
+    static_assert(sizeof(T) == 2, "four 16-bit values per 8-byte access");
+    const uint2 ov = *reinterpret_cast<const uint2 *>(o), zv = *reinterpret_cast<const uint2 *>(z);
+    const T *oe = reinterpret_cast<const T *>(&ov), *ze = reinterpret_cast<const T *>(&zv);
     float x[4], zz[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        x[e] = Elem<T>::to_f(o[e]);
-        zz[e] = Elem<T>::to_f(z[e]);
+        x[e] = Elem<T>::to_f(oe[e]);
+        zz[e] = Elem<T>::to_f(ze[e]);
     }
     const float4 w = __ldg(reinterpret_cast<const float4 *>(p.norm_w) + lane);
     float ss = __fmaf_rn(x[3], x[3], __fmaf_rn(x[2], x[2], __fmaf_rn(x[1], x[1], __fmul_rn(x[0], x[0]))));
@@ -1392,8 +1395,10 @@ __global__ void __launch_bounds__(kGateWarps * 32) norm_gate_kernel(const Prefil
     for (int m = 16; m >= 1; m >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, m));
     const float inv = rsqrtf(__fadd_rn(__fmul_rn(ss, 1.0f / D), p.eps_o));
     const float wv[4] = {w.x, w.y, w.z, w.w};
+    T y[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) o[e] = T(__fmul_rn(__fmul_rn(__fmul_rn(x[e], inv), wv[e]), sigmoid_gate(zz[e])));
+    for (int e = 0; e < 4; ++e) y[e] = T(__fmul_rn(__fmul_rn(__fmul_rn(x[e], inv), wv[e]), sigmoid_gate(zz[e])));
+    *reinterpret_cast<uint2 *>(o) = *reinterpret_cast<const uint2 *>(y);
 }
 
 }  // namespace prefill_tc
