@@ -123,15 +123,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *map, int
         : "memory");
 }
 
-// Prefetch of the box of a 2-D tensor map at (x, y) into L2 (no completion
-// to wait for).
-__device__ __forceinline__ void tma_prefetch_2d(const void *map, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
 // Shared -> global 2-D tensor store (box of the tensor map at (x, y)) in the
 // thread's bulk group.
 __device__ __forceinline__ void tma_store_2d(const void *map, int x, int y, const void *src_smem) {
@@ -156,14 +147,14 @@ __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy (bulk copy) reads of the same memory.
 // Orders this thread's earlier generic-proxy accesses to global memory before
 // later async-proxy (bulk copy) accesses to the same locations.
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (bulk copy) reads of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
