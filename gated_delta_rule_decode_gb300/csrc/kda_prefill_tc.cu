@@ -704,46 +704,70 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             }
         }
         __syncthreads();
-        for (int idx = tid; idx < 2 * 256; idx += kPrepThreads) {
-            const int o = 32 * (idx >> 8), r = (idx >> 4) & 15, j = idx & 15;
+        // The block products keep two outputs (level 1) or a 2 x 2 block of
+        // outputs (level 2) per thread, so that each operand load serves two
+        // products.  The upper triangles of the diagonal blocks and the upper
+        // right blocks hold zeros, so the sums run over whole blocks.
+        {
+            // level 1: X1 = A21 T11 per 32-row block ob (rows 2 rp, 2 rp + 1,
+            // column j of the 16 x 16 block), then T21 = -T22 X1
+            const int ob = tid >> 7, o = 32 * ob, rp = (tid >> 4) & 7, j = tid & 15;
+            const int r0 = 2 * rp;
             float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-            for (int k = 0; k < 16; k += 2) {
-                x0 = fmaf(As[o + 16 + r][o + k], Ts[o + k][o + j], x0);
-                x1 = fmaf(As[o + 16 + r][o + k + 1], Ts[o + k + 1][o + j], x1);
+            for (int k = 0; k < 16; ++k) {
+                const float t = Ts[o + k][o + j];
+                x0 = fmaf(As[o + 16 + r0][o + k], t, x0);
+                x1 = fmaf(As[o + 17 + r0][o + k], t, x1);
             }
-            sm.xs[(idx >> 8) * 16 + r][j] = x0 + x1;
+            sm.xs[16 * ob + r0][j] = x0;
+            sm.xs[16 * ob + r0 + 1][j] = x1;
+            __syncthreads();
+            float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const float x = sm.xs[16 * ob + m][j];
+                y0 = fmaf(Ts[o + 16 + r0][o + 16 + m], x, y0);
+                y1 = fmaf(Ts[o + 17 + r0][o + 16 + m], x, y1);
+            }
+            Ts[o + 16 + r0][o + j] = -y0;
+            Ts[o + 17 + r0][o + j] = -y1;
         }
         __syncthreads();
-        for (int idx = tid; idx < 2 * 256; idx += kPrepThreads) {
-            const int o = 32 * (idx >> 8), r = (idx >> 4) & 15, j = idx & 15;
-            float t = 0.f;
+        {
+            // level 2: X2 = A21 T11 over the 32 x 32 blocks (rows 2 rp,
+            // 2 rp + 1; columns cp, cp + 16), then T21 = -T22 X2
+            const int rp = tid >> 4, cp = tid & 15;
+            const int r0 = 2 * rp;
+            float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
-                if (m <= r) t = fmaf(Ts[o + 16 + r][o + 16 + m], sm.xs[(idx >> 8) * 16 + m][j], t);
-            Ts[o + 16 + r][o + j] = -t;
-        }
-        __syncthreads();
-        for (int idx = tid; idx < 32 * 32; idx += kPrepThreads) {
-            const int r = idx >> 5, j = idx & 31;
-            float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-                x0 = fmaf(As[32 + r][k], Ts[k][j], x0);
-                x1 = fmaf(As[32 + r][k + 1], Ts[k + 1][j], x1);
+            for (int k = 0; k < 32; ++k) {
+                const float a0 = As[32 + r0][k], a1 = As[33 + r0][k];
+                const float t0 = Ts[k][cp], t1 = Ts[k][cp + 16];
+                x00 = fmaf(a0, t0, x00);
+                x01 = fmaf(a0, t1, x01);
+                x10 = fmaf(a1, t0, x10);
+                x11 = fmaf(a1, t1, x11);
             }
-            sm.xs[r][j] = x0 + x1;
-        }
-        __syncthreads();
-        for (int idx = tid; idx < 32 * 32; idx += kPrepThreads) {
-            const int r = idx >> 5, j = idx & 31;
-            float t0v = 0.f, t1v = 0.f;
+            sm.xs[r0][cp] = x00;
+            sm.xs[r0][cp + 16] = x01;
+            sm.xs[r0 + 1][cp] = x10;
+            sm.xs[r0 + 1][cp + 16] = x11;
+            __syncthreads();
+            float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
 #pragma unroll
-            for (int m = 0; m < 32; m += 2) {
-                if (m <= r) t0v = fmaf(Ts[32 + r][32 + m], sm.xs[m][j], t0v);
-                if (m + 1 <= r) t1v = fmaf(Ts[32 + r][32 + m + 1], sm.xs[m + 1][j], t1v);
+            for (int m = 0; m < 32; ++m) {
+                const float a0 = Ts[32 + r0][32 + m], a1 = Ts[33 + r0][32 + m];
+                const float x0 = sm.xs[m][cp], x1 = sm.xs[m][cp + 16];
+                y00 = fmaf(a0, x0, y00);
+                y01 = fmaf(a0, x1, y01);
+                y10 = fmaf(a1, x0, y10);
+                y11 = fmaf(a1, x1, y11);
             }
-            Ts[32 + r][j] = -(t0v + t1v);
+            Ts[32 + r0][cp] = -y00;
+            Ts[32 + r0][cp + 16] = -y01;
+            Ts[33 + r0][cp] = -y10;
+            Ts[33 + r0][cp + 16] = -y11;
         }
         __syncthreads();
         // T into its swizzled tile (over gamma, which nothing reads any more)
