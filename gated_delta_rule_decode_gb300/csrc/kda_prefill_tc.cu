@@ -193,6 +193,7 @@ struct PrepSmem {
 constexpr size_t kPrepSmem = sizeof(PrepSmem) + 1024;
 static_assert(sizeof(InvScratch) <= C * D * 6, "inverse scratch must fit the k staging and the K- tile");
 static_assert(offsetof(PrepSmem, qv) % 1024 == 0 && offsetof(PrepSmem, u2) % 1024 == 0, "TMA boxes");
+static_assert(offsetof(PrepSmem, invk) % 16 == 0 && offsetof(PrepSmem, beta) % 16 == 0, "vector loads");
 
 // The staged k and q boxes hold the bf16 inputs; the fused prefill
 // overwrites them with the convolved values as fp16 (10-bit mantissa, so the
@@ -439,41 +440,40 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             }
             sm.nrm[ch][row] = ss;
         }
-        // ---- 2. gamma, in place (thread = channel lr): tokens 0..31 (running
-        // sum ending at ref = gamma_31), then 32..63 continuing from ref; rows
-        // past the chunk's end repeat gamma_C
+        // ---- 2. gamma, in place (thread = channel lr): both token halves'
+        // running sums at once, from zero; the first ends at ref = gamma_31,
+        // which the second half adds once it is known; rows past the chunk's
+        // end repeat gamma_C
         float gmin = 0.f, gmax = 0.f, gc = 0.f;
-        if (hf == 0) {
+        float part[32];
+        {
             float acc = 0.f;
-#pragma unroll 8
-            for (int r = 0; r < 32; ++r) {
-                float &g = st_f32(gam, r, lr);
-                acc += r < L ? g : 0.f;
-                g = acc;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int r = 32 * hf + i;
+                acc += r < L ? st_f32(gam, r, lr) : 0.f;
+                part[i] = acc;
                 if (r == L - 1) gc = acc;
-                gmin = r == 0 ? acc : fminf(gmin, acc);
-                gmax = r == 0 ? acc : fmaxf(gmax, acc);
+                gmin = i == 0 ? acc : fminf(gmin, acc);
+                gmax = i == 0 ? acc : fmaxf(gmax, acc);
             }
-            sm.ref[lr] = acc;
-            sm.lo[lr] = gmin;
-            sm.hi[lr] = gmax;
-            if (L <= 32) sm.gC[lr] = gc;
+            if (hf == 0) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) st_f32(gam, i, lr) = part[i];
+                sm.ref[lr] = acc;
+                sm.lo[lr] = gmin;
+                sm.hi[lr] = gmax;
+                if (L <= 32) sm.gC[lr] = gc;
+            }
         }
         __syncthreads();
         if (hf == 1) {
             const float ref = sm.ref[lr];
-            float acc = ref;
-            gmin = sm.lo[lr];
-            gmax = sm.hi[lr];
-#pragma unroll 8
-            for (int r = 32; r < 64; ++r) {
-                float &g = st_f32(gam, r, lr);
-                acc += r < L ? g : 0.f;
-                g = acc;
-                if (r == L - 1) gc = acc;
-                gmin = fminf(gmin, acc);
-                gmax = fmaxf(gmax, acc);
-            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) st_f32(gam, 32 + i, lr) = part[i] + ref;
+            gmin = fminf(sm.lo[lr], gmin + ref);
+            gmax = fmaxf(sm.hi[lr], gmax + ref);
+            gc += ref;
             if (L > 32) sm.gC[lr] = gc;
             const float gCv = L > 32 ? gc : sm.gC[lr];
             unsafe = fmaxf(gmax - ref, ref - gmin) > kSpanLimit;
@@ -529,7 +529,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                         const float E = __expf(gm[e] - rf[e]);  // e^{gamma - ref}
                         plus[e] = x[e] * E;
                         qt[e] = plus[e] * er[e];
-                        ei[e] = __expf(rf[e] - gm[e]);          // e^{ref - gamma}
+                    }
+                    if (!isq) {  // (warp-uniform) K- for the key rows
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ei[e] = __expf(rf[e] - gm[e]);  // e^{ref - gamma}
                     }
                 } else {
 #pragma unroll
@@ -590,12 +593,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
                 float kh2[2];
+                const float2 ik = *reinterpret_cast<const float2 *>(&sm.invk[32 * hf + i]);
+                const float2 bt = *reinterpret_cast<const float2 *>(&sm.beta[32 * hf + i]);
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int r = 32 * hf + i + e;
-                    const float kx = box_elem<FUSED>(kst, r, lr) * sm.invk[r];
+                    const float kx = box_elem<FUSED>(kst, r, lr) * (e ? ik.y : ik.x);
                     const float g = st_f32(gam, r, lr);
-                    bk[i + e] = sm.beta[r] * kx * __expf(g);
+                    bk[i + e] = (e ? bt.y : bt.x) * kx * __expf(g);
                     kh2[e] = !unsafe ? st_f32(km, r, lr) * egcref : (r < L ? kx * expf(gCv - g) : 0.f);
                 }
                 kw[i >> 1] = pack_h2(kh2[0], kh2[1]);
@@ -792,9 +797,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             float bv[32];
             if constexpr (!FUSED) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int r = 32 * hf + i;
-                    bv[i] = r < L ? sm.beta[r] * st_bf16(qv, r, lr) : 0.f;
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 b4 = *reinterpret_cast<const float4 *>(&sm.beta[32 * hf + i]);
+                    const float bb4[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = 32 * hf + i + e;
+                        bv[i + e] = r < L ? bb4[e] * st_bf16(qv, r, lr) : 0.f;
+                    }
                 }
             } else {
                 // ShortConv of value channel lr on the fly (fp32), the three
