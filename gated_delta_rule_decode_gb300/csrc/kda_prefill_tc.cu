@@ -1459,6 +1459,9 @@ constexpr int kSegMinCtas = 2048;
 #define KDA_SEG_FIRST_PCT 72
 #endif
 constexpr int kSegMinChunks = 64;
+// Measured at 102 400 tokens x 32 heads: 7 segments (25) took 4.90 ms, 12
+// segments (10) 4.96 ms, 5 (40) 4.94 ms, 3 (100) 4.98 ms, one 6.21 ms.
+constexpr int64_t kSegTailChunks = 25;
 
 template <bool FUSED>
 static cudaError_t launch_tc(const PrefillParams &p, cudaStream_t st) {
@@ -1519,10 +1522,11 @@ static cudaError_t launch_tc(const PrefillParams &p, cudaStream_t st) {
     int nseg = 1, seg_chunks = 0;
     if (any && p.num_seqs > 0 && (int64_t)p.num_seqs * p.H <= (int64_t)sms) {
         const int64_t per_seq = (p.total_tokens + C - 1) / C / p.num_seqs;  // mean chunks per sequence
-        // about sqrt(per_seq / 10) segments balance the exposed last chain
-        // (per_seq / K chunks at ~1.7 us) against the K prep tails (~17 us)
+        // about sqrt(per_seq / kSegTailChunks) segments balance the exposed
+        // last chain (per_seq / K chunk steps) against what each segment
+        // boundary costs (a prep grid's tail, about kSegTailChunks chunk steps)
         int64_t kopt = 1;
-        while ((kopt + 1) * (kopt + 1) * 10 <= per_seq) ++kopt;
+        while ((kopt + 1) * (kopt + 1) * kSegTailChunks <= per_seq) ++kopt;
         const int64_t ctas_per_chunk = (int64_t)p.num_seqs * p.H;
         int64_t len = (kSegMinCtas + ctas_per_chunk - 1) / ctas_per_chunk;
         if (len < kSegMinChunks) len = kSegMinChunks;
