@@ -59,6 +59,7 @@ namespace prefill_tc {
 constexpr int C = 64;   // chunk length
 constexpr int D = 128;  // dk = dv
 constexpr float kSpanLimit = 80.f;
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
 
 // Operand image of one (chunk, head) in the workspace (bytes).
 // Every tile is fp16, K-major and 128B-swizzled, in the layout the chain's
@@ -97,6 +98,14 @@ __device__ __forceinline__ uint32_t pack_h2_track(float a, float b, __half2 &hma
     const __half2 h = __floats2half2_rn(a, b);
     hmax = __hmax2(hmax, __habs2(h));
     return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// 2^x with the special function unit's approximate base-2 exponential
+// (results below the normal range flush to zero); e^y = 2^{y log2(e)}
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ void sync_for_mma() {
@@ -185,6 +194,7 @@ struct PrepSmem {
     float lo[D], hi[D];   // extremes of gamma over the chunk
     float gC[D];          // gamma at the chunk's last token
     float eref[D];        // e^{ref}
+    float nrl[D];         // -ref log2(e)
     float xs[32][33];     // partial products of the UT inverse
     float vhist[3][D];    // fused: the three value inputs before the chunk
     uint64_t bar_in, bar_v, bar_mma, bar_q, bar_kp;
@@ -336,7 +346,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         mbar_init(&sm.bar_v, 1);
         mbar_init(&sm.bar_q, 1);
         mbar_init(&sm.bar_kp, 1);
-        mbar_init(&sm.bar_mma, 1);
+        mbar_init(&sm.bar_mma, 2);  // threads 0 and 32 each commit their products
         fence_barrier_init();
         mbar_arrive_expect_tx(&sm.bar_in, 2 * (C * D * 2) + C * D * 4);  // k, q (bf16) and g (fp32)
         tma_load_2d(kst, &kmap, h * D, t0, &sm.bar_in);
@@ -479,6 +489,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             unsafe = fmaxf(gmax - ref, ref - gmin) > kSpanLimit;
             reinterpret_cast<float *>(img + IMG_EGC)[lr] = expf(gCv);
             sm.eref[lr] = expf(ref);
+            sm.nrl[lr] = -ref * kLog2e;
         } else {
             // (thread = k row, then q row) the norms and beta
             const int r = tid & (C - 1);
@@ -504,60 +515,58 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                 const int c0 = 64 * hf + 8 * u;
                 const uint4 raw = *reinterpret_cast<const uint4 *>(box + tok * 128 + ((u ^ (tok & 7)) << 4));
                 const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-                float x[8], gm[8];
+                float2 x2[4], g2[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 ab = box_pair<FUSED>(w4[e]);
-                    x[2 * e] = ab.x * inv;
-                    x[2 * e + 1] = ab.y * inv;
-                }
+                for (int e = 0; e < 4; ++e) x2[e] = __fmul2_rn(box_pair<FUSED>(w4[e]), make_float2(inv, inv));
                 {
                     const float4 g0 = *reinterpret_cast<const float4 *>(gam + tc::sw128_off(tok, c0, C));
                     const float4 g1 = *reinterpret_cast<const float4 *>(gam + tc::sw128_off(tok, c0 + 4, C));
-                    gm[0] = g0.x; gm[1] = g0.y; gm[2] = g0.z; gm[3] = g0.w;
-                    gm[4] = g1.x; gm[5] = g1.y; gm[6] = g1.z; gm[7] = g1.w;
+                    g2[0] = make_float2(g0.x, g0.y);
+                    g2[1] = make_float2(g0.z, g0.w);
+                    g2[2] = make_float2(g1.x, g1.y);
+                    g2[3] = make_float2(g1.z, g1.w);
                 }
-                float plus[8], qt[8], ei[8];
+                float2 qt2[4];
                 if (!unsafe) {
-                    float rf[8], er[8];
-                    *reinterpret_cast<float4 *>(&rf[0]) = *reinterpret_cast<const float4 *>(&sm.ref[c0]);
-                    *reinterpret_cast<float4 *>(&rf[4]) = *reinterpret_cast<const float4 *>(&sm.ref[c0 + 4]);
-                    *reinterpret_cast<float4 *>(&er[0]) = *reinterpret_cast<const float4 *>(&sm.eref[c0]);
-                    *reinterpret_cast<float4 *>(&er[4]) = *reinterpret_cast<const float4 *>(&sm.eref[c0 + 4]);
+                    // t = (gamma - ref) log2(e): e^{gamma - ref} = 2^t and
+                    // e^{ref - gamma} = 2^-t
+                    const float4 n0 = *reinterpret_cast<const float4 *>(&sm.nrl[c0]);
+                    const float4 n1 = *reinterpret_cast<const float4 *>(&sm.nrl[c0 + 4]);
+                    const float2 nr2[4] = {make_float2(n0.x, n0.y), make_float2(n0.z, n0.w), make_float2(n1.x, n1.y),
+                                           make_float2(n1.z, n1.w)};
+                    float2 t2[4], plus2[4];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float E = __expf(gm[e] - rf[e]);  // e^{gamma - ref}
-                        plus[e] = x[e] * E;
-                        qt[e] = plus[e] * er[e];
+                    for (int e = 0; e < 4; ++e) {
+                        t2[e] = __ffma2_rn(g2[e], make_float2(kLog2e, kLog2e), nr2[e]);
+                        plus2[e] = __fmul2_rn(x2[e], make_float2(ex2_approx(t2[e].x), ex2_approx(t2[e].y)));
                     }
-                    if (!isq) {  // (warp-uniform) K- for the key rows
+                    tc::st8(tc::lane_addr(tm, warp, PT_A + c0), *reinterpret_cast<const float(*)[8]>(&plus2[0]));
+                    if (!isq) {  // (warp-uniform) K- = k^ e^{ref - gamma}
+                        float2 mi2[4];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) ei[e] = __expf(rf[e] - gm[e]);  // e^{ref - gamma}
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        plus[e] = 0.f;
-                        ei[e] = 0.f;
-                        qt[e] = x[e] * expf(gm[e]);
-                    }
-                }
-                if (!unsafe) {
-                    tc::st8(tc::lane_addr(tm, warp, PT_A + c0), plus);  // [K+; Q+] row lr
-                    if (!isq) {
-                        float mi[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) mi[e] = x[e] * ei[e];
+                        for (int e = 0; e < 4; ++e)
+                            mi2[e] = __fmul2_rn(x2[e], make_float2(ex2_approx(-t2[e].x), ex2_approx(-t2[e].y)));
                         *reinterpret_cast<float4 *>(km + tc::sw128_off(tok, c0, C)) =
-                            make_float4(mi[0], mi[1], mi[2], mi[3]);
+                            make_float4(mi2[0].x, mi2[0].y, mi2[1].x, mi2[1].y);
                         *reinterpret_cast<float4 *>(km + tc::sw128_off(tok, c0 + 4, C)) =
-                            make_float4(mi[4], mi[5], mi[6], mi[7]);
+                            make_float4(mi2[2].x, mi2[2].y, mi2[3].x, mi2[3].y);
+                    } else {  // Q~ = q^ e^{gamma} = Q+ e^{ref}
+                        const float4 e0 = *reinterpret_cast<const float4 *>(&sm.eref[c0]);
+                        const float4 e1 = *reinterpret_cast<const float4 *>(&sm.eref[c0 + 4]);
+                        qt2[0] = __fmul2_rn(plus2[0], make_float2(e0.x, e0.y));
+                        qt2[1] = __fmul2_rn(plus2[1], make_float2(e0.z, e0.w));
+                        qt2[2] = __fmul2_rn(plus2[2], make_float2(e1.x, e1.y));
+                        qt2[3] = __fmul2_rn(plus2[3], make_float2(e1.z, e1.w));
                     }
+                } else if (isq) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        qt2[e] = make_float2(x2[e].x * expf(g2[e].x), x2[e].y * expf(g2[e].y));
                 }
-                if (isq)  // Q~ = q^ e^{gamma}: row 128 + tok of [-G^T; Q'] until Q' replaces it
+                if (isq)  // Q~: row 128 + tok of [-G^T; Q'] until Q' replaces it
                     *reinterpret_cast<uint4 *>(img + IMG_BQ + tc::sw128_off16(128 + tok, c0, 192)) =
-                        make_uint4(pack_h2(qt[0], qt[1]), pack_h2(qt[2], qt[3]), pack_h2(qt[4], qt[5]),
-                                   pack_h2(qt[6], qt[7]));
+                        make_uint4(pack_h2(qt2[0].x, qt2[0].y), pack_h2(qt2[1].x, qt2[1].y),
+                                   pack_h2(qt2[2].x, qt2[2].y), pack_h2(qt2[3].x, qt2[3].y));
             }
             // the Q~ rows come back by bulk copy in step 9
             fence_proxy_async_global();
@@ -568,15 +577,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         __syncthreads();
         tc::fence_after_sync();
         if (!unsafe) {
-            if (tid == 0) {
-                // G = [K+; Q+] K-^T: M = 128, N = 64, K = 128 (kind::tf32)
-                constexpr uint32_t id = tc::idesc_tf32(128, 64);
-                const uint32_t b0 = tc::smem_u32(km);
+            if (tid == 0 || tid == 32) {
+                // G = [K+; Q+] K-^T: M = 128, N = 64 tokens j, K = 128
+                // (kind::tf32); threads 0 and 32 issue one 32-token half each
+                constexpr uint32_t id = tc::idesc_tf32(128, 32);
+                const int jh = tid >> 5;
+                const uint32_t b0 = tc::smem_u32(km) + jh * 32 * 128;
 #pragma unroll
                 for (int ks = 0; ks < D / 8; ++ks)
-                    tc::mma_tf32_ts(tm + PT_G, tm + PT_A + 8 * ks, tc::desc_tf32_kstep(b0, 64, ks), id, ks > 0);
+                    tc::mma_tf32_ts(tm + PT_G + 32 * jh, tm + PT_A + 8 * ks, tc::desc_tf32_kstep(b0, 64, ks), id,
+                                    ks > 0);
                 tc::commit(&sm.bar_mma);
-                issue_v();  // q has been read: v takes its buffer
+                if (tid == 0) issue_v();  // q has been read: v takes its buffer
             }
             mma_pend = v_pend = true;
         }
@@ -842,16 +854,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         tc::fence_after_sync();
     }
     if (ok) {
-        // ---- W^T = (beta K~)^T T^T and U'^T = (beta V)^T T^T
-        if (tid == 0) {
+        // ---- W^T = (beta K~)^T T^T (thread 0) and U'^T = (beta V)^T T^T
+        // (thread 32)
+        if (tid == 0 || tid == 32) {
             constexpr uint32_t id = tc::idesc_tf32(128, 64);
             const uint32_t b0 = tc::smem_u32(sm.u2.t);
+            const uint32_t d = tid == 0 ? PT_WT : PT_UPT, a = tid == 0 ? PT_BK : PT_BV;
 #pragma unroll
-            for (int ks = 0; ks < C / 8; ++ks) {
-                const uint64_t bd = tc::desc_tf32_kstep(b0, 64, ks);
-                tc::mma_tf32_ts(tm + PT_WT, tm + PT_BK + 8 * ks, bd, id, ks > 0);
-                tc::mma_tf32_ts(tm + PT_UPT, tm + PT_BV + 8 * ks, bd, id, ks > 0);
-            }
+            for (int ks = 0; ks < C / 8; ++ks)
+                tc::mma_tf32_ts(tm + d, tm + a + 8 * ks, tc::desc_tf32_kstep(b0, 64, ks), id, ks > 0);
             tc::commit(&sm.bar_mma);
         }
         mma_pend = true;
@@ -924,15 +935,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
         }
         tc::fence_after_sync();
-        if (ok && tid == 0) {
+        if (ok && (tid == 0 || tid == 32)) {
+            // G^T (thread 0, columns 0..127) and P W (thread 32, 128..255)
             constexpr uint32_t id = tc::idesc_f16(128, 128);
-            const uint32_t ak = tc::smem_u32(kp), ap = tc::smem_u32(kp + 128 * 128), bw = tc::smem_u32(wt);
+            const uint32_t a0 = tc::smem_u32(tid == 0 ? kp : kp + 128 * 128), bw = tc::smem_u32(wt);
+            const uint32_t d = tid == 0 ? 0u : 128u;
 #pragma unroll
-            for (int ks = 0; ks < C / 16; ++ks) {
-                const uint64_t bd = tc::desc_tf32_kstep(bw, 128, ks);
-                tc::mma_f16_ss(tm + 0, tc::desc_tf32_kstep(ak, 128, ks), bd, id, ks > 0);
-                tc::mma_f16_ss(tm + 128, tc::desc_tf32_kstep(ap, 128, ks), bd, id, ks > 0);
-            }
+            for (int ks = 0; ks < C / 16; ++ks)
+                tc::mma_f16_ss(tm + d, tc::desc_tf32_kstep(a0, 128, ks), tc::desc_tf32_kstep(bw, 128, ks), id, ks > 0);
             tc::commit(&sm.bar_mma);
         }
         mma_pend = ok;
