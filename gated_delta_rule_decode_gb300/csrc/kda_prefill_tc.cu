@@ -171,7 +171,7 @@ constexpr int kPrepThreads = 256;
 // Scratch of the UT inverse, laid over the k staging and the K- tile once the
 // A/P product and the channel phase have read them.
 struct InvScratch {
-    float As[C][C + 1];
+    float As[C][C + 4];  // rows 16-byte aligned; a quarter warp's rows hit distinct banks
     float Ts[C][C + 1];
 };
 
@@ -604,18 +604,23 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             uint32_t kw[16];
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
-                float kh2[2];
-                const float2 ik = *reinterpret_cast<const float2 *>(&sm.invk[32 * hf + i]);
-                const float2 bt = *reinterpret_cast<const float2 *>(&sm.beta[32 * hf + i]);
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int r = 32 * hf + i + e;
-                    const float kx = box_elem<FUSED>(kst, r, lr) * (e ? ik.y : ik.x);
-                    const float g = st_f32(gam, r, lr);
-                    bk[i + e] = (e ? bt.y : bt.x) * kx * __expf(g);
-                    kh2[e] = !unsafe ? st_f32(km, r, lr) * egcref : (r < L ? kx * expf(gCv - g) : 0.f);
-                }
-                kw[i >> 1] = pack_h2(kh2[0], kh2[1]);
+                // tokens r and r + 1 as pairs: beta k^ e^{gamma} = beta k^ 2^{gamma log2(e)}
+                const int r = 32 * hf + i;
+                const float2 ik = *reinterpret_cast<const float2 *>(&sm.invk[r]);
+                const float2 bt = *reinterpret_cast<const float2 *>(&sm.beta[r]);
+                const float2 kx =
+                    __fmul2_rn(make_float2(box_elem<FUSED>(kst, r, lr), box_elem<FUSED>(kst, r + 1, lr)), ik);
+                const float2 g = make_float2(st_f32(gam, r, lr), st_f32(gam, r + 1, lr));
+                const float2 t = __fmul2_rn(g, make_float2(kLog2e, kLog2e));
+                const float2 b2 = __fmul2_rn(__fmul2_rn(bt, kx), make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+                bk[i] = b2.x;
+                bk[i + 1] = b2.y;
+                float2 kh;
+                if (!unsafe)
+                    kh = __fmul2_rn(make_float2(st_f32(km, r, lr), st_f32(km, r + 1, lr)), make_float2(egcref, egcref));
+                else
+                    kh = make_float2(r < L ? kx.x * expf(gCv - g.x) : 0.f, r + 1 < L ? kx.y * expf(gCv - g.y) : 0.f);
+                kw[i >> 1] = pack_h2(kh.x, kh.y);
             }
             tc::st16(tc::lane_addr(tm, warp, PT_BK + 32 * hf), *reinterpret_cast<float(*)[16]>(&bk[0]));
             tc::st16(tc::lane_addr(tm, warp, PT_BK + 32 * hf + 16), *reinterpret_cast<float(*)[16]>(&bk[16]));
@@ -640,9 +645,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                     const int r = lr;
                     const float br = sm.beta[r];
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int j = 32 * hf + jj;
-                        sm.u1.inv.As[r][j] = (j < r) ? br * g32[jj] : 0.f;
+                    for (int j4 = 0; j4 < 32; j4 += 4) {
+                        float a4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = 32 * hf + j4 + e;
+                            a4[e] = (j < r) ? br * g32[j4 + e] : 0.f;
+                        }
+                        *reinterpret_cast<float4 *>(&sm.u1.inv.As[r][32 * hf + j4]) = make_float4(a4[0], a4[1], a4[2], a4[3]);
                     }
                 } else {
                     const int r = lr - C;
@@ -699,7 +709,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         // thread, in registers); then the lower-left 16 x 16 block of each
         // 32-row block as -T22 (A21 T11); then the lower-left 32 x 32 block of
         // the whole matrix the same way
-        float(*As)[C + 1] = sm.u1.inv.As;
+        float(*As)[C + 4] = sm.u1.inv.As;
         float(*Ts)[C + 1] = sm.u1.inv.Ts;
         if (tid < C) {
             const int I = tid >> 4, jj = tid & 15, o = 16 * I;
@@ -797,10 +807,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         ok = __syncthreads_and(tid == 0 ? mbar_wait(&sm.bar_v, 0) : true) != 0;
         if (ok && tid == 0) {
             // [K^^T; P] (this CTA's image rows) back into u1 behind the
-            // coming W^T tile, for the products of step 9; the inverse's
-            // scratch there has been read
-            mbar_arrive_expect_tx(&sm.bar_kp, 192 * 64 * 2);
-            bulk_g2s(reinterpret_cast<unsigned char *>(&sm.u1) + 128 * 64 * 2, img + IMG_KP, 192 * 64 * 2, &sm.bar_kp);
+            // coming W^T tile, and a second copy of P behind them, for the
+            // products of step 9; the inverse's scratch there has been read
+            unsigned char *kp = reinterpret_cast<unsigned char *>(&sm.u1) + 128 * 64 * 2;
+            mbar_arrive_expect_tx(&sm.bar_kp, 256 * 64 * 2);
+            bulk_g2s(kp, img + IMG_KP, 192 * 64 * 2, &sm.bar_kp);
+            bulk_g2s(kp + 192 * 128, img + IMG_KP + 128 * 128, 64 * 64 * 2, &sm.bar_kp);
         }
         kp_pend = ok;
         if (ok) {
@@ -810,13 +822,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             if constexpr (!FUSED) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
-                    const float4 b4 = *reinterpret_cast<const float4 *>(&sm.beta[32 * hf + i]);
-                    const float bb4[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int r = 32 * hf + i + e;
-                        bv[i + e] = r < L ? bb4[e] * st_bf16(qv, r, lr) : 0.f;
-                    }
+                    const int r = 32 * hf + i;
+                    const float4 b4 = *reinterpret_cast<const float4 *>(&sm.beta[r]);
+                    const float2 lo = __fmul2_rn(make_float2(b4.x, b4.y),
+                                                 make_float2(st_bf16(qv, r, lr), st_bf16(qv, r + 1, lr)));
+                    const float2 hi = __fmul2_rn(make_float2(b4.z, b4.w),
+                                                 make_float2(st_bf16(qv, r + 2, lr), st_bf16(qv, r + 3, lr)));
+                    bv[i] = r < L ? lo.x : 0.f;
+                    bv[i + 1] = r + 1 < L ? lo.y : 0.f;
+                    bv[i + 2] = r + 2 < L ? hi.x : 0.f;
+                    bv[i + 3] = r + 3 < L ? hi.y : 0.f;
                 }
             } else {
                 // ShortConv of value channel lr on the fly (fp32), the three
@@ -901,12 +916,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
     }
     if (ok) {
         // ---- 9. the state-independent products of the chain step:
-        // G^T = K^^T W (M = 128 key rows, N = 128 keys) and P W (M = 128, of
-        // which rows 0..63 are P's; N = 128 keys), kind::f16, K = 64 tokens.
+        // G^T = K^^T W (M = 128 key rows, N = 128 keys) and P W (M = 128:
+        // P's 64 rows twice; N = 128 keys), kind::f16, K = 64 tokens.
         // [K^^T; P] came back from the image (this CTA's own writes) into
         // the shared memory behind the W^T tile by a bulk copy issued in
-        // step 7; the A tile of P W spans
-        // 64 rows past P, whose products land in TMEM lanes nobody reads.
+        // step 7, and a second copy of P behind it, so that TMEM lanes
+        // 64..127 hold P W again and every warp takes part in Q'.
         unsigned char *wt = reinterpret_cast<unsigned char *>(&sm.u1);
         unsigned char *kp = wt + 128 * 64 * 2;
         static_assert(128 * 64 * 2 + 2 * 128 * 64 * 2 <= sizeof(sm.u1), "W^T and the [K^^T; P] A tiles fit u1");
@@ -971,8 +986,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                         make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
-            // Q' = Q~ - P W: row 128 + lr of the tile, lanes 0..63 (Q~ from
-            // its staged copy: row lr of the 64-row run of column block hf)
+            // Q' = Q~ - P W: row 128 + rq of the tile; lanes 0..63 take keys
+            // 0..31 of column block hf, lanes 64..127 (the second copy of
+            // P W) keys 32..63 (Q~ from its staged copy: row rq of the 64-row
+            // run of column block hf)
             ok = __syncthreads_and(tid == 0 ? mbar_wait(&sm.bar_q, 0) : true) != 0;
             if (ok) {
                 q_pend = false;
@@ -980,17 +997,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             } else if (tid == 0 && p.err_flag) {
                 atomicOr(p.err_flag, KDA_DEVERR_TIMEOUT);
             }
-            if (ok && lr < C) {
+            if (ok) {
+                const int rq = lr & (C - 1), c32 = 32 * (lr >> 6);
 #pragma unroll
-                for (int j0 = 0; j0 < 64; j0 += 16) {
+                for (int j0 = c32; j0 < c32 + 32; j0 += 16) {
                     float pw16[16];
                     tc::ld16(tc::lane_addr(tm, warp, 128 + 64 * hf + j0), pw16);
                     tc::wait_ld();
 #pragma unroll
                     for (int q8 = 0; q8 < 16; q8 += 8) {
                         const int u = (j0 + q8) >> 3;
-                        const uint4 qt = *reinterpret_cast<const uint4 *>(qs + hf * C * 128 + lr * 128 +
-                                                                          ((u ^ (lr & 7)) << 4));
+                        const uint4 qt = *reinterpret_cast<const uint4 *>(qs + hf * C * 128 + rq * 128 +
+                                                                          ((u ^ (rq & 7)) << 4));
                         const uint32_t qw[4] = {qt.x, qt.y, qt.z, qt.w};
                         uint32_t w[4];
 #pragma unroll
@@ -999,7 +1017,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                             const float a0 = qf.x - pw16[q8 + 2 * e], a1 = qf.y - pw16[q8 + 2 * e + 1];
                             w[e] = pack_h2_track(a0, a1, hmax);
                         }
-                        *reinterpret_cast<uint4 *>(bq + tc::sw128_off16(128 + lr, 64 * hf + j0 + q8, 192)) =
+                        *reinterpret_cast<uint4 *>(bq + tc::sw128_off16(128 + rq, 64 * hf + j0 + q8, 192)) =
                             make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
