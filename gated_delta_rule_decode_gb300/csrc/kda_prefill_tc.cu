@@ -46,6 +46,7 @@
 #include <stdint.h>
 
 #include <climits>
+#include <cmath>
 
 #include "kda.h"
 #include "kda_bulk.cuh"
@@ -302,20 +303,24 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
     // the chunk: seg_len > 0 maps CTA x to local chunk seg_lo + x % seg_len
     // of sequence x / seg_len; seg_len = 0 maps it to global chunk x, taken
     // only from local chunk seg_lo on
+    auto map_chunk = [&](int x, int &sq, int32_t &ch) {
+        if (seg_len > 0) {
+            sq = x / seg_len;
+            if (sq >= n) return false;
+            const int32_t local = seg_lo + (int32_t)(x % seg_len);
+            if (local >= plan[sq + 1] - plan[sq]) return false;
+            ch = plan[sq] + local;
+        } else {
+            ch = x;
+            if (ch >= plan[n]) return false;
+            sq = find_seq(plan, n, ch);
+            if (ch - plan[sq] < seg_lo) return false;
+        }
+        return true;
+    };
     int32_t chunk;
     int s;
-    if (seg_len > 0) {
-        s = (int)(blockIdx.x / seg_len);
-        if (s >= n) return leave();
-        const int32_t local = seg_lo + (int32_t)(blockIdx.x % seg_len);
-        if (local >= plan[s + 1] - plan[s]) return leave();
-        chunk = plan[s] + local;
-    } else {
-        chunk = blockIdx.x;
-        if (chunk >= plan[n]) return leave();
-        s = find_seq(plan, n, chunk);
-        if (chunk - plan[s] < seg_lo) return leave();
-    }
+    if (!map_chunk((int)blockIdx.x, s, chunk)) return leave();
     const int h = blockIdx.y, H = p.H;
     const int slot = p.slot_ids[s];
     if (slot < 0 || (int64_t)slot >= p.num_slots) return leave();  // the chain writes zeros
@@ -434,7 +439,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             const int row = tid & 127, ch = tid >> 7;
             const int r = row & 63;
             const unsigned char *box = (row < 64 ? kst : qv) + ch * C * 128;
-            float ss = 0.f;
+            float2 ss = make_float2(0.f, 0.f);
             if (r < L) {
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -443,12 +448,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 ab = box_pair<FUSED>(w4[e]);
-                        ss = fmaf(ab.x, ab.x, ss);
-                        ss = fmaf(ab.y, ab.y, ss);
+                        ss = __ffma2_rn(ab, ab, ss);
                     }
                 }
             }
-            sm.nrm[ch][row] = ss;
+            sm.nrm[ch][row] = ss.x + ss.y;
         }
         // ---- 2. gamma, in place (thread = channel lr): both token halves'
         // running sums at once, from zero; the first ends at ref = gamma_31,
@@ -1478,18 +1482,46 @@ size_t prefill_tc_workspace_bytes(int H, int32_t num_seqs, int64_t total_tokens)
     return plan_bytes(num_seqs) + (size_t)max_chunks(num_seqs, total_tokens) * (size_t)H * IMG_BYTES;
 }
 
-// Segments of a pipelined prefill (see launch_prefill_tc): a prep CTA lives
-// tens of microseconds, so a segment's prep grid must span several waves
-// (at least kSegMinCtas CTAs) for its tail to stay small, and a segment holds
-// at least kSegMinChunks chunks of each sequence.
-constexpr int kSegMinCtas = 2048;
-#ifndef KDA_SEG_FIRST_PCT
-#define KDA_SEG_FIRST_PCT 72
-#endif
-constexpr int kSegMinChunks = 64;
-// Measured at 102 400 tokens x 32 heads: 7 segments (25) took 4.90 ms, 12
-// segments (10) 4.96 ms, 5 (40) 4.94 ms, 3 (100) 4.98 ms, one 6.21 ms.
-constexpr int64_t kSegTailChunks = 25;
+// Segments of a pipelined prefill (see launch_tc).  Segment k + 1's prep
+// runs on the SMs that segment k's chains leave free and should take about
+// as long as those chains, so segment lengths form a geometric series of
+// ratio rho = (a chain step) / (a chunk's prep for every chain on the free
+// SMs).  A prep CTA lives about 12 chain steps at two CTAs per SM, so
+// rho = kSegRatioScale x free SMs / chains (0.6 at 32 chains; below 1 the
+// segments shrink, above it they grow).  Segments hold at least
+// max(16, chunks / 50) chunks and 256 prep CTAs.  Measured at 32 heads,
+// against equal segments: 8192 tokens 65 / 39 / 24 chunks, 438.7 us against
+// 444.6 us; 102 400 tokens six segments from 671 chunks down to 52, 4.22 ms
+// against 4.44 ms (the minimum of 16 chunks there: 4.27 ms).
+constexpr double kSegRatioScale = 0.16;
+constexpr int kMaxSegments = 64;
+
+// Local chunk indices where segments start (lo[0] = 0); returns the segment
+// count (1: no pipelining).  chains = sequences x heads; per_seq = mean
+// chunks per sequence.
+static int plan_segments(int64_t chains, int sms, int64_t per_seq, int (&lo)[kMaxSegments + 1]) {
+    lo[0] = 0;
+    if (chains <= 0 || chains >= sms || per_seq < 2) return 1;
+    const double rho = kSegRatioScale * (double)(sms - chains) / (double)chains;
+    const double P = (double)per_seq;
+    double m = per_seq / 50 > 16 ? (double)(per_seq / 50) : 16.0;
+    if ((double)((256 + chains - 1) / chains) > m) m = (double)((256 + chains - 1) / chains);
+    auto first = [&](int k) {  // first length of k segments summing to P
+        return std::fabs(rho - 1.0) < 1e-9 ? P / k : P * (1.0 - rho) / (1.0 - std::pow(rho, k));
+    };
+    int K = 1;
+    for (int k = 2; k <= kMaxSegments; ++k) {
+        const double n0 = first(k), nl = n0 * std::pow(rho, k - 1);
+        if ((n0 < nl ? n0 : nl) >= m) K = k; else break;
+    }
+    const double n0 = first(K);
+    double acc = 0.0;
+    for (int k = 1; k < K; ++k) {
+        acc += n0 * std::pow(rho, k - 1);
+        lo[k] = (int)(acc + 0.5);
+    }
+    return K;
+}
 
 template <bool FUSED>
 static cudaError_t launch_tc(const PrefillParams &p, cudaStream_t st) {
@@ -1537,8 +1569,7 @@ static cudaError_t launch_tc(const PrefillParams &p, cudaStream_t st) {
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
     // Pipelining: when few (sequence, head) chains would walk many chunks
-    // each, the chunks are cut into segments of seg_chunks local chunks.
-    // Segment k's prep runs beside segment k - 1's chain (programmatic
+    // each, the chunks are cut into segments (plan_segments).  Segment k's prep runs beside segment k - 1's chain (programmatic
     // dependent launch: the chain lets it start at once; one of its CTAs
     // waits for that chain before the grid ends), and segment k's chain, an
     // ordinary launch, follows its prep and so the previous chain.  The last
@@ -1547,40 +1578,16 @@ static cudaError_t launch_tc(const PrefillParams &p, cudaStream_t st) {
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                   cudaSuccess)
         sms = 1;
-    int nseg = 1, seg_chunks = 0;
-    if (any && p.num_seqs > 0 && (int64_t)p.num_seqs * p.H <= (int64_t)sms) {
-        const int64_t per_seq = (p.total_tokens + C - 1) / C / p.num_seqs;  // mean chunks per sequence
-        // about sqrt(per_seq / kSegTailChunks) segments balance the exposed
-        // last chain (per_seq / K chunk steps) against what each segment
-        // boundary costs (a prep grid's tail, about kSegTailChunks chunk steps)
-        int64_t kopt = 1;
-        while ((kopt + 1) * (kopt + 1) * kSegTailChunks <= per_seq) ++kopt;
-        const int64_t ctas_per_chunk = (int64_t)p.num_seqs * p.H;
-        int64_t len = (kSegMinCtas + ctas_per_chunk - 1) / ctas_per_chunk;
-        if (len < kSegMinChunks) len = kSegMinChunks;
-        if (len < (per_seq + kopt - 1) / kopt) len = (per_seq + kopt - 1) / kopt;
-        const int64_t k = (per_seq + len - 1) / len;
-        if (k >= 2) {
-            nseg = k > 256 ? 256 : (int)k;
-            seg_chunks = (int)len;
-        }
-    }
-    // With two segments the first is made larger (KDA_SEG_FIRST_PCT percent
-    // of the mean chunks per sequence): the second prep then runs on the SMs
-    // the first chain leaves free for about as long as that chain, and the
-    // exposed second chain is shorter.  72 % measured best at 8192 tokens x 32
-    // heads (507 us, against 550 us for halves and 521 us for 66 % or 78 %).
-    int first_len = seg_chunks;
-    if (nseg == 2) {
-        const int64_t per_seq = (p.total_tokens + C - 1) / C / p.num_seqs;
-        const int64_t f = per_seq * KDA_SEG_FIRST_PCT / 100;
-        if (f > first_len && f < per_seq) first_len = (int)f;
-    }
+    int lo_k[kMaxSegments + 1];
+    const int nseg = any && p.num_seqs > 0
+                         ? plan_segments((int64_t)p.num_seqs * p.H, sms, (p.total_tokens + C - 1) / C / p.num_seqs, lo_k)
+                         : 1;
+    lo_k[0] = 0;
     const dim3 cgrid((unsigned)p.num_seqs, (unsigned)p.H);
     for (int k = 0; k < nseg; ++k) {
         const bool last = k == nseg - 1;
-        const int lo = k == 0 ? 0 : first_len + (k - 1) * seg_chunks;
-        const int len = k == 0 ? first_len : seg_chunks;
+        const int lo = lo_k[k];
+        const int len = last ? 0 : lo_k[k + 1] - lo_k[k];
         if (any) {
             const int seg_len = last ? 0 : len;
             const int64_t gx = last ? mc : (int64_t)p.num_seqs * len;

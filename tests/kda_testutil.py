@@ -40,3 +40,33 @@ def assert_close(got, ref, atol, rtol, what=""):
 
 def err_flag(device="cuda"):
     return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def segment_starts(chains: int, sms: int, per_seq: int) -> list[int]:
+    """Local chunk indices where the pipelined tensor-core prefill starts its
+    segments, by the library's rule (restated here so that tests can put
+    snapshot requests on segment boundaries): a geometric series of ratio
+    rho = 0.16 x (sms - chains) / chains summing to the mean chunks per
+    sequence, each segment at least max(16, per_seq // 50) chunks and 256
+    prep CTAs, as many segments as that allows (at most 64)."""
+    lo = [0]
+    if chains <= 0 or chains >= sms or per_seq < 2:
+        return lo
+    rho = 0.16 * (sms - chains) / chains
+    m = max(16.0, float(per_seq // 50), float((256 + chains - 1) // chains))
+
+    def first(k):
+        return per_seq / k if abs(rho - 1.0) < 1e-9 else per_seq * (1.0 - rho) / (1.0 - rho ** k)
+
+    K = 1
+    for k in range(2, 65):
+        n0 = first(k)
+        if min(n0, n0 * rho ** (k - 1)) >= m:
+            K = k
+        else:
+            break
+    acc = 0.0
+    for k in range(1, K):
+        acc += first(K) * rho ** (k - 1)
+        lo.append(int(acc + 0.5))
+    return lo

@@ -102,8 +102,9 @@ def test_fused_prefill_then_fused_decode():
 
 def test_fused_prefill_pipelined_segments():
     """One sequence of 3 x 8192 + 337 tokens x 16 heads, which the library
-    pipelines in four segments: the conv history crosses chunk and segment
-    boundaries and the conv state is written by the last segment's chain."""
+    pipelines in seven growing segments: the conv history crosses chunk and
+    segment boundaries and the conv state is written by the last segment's
+    chain."""
     lens = [3 * 8192 + 337]
     x, ex, pool, cst, out, o_ref, p_ref, c_ref = _run(lens, [0], 16, 2, 54, True)
     atol, rtol = tol_for(torch.bfloat16)

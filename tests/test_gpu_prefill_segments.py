@@ -1,18 +1,18 @@
 """GPU parity of the pipelined tensor-core prefill: when a few (sequence,
 head) chains each walk many chunks, the chunks are cut into segments and
-segment k's prep runs beside segment k - 1's chain.  The library takes about
-sqrt(mean chunks per sequence / 10) segments (rounded up after the length
-is fixed), each of at least 64 chunks and at least 2048 prep CTAs, when
-(sequences x heads) is at most the SM count; the last segment takes the
-rest.  These batches take that path (5 and 4 segments); outputs, final
-states and snapshots on both sides of segment boundaries are compared with
-the fp64 oracle."""
+segment k's prep runs beside segment k - 1's chain.  The library sizes the
+segments as a geometric series (ratio 0.16 x free SMs / chains, at least
+16 chunks, chunks / 50 and 256 prep CTAs each) when (sequences x heads) is
+below the SM count; the last segment takes the rest.  These batches take
+that path with shrinking (32 chains) and growing (8 and 16 chains)
+segments; outputs, final states and snapshots on both sides of segment
+boundaries are compared with the fp64 oracle."""
 import pytest
 import torch
 
 import oracle
 from gated_delta_rule_decode_gb300 import inputs
-from kda_testutil import assert_close, err_flag, round_to, to_np64, tol_for
+from kda_testutil import assert_close, err_flag, round_to, segment_starts, to_np64, tol_for
 
 pytestmark = pytest.mark.gpu
 
@@ -55,35 +55,46 @@ def _run(lens, slots, H, reqs, num_slots, seed):
     return x, pool, out
 
 
-def test_five_segments_mixed_batch():
+def _starts(lens, H):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    per_seq = (sum(lens) + 63) // 64 // len(lens)
+    return segment_starts(len(lens) * H, sms, per_seq)
+
+
+def test_segments_mixed_batch():
     """Five sequences (60000, 26000, 100, 0 and 300 tokens; the third is
-    padding) x 8 heads: 1350 chunks, 270 per sequence on average, so five
-    segments of 64 chunks (the last takes the rest); the short sequences lie
-    in the first only.  Snapshots at a segment boundary (4096 tokens), one
-    chunk past it and deep in the last segment."""
-    seg = 64 * 64
+    padding) x 8 heads: 1350 chunks, 270 per sequence on average, in growing
+    segments; the short sequences lie in the first only.  Snapshots at the
+    second segment's start, one chunk past it and deep in the last
+    segment."""
     lens = [60000, 26000, 100, 0, 300]
+    lo = _starts(lens, 8)
+    assert len(lo) >= 3, lo
+    b = lo[1] * 64
     slots = [0, 1, -1, 2, 3]
-    reqs = [(0, seg, 4), (0, seg + 64, 5), (1, 25600, 6), (4, 256, 7)]
+    reqs = [(0, b, 4), (0, b + 64, 5), (1, 25600, 6), (4, 256, 7)]
     x, pool, out = _run(lens, slots, 8, reqs, num_slots=9, seed=41)
     cu = x.cu_seqlens.tolist()
     assert torch.all(out[cu[2]:cu[3]] == 0)          # padding sequence: zero outputs
     assert torch.equal(pool[8].cpu(), x.pool[8])     # a slot nobody names keeps its bits
 
 
-def test_four_segments_one_sequence():
-    """One sequence of 3 x 8192 + 337 tokens x 16 heads (390 chunks): three
-    segments of 128 chunks and a last one of 6 ending in a partial chunk;
-    snapshots at two segment boundaries and at the last whole chunk."""
-    seg = 128 * 64
-    T = 3 * seg + 337
-    reqs = [(0, seg, 1), (0, 2 * seg, 2), (0, 3 * seg + 320, 3)]
+def test_growing_segments_one_sequence():
+    """One sequence of 3 x 8192 + 337 tokens x 16 heads (390 chunks, the last
+    partial): growing segments; snapshots at two segment boundaries and at
+    the last whole chunk."""
+    T = 3 * 8192 + 337
+    lo = _starts([T], 16)
+    assert len(lo) >= 4, lo
+    reqs = [(0, lo[1] * 64, 1), (0, lo[-1] * 64, 2), (0, 3 * 8192 + 320, 3)]
     _run([T], [0], 16, reqs, num_slots=4, seed=42)
 
 
-def test_two_uneven_segments_one_sequence():
+def test_shrinking_segments_one_sequence():
     """One sequence of 8172 tokens x 32 heads (128 chunks, the last partial):
-    two segments, the first holding 72 % of the chunks (92).  Snapshots at
-    the boundary, one chunk past it and at the last whole chunk."""
-    reqs = [(0, 92 * 64, 1), (0, 93 * 64, 2), (0, 127 * 64, 3)]
-    _run([8172], [0], 32, reqs, num_slots=4, seed=43)
+    shrinking segments.  Snapshots at the first boundary, one chunk past it,
+    at the last boundary and at the last whole chunk."""
+    lo = _starts([8172], 32)
+    assert len(lo) >= 3, lo
+    reqs = [(0, lo[1] * 64, 1), (0, lo[1] * 64 + 64, 2), (0, lo[-1] * 64, 3), (0, 127 * 64, 4)]
+    _run([8172], [0], 32, reqs, num_slots=5, seed=43)
