@@ -11,24 +11,29 @@
 //   U^T = U'^T - S W^T,  O^T = scale (S Q~^T + U^T P^T),
 //   S <- S diag(e^{gamma_C}) + U^T K^                            (chunk step)
 //
-// Two kernels on tcgen05 (fp32 accumulate):
+// The chunk step splits into what the state does not touch and one product
+// of the state (G = W^T K^, Q' = Q~ - P W):
 //
-// prep_tc_kernel  one CTA per (chunk, head), all chunks of all sequences in
-//   parallel over the whole GPU.  Computes everything that does not depend on
-//   the state (A/P on kind::tf32, the WY factors on kind::tf32) and writes,
-//   per (chunk, head), an operand image that the chain kernel copies into
-//   shared memory with two bulk copies:
-//     [W; Q~] (128 x 128), P (64 x 64) and K^^T (128 x 64) as K-major
-//     128B-swizzled fp16 tiles, e^{gamma_C} (128 fp32) and U'^T (128 x 64 fp32,
-//     each row's 16-byte units swizzled).
+//   D = U'^T K^ - S G,  O^T = scale (S Q'^T + U'^T P^T),
+//   S <- S diag(e^{gamma_C}) + D
+//
+// Two kernels on tcgen05 (fp32 accumulate), pipelined in segments of the
+// chunks (plan_segments):
+//
+// prep_tc_kernel  one CTA per (chunk, head), the chunks of a segment of all
+//   sequences in parallel.  Computes everything that does not depend on the
+//   state (A/P and the WY factors on kind::tf32, G^T and P W on kind::f16)
+//   and writes, per (chunk, head), an operand image that the chain copies
+//   into shared memory with one bulk copy: [-G^T; Q'] (192 x 128 keys),
+//   U'^T (128 x 64 tokens) and [K^^T; P] (192 x 64 tokens) as K-major
+//   128B-swizzled fp16 tiles, then e^{gamma_C} (128 fp32).
 // chain_kernel  one CTA per (sequence, head) walks the chunks in order with
-//   the state in tensor memory (value row i = TMEM lane i), so the state is
-//   the A operand of the chunk step's products and never leaves the SM:
-//     X = S [W; Q~]^T,  U^T = U'^T - X[:, :64],  S <- S diag(e^{gamma_C}),
-//     S += U^T K^,  O^T = scale (X[:, 64:] + U^T P^T)
-//   all on kind::f16.  The next chunk's operand images are in flight while a
-//   chunk computes, and a chunk's outputs are written while the next chunk's
-//   first product runs.
+//   the fp32 state in registers and its fp16 copy S16 in tensor memory
+//   (value row i = TMEM lane i), the A operand of the one state product:
+//     ACC = U'^T [K^^T; P]^T + S16 [-G^T; Q']^T = [D | O^T]     (N = 192)
+//   on kind::f16.  The first product is issued for the next chunk while the
+//   state of this one is updated; the next chunks' images are in flight, and
+//   a chunk's outputs leave while the next chunk's product runs.
 //
 // Operand precision of the chain: fp16 has the same 10-bit mantissa as tf32
 // and rounds to nearest; the operands (normalised keys and queries times
@@ -152,9 +157,10 @@ __device__ inline int find_seq(const int32_t *plan, int n, int32_t c) {
 // The chunk's k, q and g arrive by TMA as K-major 128B-swizzled boxes (the
 // layout of an MMA operand tile, so both row and column reads are free of
 // bank conflicts); v follows into q's buffer once q has been used.  Steps:
-//   1. gamma = running sum of g per channel, in place (first token half, then
-//      the second continuing from gamma_31 = ref); span check
-//   2. L2Norm sums of squares per token row
+//   0. (fused prefill) ShortConv of k and q in place in their boxes
+//   1. L2Norm sums of squares per token row
+//   2. gamma = running sum of g per channel, in place (both token halves at
+//      once; the second adds gamma_31 = ref); span check; norms and beta
 //   3. row phase: [K+; Q+] into TMEM (the A operand of the A/P product),
 //      K- into a shared tile (its B operand), Q~ rows of the image
 //   4. channel phase, while G = [K+; Q+] K-^T runs: beta K~^T into TMEM (the
@@ -162,9 +168,13 @@ __device__ inline int find_seq(const int32_t *plan, int n, int32_t c) {
 //   5. A' and P from G; P rows of the image
 //   6. T = (I + A)^-1 by doubling
 //   7. beta V^T into TMEM; W^T = (beta K~)^T T^T, U'^T = (beta V)^T T^T
-//   8. W rows and U'^T rows of the image
+//   8. W^T into a shared tile, U'^T rows of the image (one bulk store)
+//   9. G^T = K^^T W and P W (kind::f16, [K^^T; P] read back from the
+//      image); [-G^T; Q'] rows of the image (one bulk store)
+// Independent products are issued from two threads (0 and 32).
 // TMEM columns: [K+; Q+] 0..127 (then beta V^T 0..63 and W^T 64..127),
-// G 128..191 (then U'^T), beta K~^T 192..255.
+// G 128..191 (then U'^T), beta K~^T 192..255; step 9's G^T 0..127 and
+// P W 128..255.
 constexpr uint32_t PT_A = 0, PT_BV = 0, PT_WT = 64, PT_G = 128, PT_UPT = 128, PT_BK = 192;
 constexpr uint32_t PT_COLS = 256;
 constexpr int kPrepThreads = 256;
