@@ -364,7 +364,37 @@ static cudaError_t launch_replay_t(const ReplayParams &p, cudaStream_t st) {
 }
 
 cudaError_t launch_verify(const VerifyParams &p, int dk, int dtype, cudaStream_t st) {
-    if (verify_tc_supported(p, dk, dtype)) return launch_verify_tc(p, st);
+    if (verify_tc_supported(p, dk, dtype)) {
+        if (p.prev_accepted == nullptr) return launch_verify_tc(p, st);
+        // A commit before the verify on the tensor-core shape: the commit's
+        // own launch (replay_u_kernel), then the verify from the committed
+        // state, in stream order.  One launch doing both (the state kernel
+        // committing its staged tile, storing it back and then verifying)
+        // was slower, 174 us against 157 us at 128 x 7 x 32 heads: with the
+        // previous window's staging it held two CTAs per SM instead of three
+        // and ran its stages one after another.  Running the commit beside
+        // the window kernel (which does not read the state) took 162 us.
+        ReplayParams r{};
+        r.rec_k_hat = p.prev_k_hat;
+        r.rec_g = p.prev_g;
+        r.rec_u = p.prev_u;
+        r.num_accepted = p.prev_accepted;
+        r.slot_ids = p.slot_ids;
+        r.pool = const_cast<float *>(p.pool);
+        r.num_slots = p.num_slots;
+        r.err_flag = p.err_flag;
+        r.batch = p.batch;
+        r.D = p.prev_D;
+        r.H = p.H;
+        r.dv = p.dv;
+        const cudaError_t e = launch_replay_u(r, dk, st);
+        if (e != cudaSuccess) return e;
+        VerifyParams v = p;
+        v.prev_k_hat = v.prev_g = v.prev_u = nullptr;
+        v.prev_accepted = nullptr;
+        v.prev_D = 0;
+        return launch_verify_tc(v, st);
+    }
     if (dtype == KDA_DT_BF16) {
         if (dk == 128) return launch_verify_t<128, __nv_bfloat16>(p, st);
         if (dk == 64) return launch_verify_t<64, __nv_bfloat16>(p, st);

@@ -35,7 +35,6 @@
 // below 1e-30 in some channel takes the running products instead (the window
 // kernel forms a_jm and p_jm itself and flags the record).
 #include <cudaTypedefs.h>
-#include <type_traits>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -87,14 +86,6 @@ static_assert(offsetof(StateSmem, flag) - offsetof(StateSmem, kq) == kOffFlag, "
 static_assert(offsetof(StateSmem, rbar) - offsetof(StateSmem, kq) >= kCopyBytes, "record layout");
 constexpr size_t kStateSmemBytes = sizeof(StateSmem) + 1024;  // + alignment of the swizzled tiles
 
-// The fused commit's staging: alpha = exp(g) and k^ of the previous window's
-// accepted records (appended, so the record layout above is unchanged).
-struct StateSmemFused : StateSmem {
-    float pa[kDraft][DK];
-    float pk[kDraft][DK];
-};
-constexpr size_t kStateSmemFusedBytes = sizeof(StateSmemFused) + 1024;
-
 __device__ __forceinline__ uint64_t evict_first_policy() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -108,13 +99,6 @@ __device__ __forceinline__ void tma_load_3d_ef(void *dst, const CUtensorMap *map
         "%3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "l"(pol)
         : "memory");
-}
-
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z, const void *src) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y), "r"(z), "r"(smem_addr(src))
-                 : "memory");
 }
 
 __device__ __forceinline__ void bulk_g2s_ef(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol) {
@@ -291,13 +275,12 @@ __global__ void __launch_bounds__(kWinThreads) window_kernel(const VerifyParams 
     if (tid == 0) *reinterpret_cast<int *>(rec + kOffFlag) = slow ? 1 : 0;
 }
 
-template <typename T, bool FUSED>
+template <typename T>
 __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyParams p,
                                                                const __grid_constant__ CUtensorMap smap,
                                                                const unsigned char *ws) {
     extern __shared__ unsigned char smem_raw[];
-    using Smem = typename std::conditional<FUSED, StateSmemFused, StateSmem>::type;
-    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    StateSmem &sm = *reinterpret_cast<StateSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int sh = blockIdx.x;
     const int h = sh % p.H, n = sh / p.H;
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -355,38 +338,12 @@ __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyPar
             set_ones<DK>(kb[r]);
         }
     }
-    // fused commit: the previous window's accepted prefix (thread tid stages
-    // channel tid of each record's alpha and k^)
-    int ca = 0;
-    float pg[kDraft], pkv[kDraft], uj[kDraft];
-    if constexpr (FUSED) {
-        ca = __ldg(p.prev_accepted + n);
-        if (ca < 0 || ca > p.prev_D) {
-            if (tid == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_ACCEPTED);
-            ca = 0;
-        }
-        if (!valid) ca = 0;
-        // loads first; shared stores once the value loads below are out
-#pragma unroll
-        for (int j = 0; j < kDraft; ++j) {
-            const int64_t tk = ((int64_t)n * p.prev_D + j) * p.H + h;
-            pg[j] = j < ca ? __ldg(p.prev_g + tk * DK + tid) : 0.f;
-            pkv[j] = j < ca ? __ldg(p.prev_k_hat + tk * DK + tid) : 0.f;
-            uj[j] = j < ca ? __ldg(p.prev_u + tk * p.dv + tid) : 0.f;
-        }
-    }
     // this thread's state row: its value entries
     float vr[kDraft];
     {
         const T *vb = static_cast<const T *>(p.v) + ((int64_t)n * D * p.H + h) * p.dv + tid;
 #pragma unroll
         for (int j = 0; j < kDraft; ++j) vr[j] = j < D ? Elem<T>::load1(vb + (int64_t)j * p.H * p.dv) : 0.f;
-    }
-    if constexpr (FUSED) {
-        for (int j = 0; j < ca; ++j) {
-            sm.pa[j][tid] = expf(pg[j]);
-            sm.pk[j][tid] = pkv[j];
-        }
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -423,38 +380,6 @@ __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyPar
             }
         }
         if (ok) ok = __syncthreads_and(mbar_wait(&sm.sbar, 0)) != 0;
-        if constexpr (FUSED) {
-            // thread tid = state row tid: S <- S diag(alpha_j) + u_j k^_j for
-            // the accepted records, in the swizzled tile, then back to the pool
-            if (ok && ca > 0) {
-#pragma unroll 4
-                for (int q = 0; q < DK / 4; ++q) {
-                    float4 *cell = reinterpret_cast<float4 *>(&sm.st[q >> 3][0] + tid * 128 + (((q & 7) ^ (tid & 7)) << 4));
-                    float4 x = *cell;
-#pragma unroll
-                    for (int j = 0; j < kDraft; ++j) {
-                        if (j < ca) {
-                            const float4 a4 = *reinterpret_cast<const float4 *>(&sm.pa[j][4 * q]);
-                            const float4 k4 = *reinterpret_cast<const float4 *>(&sm.pk[j][4 * q]);
-                            x.x = __fmaf_rn(uj[j], k4.x, __fmul_rn(x.x, a4.x));
-                            x.y = __fmaf_rn(uj[j], k4.y, __fmul_rn(x.y, a4.y));
-                            x.z = __fmaf_rn(uj[j], k4.z, __fmul_rn(x.z, a4.z));
-                            x.w = __fmaf_rn(uj[j], k4.w, __fmul_rn(x.w, a4.w));
-                        }
-                    }
-                    *cell = x;
-                }
-                fence_proxy_async_smem();  // the product and the tensor stores read the committed tile
-            }
-            __syncthreads();
-            // the committed state back to the pool: four tensor stores through
-            // the load's map (the fused call's pool is written)
-            if (ok && ca > 0 && tid == 0) {
-#pragma unroll
-                for (int a4 = 0; a4 < 4; ++a4) tma_store_3d(&smap, 32 * a4, 0, slot * p.H + h, sm.st[a4]);
-                bulk_commit();
-            }
-        }
         // every read of the scratch record is complete: drop its lines from L2
         // without writing them back
         if (ok && warp == 1)
@@ -514,9 +439,6 @@ __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyPar
                 if (j < D) __stcs(ub + (int64_t)j * p.H * p.dv, (valid && ok) ? uu[j] : 0.f);
         }
     }
-    if constexpr (FUSED) {
-        if (tid == 0) bulk_wait_all();  // the committed state's stores are complete
-    }
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tm, kTmemCols);
@@ -548,7 +470,6 @@ size_t verify_workspace_bytes(int H, int dk, int dv, int dtype, int64_t batch, i
 
 bool verify_tc_supported(const VerifyParams &p, int dk, int dtype) {
     return verify_workspace_bytes(p.H, dk, p.dv, dtype, p.batch, p.D) > 0 && p.workspace != nullptr &&
-           (p.prev_accepted == nullptr || p.prev_D <= verify_tc::kDraft) &&
            p.num_slots > 0 && p.num_slots * (int64_t)p.H <= 0x7fffffffLL &&
            (int64_t)p.batch * p.H <= 0x7fffffffLL && tensor_map_encode_fn() != nullptr;
 }
@@ -566,9 +487,8 @@ cudaError_t launch_verify_tc(const VerifyParams &p, cudaStream_t st) {
                                    strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    const bool fused = p.prev_accepted != nullptr;
-    const size_t smem_bytes = fused ? kStateSmemFusedBytes : kStateSmemBytes;
-    auto kern = fused ? state_kernel<__nv_bfloat16, true> : state_kernel<__nv_bfloat16, false>;
+    const size_t smem_bytes = kStateSmemBytes;
+    auto kern = state_kernel<__nv_bfloat16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
     if (e != cudaSuccess) return e;
     window_kernel<__nv_bfloat16><<<(unsigned)items, kWinThreads, 0, st>>>(p, ws);

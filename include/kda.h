@@ -298,15 +298,18 @@ KDA_API int kda_replay_commit_u(const kda_dims *dims, int32_t batch, int32_t dra
                                 int32_t *err_flag, void *stream);
 
 /*
- * kda_commit_verify_u: the previous window's commit fused with this window's
- * verify, for when the previous window's acceptance is already on the
- * device.  Per (sequence, head) one launch reads the state once, applies
- * the accepted prefix (prev_accepted[n] records, 0..prev_draft_len) of the
+ * kda_commit_verify_u: the previous window's commit and this window's
+ * verify in one call, for when the previous window's acceptance is already
+ * on the device (no host round trip between them).  It applies the
+ * accepted prefix (prev_accepted[n] records, 0..prev_draft_len) of the
  * previous window's u records `prev` exactly as kda_replay_commit_u does
  * (same bits), writes the committed state back to the pool, and verifies
- * the new draft window from it into `rec` (as kda_verify_record_u).  One
- * state read and one write, against a read and a write for the commit plus
- * a read for the verify.  prev and rec must not overlap.  prev_accepted
+ * the new draft window from it into `rec` (as kda_verify_record_u).  On the
+ * tensor-core verify shape (bf16, dk = dv = 128, draft_len <= 8, with a
+ * workspace) the commit and the verify are two launches in stream order
+ * (measured faster than one launch doing both); on the other shapes the
+ * verify kernel commits the state it has loaded, one state read and one
+ * write in one launch.  prev and rec must not overlap.  prev_accepted
  * outside 0..prev_draft_len sets KDA_DEVERR_ACCEPTED and that sequence is
  * verified without a commit.
  */

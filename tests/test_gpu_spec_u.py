@@ -1,9 +1,11 @@
 """GPU checks of the ReplaySSM u-record variant ("2.8x faster Kimi K3
 inference on CANN", section 04 "ReplaySSM"): verify writes u = beta (v - S'k^)
 per value row, the commit applies S <- S diag(exp g) + u k^^T, and
-kda_commit_verify_u fuses the previous window's commit with this window's
-verify.  Outputs and committed states are compared with the fp64 oracle; the
-fused launch is compared bit for bit with the separate commit + verify."""
+kda_commit_verify_u does the previous window's commit and this window's
+verify in one call (one launch on the CUDA-core shapes, the commit and the
+verify launches on the tensor-core one).  Outputs and committed states are
+compared with the fp64 oracle; the call is compared bit for bit with the
+separate commit + verify calls."""
 import pytest
 import torch
 
@@ -118,8 +120,8 @@ def test_commit_verify_bad_accepted_length():
 
 
 def test_u_records_full_size_b128_d7_h32():
-    """The benchmark's verify shape: fused commit + verify against the
-    separate launches, bit for bit, on a 4096-slot pool."""
+    """The benchmark's verify shape: the commit + verify call against the
+    separate calls, bit for bit, on a 4096-slot pool."""
     kda = _kda()
     B, D, H, d = 128, 7, 32, 128
     w1 = inputs.verify_inputs(B, D, H, d, d, dtype="bf16", num_slots=4096, seed=61, device="cuda")
