@@ -186,6 +186,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 3)
         o[rr] = row_output(c, u, tc.kq, p.scale);
         ss = __fmaf_rn(o[rr], o[rr], ss);
     }
+    // the updated state leaves first: nothing below waits for these stores
+    // (the exchange below is st.async into an mbarrier, with no release)
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) store_row<DK>(S + (int64_t)(lrow0 + rr * kFusedGroups) * DK, l, s[rr]);
 
     // sum of o_i^2: the 4 groups of a warp, the 4 warps in order, then the
     // two CTAs (rank 0's half first, on both CTAs: the same bits)
@@ -200,8 +204,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 3)
     // every read of the old conv state has been consumed (the partial sum
     // depends on it) when the partial leaves
     if (tid == 0) st_async_peer(&peer_part, &xbar, mine, rank ^ 1u);
-#pragma unroll
-    for (int rr = 0; rr < R; ++rr) store_row<DK>(S + (int64_t)(lrow0 + rr * kFusedGroups) * DK, l, s[rr]);
     // the other CTA's partial (thread 0 polls, bounded)
     const bool got = __syncthreads_and(tid == 0 ? mbar_wait(&xbar, 0) : true) != 0;
     if (got) {
