@@ -47,6 +47,14 @@ extern "C" {
 
 int kda_abi_version(void) { return KDA_ABI_VERSION; }
 
+int kda_checked_build(void) {
+#ifdef KDA_CHECKED
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 const char *kda_status_string(int status) {
     switch (status) {
         case KDA_OK: return "ok";

@@ -13,6 +13,7 @@
 // once with 128-bit streaming accesses, the two row dot products (S'k^ and
 // S'q^) are 3-level shuffle reductions, and no __syncthreads is needed.
 #include "kda.h"
+#include "kda_check.cuh"
 #include "kda_internal.h"
 #include "kda_rowmath.cuh"
 
@@ -35,6 +36,11 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams 
 
     const T *vrow = static_cast<const T *>(p.v) + sh * p.dv;
     T *orow = static_cast<T *>(p.out) + sh * p.dv;
+    // checked build: this CTA's token vectors and its rows of v and out
+    const int64_t tokens = (int64_t)p.batch * p.H;
+    if (!in_bounds(sh * DK, DK, tokens * DK, p.err_flag) ||
+        !in_bounds(sh * p.dv + blk * ROWS, ROWS, tokens * p.dv, p.err_flag))
+        return;
     const int slot = __ldg(p.slot_ids + n);
     if (slot < 0 || (int64_t)slot >= p.num_slots) {
         if (l == 0) {
@@ -45,6 +51,9 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams 
         return;
     }
     float *S = p.pool + ((int64_t)slot * p.H + h) * (int64_t)p.dv * DK;
+    if (!in_bounds(((int64_t)slot * p.H + h) * p.dv * DK + (int64_t)blk * ROWS * DK, (int64_t)ROWS * DK,
+                   p.num_slots * p.H * (int64_t)p.dv * DK, p.err_flag))
+        return;
 
     // Issue the state loads first: they do not depend on the token.
     LaneVec<DK> s[R];

@@ -23,6 +23,7 @@
 // same convolved inputs held in fp32.
 #include "kda.h"
 #include "kda_bulk.cuh"
+#include "kda_check.cuh"
 #include "kda_internal.h"
 #include "kda_rowmath.cuh"
 
@@ -102,6 +103,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 3)
     const int vbase = (int)rank * HV;               // first value row of this CTA
 
     T *orow = static_cast<T *>(p.out) + sh * DV + vbase;
+    // checked build: the token's vectors and this CTA's rows of z and out
+    // (both CTAs of the pair take the same decision, so neither waits alone)
+    const int64_t tokens = (int64_t)p.batch * p.H;
+    if (!in_bounds(sh * DK, DK, tokens * DK, p.err_flag) || !in_bounds(sh * DV, DV, tokens * DV, p.err_flag))
+        return;
     const int slot = __ldg(p.slot_ids + n);
     if (slot < 0 || (int64_t)slot >= p.num_slots) {
         // uniform over the pair: both CTAs read the same slot id
@@ -110,6 +116,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFusedThreads, 3)
         return;
     }
     float *S = p.pool + ((int64_t)slot * p.H + h) * (int64_t)DV * DK + (int64_t)vbase * DK;
+    if (!in_bounds(((int64_t)slot * p.H + h) * DV * DK, (int64_t)DV * DK, p.num_slots * p.H * (int64_t)DV * DK,
+                   p.err_flag) ||
+        !in_bounds(((int64_t)slot * p.H + h) * 3 * NC, 3 * NC, p.num_slots * p.H * (int64_t)(3 * NC), p.err_flag))
+        return;
 
     // Every global load of the step is issued here, before any of them is
     // used: the state rows, the token's gate, beta, output gate and norm

@@ -59,9 +59,10 @@ struct VerifyParams {
     // u-record variant: u_j = beta_j (v_j - S'_j k^_j) per value row, fp32
     // [B][D][H][dv] (null: not written; rec_v and rec_beta may then be null)
     float *rec_u;
-    // fused commit: before this window, the accepted prefix of the previous
+    // commit first: before this window, the accepted prefix of the previous
     // window's u records is applied to the committed state, which is written
-    // back (prev_accepted null: no commit)
+    // back (prev_accepted null: no commit; the CUDA-core verify kernel does it
+    // in the same launch, the tensor-core path as a launch of its own)
     const float *prev_k_hat, *prev_g, *prev_u;
     const int32_t *prev_accepted;
     int32_t prev_D;

@@ -33,6 +33,7 @@
 #include <stdint.h>
 
 #include "kda.h"
+#include "kda_check.cuh"
 #include "kda_internal.h"
 #include "kda_rowmath.cuh"
 
@@ -136,6 +137,11 @@ __global__ void __launch_bounds__(kPrepThreads) chunk_prep_kernel(const PrefillP
     if (slot < 0 || (int64_t)slot >= p.num_slots) return;  // nothing to prepare
     const int64_t t0 = (int64_t)p.cu_seqlens[s] + (int64_t)(chunk - plan[s]) * C;
     const int len = (int)((int64_t)p.cu_seqlens[s + 1] - t0 < C ? (int64_t)p.cu_seqlens[s + 1] - t0 : C);
+    // checked build: the chunk's tokens and its workspace block
+    if (!in_bounds(t0, len, p.total_tokens, p.err_flag) ||
+        !in_bounds((int64_t)(L.plan_bytes + ((size_t)chunk * H + h) * L.chunk_bytes), (int64_t)L.chunk_bytes,
+                   (int64_t)p.workspace_bytes, p.err_flag))
+        return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const T *q = static_cast<const T *>(p.q);
     const T *k = static_cast<const T *>(p.k);
@@ -345,6 +351,12 @@ __global__ void __launch_bounds__(kChainThreads) chunk_chain_kernel(const Prefil
     const int32_t cs = p.cu_seqlens[s], ce = p.cu_seqlens[s + 1];
     const int slot = p.slot_ids[s];
     T *out = static_cast<T *>(p.out);
+    // checked build: the sequence's tokens and its chunks' workspace blocks
+    if (!in_bounds(cs, (int64_t)ce - cs, p.total_tokens, p.err_flag) ||
+        !in_bounds((int64_t)(L.plan_bytes + (size_t)plan[s] * H * L.chunk_bytes),
+                   (int64_t)(plan[s + 1] - plan[s]) * H * (int64_t)L.chunk_bytes, (int64_t)p.workspace_bytes,
+                   p.err_flag))
+        return;
     if (slot < 0 || (int64_t)slot >= p.num_slots) {
         for (int64_t idx = tid; idx < (int64_t)(ce - cs) * kChainRows; idx += kChainThreads) {
             const int64_t t = cs + idx / kChainRows;
@@ -356,6 +368,9 @@ __global__ void __launch_bounds__(kChainThreads) chunk_chain_kernel(const Prefil
         return;
     }
     float *Sg = p.pool + ((int64_t)slot * H + h) * (int64_t)DV * DK + (int64_t)rb * kChainRows * DK;
+    if (!in_bounds(((int64_t)slot * H + h) * DV * DK + (int64_t)rb * kChainRows * DK, (int64_t)kChainRows * DK,
+                   p.num_slots * H * (int64_t)DV * DK, p.err_flag))
+        return;
     for (int idx = tid; idx < kChainRows * DK; idx += kChainThreads)
         sm.S[idx / DK][idx % DK] = p.init_from_pool ? Sg[idx] : 0.f;
     const float scale = p.scale;

@@ -55,6 +55,7 @@
 
 #include "kda.h"
 #include "kda_bulk.cuh"
+#include "kda_check.cuh"
 #include "kda_internal.h"
 #include "kda_rowmath.cuh"
 #include "kda_tc.cuh"
@@ -336,6 +337,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
     if (slot < 0 || (int64_t)slot >= p.num_slots) return leave();  // the chain writes zeros
     const int t0 = p.cu_seqlens[s] + (chunk - plan[s]) * C;
     const int L = p.cu_seqlens[s + 1] - t0 < C ? p.cu_seqlens[s + 1] - t0 : C;
+    // checked build: the chunk's tokens, its operand image and the slot's
+    // conv state
+    if (!in_bounds(t0, L, p.total_tokens, p.err_flag) ||
+        !in_bounds((int64_t)(plan_bytes(n) + ((size_t)chunk * H + h) * IMG_BYTES), IMG_BYTES,
+                   (int64_t)p.workspace_bytes, p.err_flag) ||
+        (FUSED && !in_bounds(((int64_t)slot * H + h) * 3 * kConvChannels, 3 * kConvChannels,
+                             p.num_slots * H * (int64_t)(3 * kConvChannels), p.err_flag)))
+        return leave();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int lr = ((warp & 3) << 5) | lane;  // TMEM lane
     const int hf = warp >> 2;                 // half of the columns or tokens
@@ -1167,6 +1176,16 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
     }
     const unsigned char *ws = static_cast<const unsigned char *>(p.workspace) + plan_bytes(n);
     auto image = [&](int ci) { return ws + ((size_t)(plan[s] + c_lo + ci) * H + h) * (size_t)IMG_BYTES; };
+    // checked build: this launch's operand images (its last one ends highest),
+    // the sequence's tokens, the slot's state and conv state
+    if ((nchunks > 0 && !in_bounds((int64_t)(plan_bytes(n) + ((size_t)(plan[s] + c_lo + nchunks - 1) * H + h) *
+                                                             (size_t)IMG_BYTES),
+                                   IMG_BYTES, (int64_t)p.workspace_bytes, p.err_flag)) ||
+        !in_bounds(cs, (int64_t)ce - cs, p.total_tokens, p.err_flag) ||
+        !in_bounds(((int64_t)slot * H + h) * D * D, D * D, p.num_slots * H * (int64_t)(D * D), p.err_flag) ||
+        (FUSED && !in_bounds(((int64_t)slot * H + h) * 3 * kConvChannels, 3 * kConvChannels,
+                             p.num_slots * H * (int64_t)(3 * kConvChannels), p.err_flag)))
+        return;
 
     if (warp == 0) tc::tmem_alloc(&sm.tmem_base, CT_COLS);
     if (tid == 0) {

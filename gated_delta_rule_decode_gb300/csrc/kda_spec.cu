@@ -21,6 +21,7 @@
 #include "kda.h"
 #include "kda_internal.h"
 #include "kda_bulk.cuh"
+#include "kda_check.cuh"
 #include "kda_rowmath.cuh"
 #include "kda_window.cuh"
 
@@ -88,9 +89,19 @@ __global__ void __launch_bounds__(256, (DMAX <= 8 ? 2 : 1)) verify_kernel(const 
     const int gid = warp * kGroupsPerWarp + grp;
     const int D = p.D;
 
+    // checked build: the window's token-heads (inputs, outputs, records) and
+    // the previous window's records
+    if (!in_bounds((int64_t)n * D * p.H + h, (int64_t)(D - 1) * p.H + 1, (int64_t)p.batch * D * p.H, p.err_flag) ||
+        (p.prev_accepted != nullptr &&
+         !in_bounds((int64_t)n * p.prev_D * p.H + h, (int64_t)(p.prev_D - 1) * p.H + 1,
+                    (int64_t)p.batch * p.prev_D * p.H, p.err_flag)))
+        return;
     const int slot = __ldg(p.slot_ids + n);
     const bool valid = slot >= 0 && (int64_t)slot < p.num_slots;
     if (slot >= 0 && !valid && threadIdx.x == 0 && p.err_flag) atomicOr(p.err_flag, KDA_DEVERR_SLOT);
+    if (valid && !in_bounds(((int64_t)slot * p.H + h) * p.dv * DK, (int64_t)p.dv * DK,
+                            p.num_slots * p.H * (int64_t)p.dv * DK, p.err_flag))
+        return;
 
     // S0 is requested first, as one bulk copy into shared memory, so that the
     // coefficient phases overlap the load and hold no state registers
@@ -196,6 +207,12 @@ __global__ void __launch_bounds__(kSpecWarps * 32) replay_kernel(const ReplayPar
         return;
     }
     if (a == 0) return;  // nothing accepted: no memory access at all
+    // checked build: this CTA's state rows and the sequence's records
+    if (!in_bounds(((int64_t)slot * p.H + h) * p.dv * DK + (int64_t)blk * ROWS * DK, (int64_t)ROWS * DK,
+                   p.num_slots * p.H * (int64_t)p.dv * DK, p.err_flag) ||
+        !in_bounds((int64_t)n * p.D * p.H + h, (int64_t)(p.D - 1) * p.H + 1, (int64_t)p.batch * p.D * p.H,
+                   p.err_flag))
+        return;
 
     float *S = p.pool + ((int64_t)slot * p.H + h) * (int64_t)p.dv * DK;
     LaneVec<DK> s[R];
@@ -288,6 +305,12 @@ __global__ void __launch_bounds__(kSpecWarps * 32) replay_u_kernel(const ReplayP
         return;
     }
     if (a == 0) return;  // nothing accepted: no memory access at all
+    // checked build: this CTA's state rows and the sequence's records
+    if (!in_bounds(((int64_t)slot * p.H + h) * p.dv * DK + (int64_t)blk * ROWS * DK, (int64_t)ROWS * DK,
+                   p.num_slots * p.H * (int64_t)p.dv * DK, p.err_flag) ||
+        !in_bounds((int64_t)n * p.D * p.H + h, (int64_t)(p.D - 1) * p.H + 1, (int64_t)p.batch * p.D * p.H,
+                   p.err_flag))
+        return;
 
     float *S = p.pool + ((int64_t)slot * p.H + h) * (int64_t)p.dv * DK;
     LaneVec<DK> s[R];

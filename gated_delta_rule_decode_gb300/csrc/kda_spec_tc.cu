@@ -40,6 +40,7 @@
 
 #include "kda.h"
 #include "kda_bulk.cuh"
+#include "kda_check.cuh"
 #include "kda_internal.h"
 #include "kda_tc.cuh"
 #include "kda_window.cuh"
@@ -145,6 +146,12 @@ __global__ void __launch_bounds__(kWinThreads) window_kernel(const VerifyParams 
     // the state kernel may start now: it waits for this grid's completion
     // before it reads any scratch record
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // checked build: this (sequence, head)'s scratch record and its window's
+    // token-heads
+    const int64_t items = (int64_t)p.batch * p.H;
+    if (!in_bounds(sh * kRecBytes, kRecBytes, items * kRecBytes, p.err_flag) ||
+        !in_bounds((int64_t)n * D * p.H + h, (int64_t)(D - 1) * p.H + 1, items * D, p.err_flag))
+        return;
     unsigned char *rec = ws + sh * kRecBytes;
     float *Aw = reinterpret_cast<float *>(rec + kOffA);
     float *Pw = reinterpret_cast<float *>(rec + kOffP);
@@ -285,6 +292,11 @@ __global__ void __launch_bounds__(kStateThreads, 3) state_kernel(const VerifyPar
     const int h = sh % p.H, n = sh / p.H;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int D = p.D;
+    // checked build: the scratch record and the window's token-heads
+    const int64_t items = (int64_t)p.batch * p.H;
+    if (!in_bounds((int64_t)sh * kRecBytes, kRecBytes, items * kRecBytes, p.err_flag) ||
+        !in_bounds((int64_t)n * D * p.H + h, (int64_t)(D - 1) * p.H + 1, items * D, p.err_flag))
+        return;
 
     const int slot = __ldg(p.slot_ids + n);
     const bool valid = slot >= 0 && (int64_t)slot < p.num_slots;

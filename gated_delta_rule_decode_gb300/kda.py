@@ -29,6 +29,7 @@ KDA_DEVERR_SEQLENS = 4
 KDA_DEVERR_TIMEOUT = 8
 KDA_DEVERR_RANGE = 16
 KDA_DEVERR_SNAPSHOT = 32
+KDA_DEVERR_BOUNDS = 64  # checked builds (-DKDA_CHECKED) only
 
 EXPORTED = ("kda_decode", "kda_verify_record", "kda_replay_commit",
             "kda_prefill_chunked", "kda_prefill_workspace_bytes",
@@ -36,7 +37,7 @@ EXPORTED = ("kda_decode", "kda_verify_record", "kda_replay_commit",
             "kda_prefill_chunked_static", "kda_static_scratch_bytes",
             "kda_verify_workspace_bytes", "kda_prefill_chunked_snapshots",
             "kda_records_u_bytes", "kda_verify_record_u", "kda_replay_commit_u",
-            "kda_commit_verify_u", "kda_decode_fused", "kda_prefill_fused")
+            "kda_commit_verify_u", "kda_decode_fused", "kda_prefill_fused", "kda_checked_build")
 
 
 class KdaError(RuntimeError):
@@ -125,8 +126,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_abi_version.argtypes = []
+    lib.kda_checked_build.argtypes = []
     for name in ("kda_decode", "kda_verify_record", "kda_replay_commit",
-                 "kda_prefill_chunked", "kda_abi_version"):
+                 "kda_prefill_chunked", "kda_abi_version", "kda_checked_build"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -459,7 +461,7 @@ def commit_verify_u(prev_records, prev_accepted, q, k, v, g, b, slot_ids, pool, 
                     records=None, *, workspace=None, eps=1e-6, scale=None, err_flag=None,
                     stream=None, _prepare=False):
     """Commit the previous window's accepted u records, then verify this
-    window, in one launch (the pool receives the committed state).
+    window, in one call (the pool receives the committed state).
     Returns (out, records)."""
     B, D, dims, out, records, workspace, ws_bytes = _verify_u_args(
         q, k, v, g, b, slot_ids, pool, out, records, workspace, eps, scale, stream)

@@ -88,10 +88,13 @@ enum {
     KDA_DEVERR_RANGE = 16,    /* a value passed to the tensor-core prefill's
                                  fp16 products exceeded +-65504; the outputs and
                                  final state of that sequence are not valid  */
-    KDA_DEVERR_SNAPSHOT = 32  /* a prefill snapshot request was skipped: token
+    KDA_DEVERR_SNAPSHOT = 32, /* a prefill snapshot request was skipped: token
                                  count not a positive multiple of 64 within its
                                  sequence, requests out of order, or slot id
                                  >= num_slots                                */
+    KDA_DEVERR_BOUNDS = 64    /* (checked builds, -DKDA_CHECKED, only) an
+                                 access outside its buffer was found and
+                                 skipped                                     */
 };
 
 typedef struct kda_dims {
@@ -475,6 +478,11 @@ KDA_API const char *kda_status_string(int status);
 
 /* KDA_ABI_VERSION of the built library. */
 KDA_API int kda_abi_version(void);
+
+/* 1 when the library was built with its kernels' bounds checks
+ * (-DKDA_CHECKED: an access outside its buffer sets KDA_DEVERR_BOUNDS in the
+ * call's err_flag and is skipped), else 0. */
+KDA_API int kda_checked_build(void);
 
 #ifdef __cplusplus
 }
