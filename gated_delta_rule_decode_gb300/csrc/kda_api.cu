@@ -47,6 +47,36 @@ extern "C" {
 
 int kda_abi_version(void) { return KDA_ABI_VERSION; }
 
+// The checked build's precondition check: a slot id named twice in one call
+// (two CTAs would update the same state) sets KDA_DEVERR_DUPLICATE.  O(n^2)
+// comparisons, before the call's kernels, on its stream; nothing in the
+// normal build.
+#ifdef KDA_CHECKED
+static __global__ void duplicate_slots_kernel(const int32_t *slots, int32_t n, int32_t *flag) {
+    for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const int32_t si = slots[i];
+        if (si < 0) continue;
+        for (int32_t j = i + 1; j < n; ++j)
+            if (slots[j] == si) {
+                atomicOr(flag, KDA_DEVERR_DUPLICATE);
+                break;
+            }
+    }
+}
+#endif
+
+static int check_unique_slots(const int32_t *slots, int32_t n, int32_t *err_flag, void *stream) {
+#ifdef KDA_CHECKED
+    if (slots == nullptr || err_flag == nullptr || n < 2) return KDA_OK;
+    const int blocks = (n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024;
+    duplicate_slots_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(slots, n, err_flag);
+    return from_cuda(cudaGetLastError());
+#else
+    (void)slots, (void)n, (void)err_flag, (void)stream;
+    return KDA_OK;
+#endif
+}
+
 int kda_checked_build(void) {
 #ifdef KDA_CHECKED
     return 1;
@@ -89,6 +119,7 @@ int kda_decode(const kda_dims *dims, int32_t batch, const void *q, const void *k
     p.out = out; p.err_flag = err_flag;
     p.batch = batch; p.H = dims->num_heads; p.dv = dims->dv;
     p.eps = dims->eps; p.scale = resolve_scale(dims);
+    if (const int cs = check_unique_slots(slot_ids, batch, err_flag, stream)) return cs;
     return from_cuda(kda::launch_decode(p, dims->dk, dims->dtype, (cudaStream_t)stream));
 }
 
@@ -112,6 +143,7 @@ int kda_decode_fused(const kda_dims *dims, int32_t batch, const void *q, const v
     p.out = out; p.err_flag = err_flag;
     p.batch = batch; p.H = dims->num_heads; p.dv = dims->dv;
     p.eps = dims->eps; p.scale = resolve_scale(dims); p.eps_o = io->eps_o;
+    if (const int cs = check_unique_slots(slot_ids, batch, err_flag, stream)) return cs;
     return from_cuda(kda::launch_decode_fused(p, dims->dk, dims->dtype, (cudaStream_t)stream));
 }
 
@@ -147,6 +179,7 @@ int kda_verify_record(const kda_dims *dims, int32_t batch, int32_t draft_len, co
     p.err_flag = err_flag;
     p.batch = batch; p.D = draft_len; p.H = dims->num_heads; p.dv = dims->dv;
     p.eps = dims->eps; p.scale = resolve_scale(dims);
+    if (const int cs = check_unique_slots(slot_ids, batch, err_flag, stream)) return cs;
     return from_cuda(kda::launch_verify(p, dims->dk, dims->dtype, (cudaStream_t)stream));
 }
 
@@ -192,6 +225,7 @@ static int verify_u_impl(const kda_dims *dims, int32_t batch, int32_t prev_draft
         p.prev_k_hat = prev->k_hat; p.prev_g = prev->g; p.prev_u = prev->u;
         p.prev_accepted = prev_accepted; p.prev_D = prev_draft_len;
     }
+    if (const int cs = check_unique_slots(slot_ids, batch, err_flag, stream)) return cs;
     return from_cuda(kda::launch_verify(p, dims->dk, dims->dtype, (cudaStream_t)stream));
 }
 
@@ -230,6 +264,7 @@ int kda_replay_commit_u(const kda_dims *dims, int32_t batch, int32_t draft_len, 
     p.num_accepted = num_accepted; p.slot_ids = slot_ids;
     p.pool = pool; p.num_slots = num_slots; p.err_flag = err_flag;
     p.batch = batch; p.D = draft_len; p.H = dims->num_heads; p.dv = dims->dv;
+    if (const int cs = check_unique_slots(slot_ids, batch, err_flag, stream)) return cs;
     return from_cuda(kda::launch_replay_u(p, dims->dk, (cudaStream_t)stream));
 }
 
@@ -249,6 +284,7 @@ int kda_replay_commit(const kda_dims *dims, int32_t batch, int32_t draft_len,
     p.num_accepted = num_accepted; p.slot_ids = slot_ids;
     p.pool = pool; p.num_slots = num_slots; p.err_flag = err_flag;
     p.batch = batch; p.D = draft_len; p.H = dims->num_heads; p.dv = dims->dv;
+    if (const int cs = check_unique_slots(slot_ids, batch, err_flag, stream)) return cs;
     return from_cuda(kda::launch_replay(p, dims->dk, dims->dtype, (cudaStream_t)stream));
 }
 
@@ -303,6 +339,7 @@ static int prefill_impl(const kda_dims *dims, int32_t num_seqs, const int32_t *c
         p.conv_state = io->conv_state; p.conv_w = io->conv_w; p.z = io->z; p.norm_w = io->norm_w;
         p.eps_o = io->eps_o;
     }
+    if (const int cs = check_unique_slots(slot_ids, num_seqs, err_flag, stream)) return cs;
     return from_cuda(kda::launch_prefill(p, dims->dtype, (cudaStream_t)stream));
 }
 

@@ -30,6 +30,7 @@ KDA_DEVERR_TIMEOUT = 8
 KDA_DEVERR_RANGE = 16
 KDA_DEVERR_SNAPSHOT = 32
 KDA_DEVERR_BOUNDS = 64  # checked builds (-DKDA_CHECKED) only
+KDA_DEVERR_DUPLICATE = 128  # checked builds only
 
 EXPORTED = ("kda_decode", "kda_verify_record", "kda_replay_commit",
             "kda_prefill_chunked", "kda_prefill_workspace_bytes",

@@ -92,9 +92,12 @@ enum {
                                  count not a positive multiple of 64 within its
                                  sequence, requests out of order, or slot id
                                  >= num_slots                                */
-    KDA_DEVERR_BOUNDS = 64    /* (checked builds, -DKDA_CHECKED, only) an
+    KDA_DEVERR_BOUNDS = 64,   /* (checked builds, -DKDA_CHECKED, only) an
                                  access outside its buffer was found and
                                  skipped                                     */
+    KDA_DEVERR_DUPLICATE = 128 /* (checked builds only) a slot id appears
+                                 twice in one call's slot_ids (the call's
+                                 results for those slots are not valid)      */
 };
 
 typedef struct kda_dims {

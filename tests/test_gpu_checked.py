@@ -6,7 +6,9 @@ state rows, records, scratch records, operand images, conv states) against
 the sizes its arguments give, and an access outside them would set
 KDA_DEVERR_BOUNDS and be skipped.  Each entry point runs on the same inputs
 through the normal and the checked library: the checked one must find
-nothing (the error flag stays 0) and produce the same bits."""
+nothing (the error flag stays 0) and produce the same bits.  The checked
+build also checks a precondition the normal one leaves undefined: a slot
+id named twice in one call sets KDA_DEVERR_DUPLICATE."""
 import pytest
 import torch
 
@@ -151,3 +153,26 @@ def test_prefill_fused_checked(checked, lens, H):
                                 ex.norm_w, init_from_pool=True, err_flag=flag)
         return out, pool, cst
     _check(_both(checked, run))
+
+
+def test_duplicate_slots_flagged(checked):
+    """Two sequences naming the same slot (a precondition violation: both
+    would update that state) are flagged by the checked build, in every
+    entry point that takes slot ids; the normal build does not look."""
+    kda = _kda()
+    x = inputs.decode_inputs(4, 2, 64, 64, dtype="f32", num_slots=6, seed=16, device="cuda")
+    x.slot_ids = torch.tensor([3, 1, 3, 0], dtype=torch.int32, device="cuda")
+    y = inputs.verify_inputs(4, 3, 2, 64, 64, dtype="f32", num_slots=6, seed=16, device="cuda")
+    y.slot_ids = torch.tensor([2, 2, -1, 5], dtype=torch.int32, device="cuda")
+    z = inputs.prefill_inputs([40, 70], 2, 64, 64, dtype="f32", num_slots=3, seed=16, device="cuda")
+    z.slot_ids = torch.tensor([1, 1], dtype=torch.int32, device="cuda")
+    calls = [
+        lambda f: kda.decode(x.q, x.k, x.v, x.g, x.b, x.slot_ids, x.pool.clone(), err_flag=f),
+        lambda f: kda.verify_record(y.q, y.k, y.v, y.g, y.b, y.slot_ids, y.pool, err_flag=f),
+        lambda f: kda.prefill_chunked(z.q, z.k, z.v, z.g, z.b, z.cu_seqlens, z.slot_ids, z.pool.clone(),
+                                      err_flag=f),
+    ]
+    for call in calls:
+        (_, f0), (_, f1) = _both(checked, call)
+        assert f0 == 0
+        assert f1 == kda.KDA_DEVERR_DUPLICATE
