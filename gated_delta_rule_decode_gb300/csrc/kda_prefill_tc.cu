@@ -160,8 +160,9 @@ __device__ inline int find_seq(const int32_t *plan, int n, int32_t c) {
 // bank conflicts); v follows into q's buffer once q has been used.  Steps:
 //   0. (fused prefill) ShortConv of k and q in place in their boxes
 //   1. L2Norm sums of squares per token row
-//   2. gamma = running sum of g per channel, in place (both token halves at
-//      once; the second adds gamma_31 = ref); span check; norms and beta
+//   2. gamma = running sum of g per channel, in place (four token quarters
+//      at once, each then adding the sums of the quarters before it); ref =
+//      gamma_31, gamma_C and the span check; norms and beta
 //   3. row phase: [K+; Q+] into TMEM (the A operand of the A/P product),
 //      K- into a shared tile (its B operand), Q~ rows of the image
 //   4. channel phase, while G = [K+; Q+] K-^T runs: beta K~^T into TMEM (the
@@ -203,11 +204,17 @@ struct PrepSmem {
     float invk[C], invq[C], beta[C];
     float nrm[2][2 * C];  // sums of squares over each channel half: rows k_0..k_63, q_0..q_63
     float ref[D];         // gamma at token 31
-    float lo[D], hi[D];   // extremes of gamma over the chunk
     float gC[D];          // gamma at the chunk's last token
     float eref[D];        // e^{ref}
     float nrl[D];         // -ref log2(e)
-    float xs[32][33];     // partial products of the UT inverse
+    union {
+        float xs[32][33];  // partial products of the UT inverse
+        struct {           // the gamma scan's token quarters, per channel:
+            float tot[4][D];  // sums
+            float mn[3][D];   // extremes of the running sums of quarters 1..3
+            float mx[3][D];
+        } gq;
+    } u3;
     float vhist[3][D];    // fused: the three value inputs before the chunk
     uint64_t bar_in, bar_v, bar_mma, bar_q, bar_kp;
     uint32_t tmem_base;
@@ -216,6 +223,7 @@ constexpr size_t kPrepSmem = sizeof(PrepSmem) + 1024;
 static_assert(sizeof(InvScratch) <= C * D * 6, "inverse scratch must fit the k staging and the K- tile");
 static_assert(offsetof(PrepSmem, qv) % 1024 == 0 && offsetof(PrepSmem, u2) % 1024 == 0, "TMA boxes");
 static_assert(offsetof(PrepSmem, invk) % 16 == 0 && offsetof(PrepSmem, beta) % 16 == 0, "vector loads");
+static_assert(offsetof(PrepSmem, u3) % 8 == 0 && offsetof(PrepSmem, gC) % 8 == 0, "paired gamma statistics");
 
 // The staged k and q boxes hold the bf16 inputs; the fused prefill
 // overwrites them with the convolved values as fp16 (10-bit mantissa, so the
@@ -381,7 +389,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         for (int i = 0; i < 4; ++i) tma_load_2d(gam + i * C * 128, &gmap, h * D + 32 * i, t0, &sm.bar_in);
     }
     const T *__restrict__ bb = static_cast<const T *>(p.b);
-    const float bval = (tid < L) ? Elem<T>::load1(bb + (int64_t)(t0 + tid) * H + h) : 0.f;
+    // b of token tid - 128, for the thread that forms that token's beta
+    const float bval = (tid >= 2 * C && tid - 2 * C < L) ? Elem<T>::load1(bb + (int64_t)(t0 + tid - 2 * C) * H + h)
+                                                         : 0.f;
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -473,55 +483,70 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             }
             sm.nrm[ch][row] = ss.x + ss.y;
         }
-        // ---- 2. gamma, in place (thread = channel lr): both token halves'
-        // running sums at once, from zero; the first ends at ref = gamma_31,
-        // which the second half adds once it is known; rows past the chunk's
-        // end repeat gamma_C
-        float gmin = 0.f, gmax = 0.f, gc = 0.f;
-        float part[32];
+        // ---- 2. gamma, in place (thread = channel pair cp, channels 2 cp and
+        // 2 cp + 1, and token quarter qq, tokens 16 qq .. + 15): each
+        // quarter's running sums from zero on paired adds, then, once the
+        // quarters' sums are known, the sum of the quarters before it added;
+        // rows past the chunk's end repeat gamma_C.  The quarter-0 threads
+        // finish each channel: ref = gamma_31, gamma_C, the span check.
         {
-            float acc = 0.f;
+            const int cp = tid & 63, qq = tid >> 6, c2 = 2 * cp;
+            float2 part[16];
+            float2 acc = make_float2(0.f, 0.f), mn = acc, mx = acc, gcl = acc;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int r = 32 * hf + i;
-                acc += r < L ? st_f32(gam, r, lr) : 0.f;
+            for (int i = 0; i < 16; ++i) {
+                const int r = 16 * qq + i;
+                if (r < L) acc = __fadd2_rn(acc, *reinterpret_cast<const float2 *>(gam + tc::sw128_off(r, c2, C)));
                 part[i] = acc;
-                if (r == L - 1) gc = acc;
-                gmin = i == 0 ? acc : fminf(gmin, acc);
-                gmax = i == 0 ? acc : fmaxf(gmax, acc);
+                if (r == L - 1) gcl = acc;
+                mn = i == 0 ? acc : make_float2(fminf(mn.x, acc.x), fminf(mn.y, acc.y));
+                mx = i == 0 ? acc : make_float2(fmaxf(mx.x, acc.x), fmaxf(mx.y, acc.y));
             }
-            if (hf == 0) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) st_f32(gam, i, lr) = part[i];
-                sm.ref[lr] = acc;
-                sm.lo[lr] = gmin;
-                sm.hi[lr] = gmax;
-                if (L <= 32) sm.gC[lr] = gc;
+            *reinterpret_cast<float2 *>(&sm.u3.gq.tot[qq][c2]) = acc;
+            if (qq > 0) {
+                *reinterpret_cast<float2 *>(&sm.u3.gq.mn[qq - 1][c2]) = mn;
+                *reinterpret_cast<float2 *>(&sm.u3.gq.mx[qq - 1][c2]) = mx;
             }
-        }
-        __syncthreads();
-        if (hf == 1) {
-            const float ref = sm.ref[lr];
+            if (((L - 1) >> 4) == qq) *reinterpret_cast<float2 *>(&sm.gC[c2]) = gcl;  // the quarter's own sum
+            __syncthreads();
+            float2 off[4];
+            off[0] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) st_f32(gam, 32 + i, lr) = part[i] + ref;
-            gmin = fminf(sm.lo[lr], gmin + ref);
-            gmax = fmaxf(sm.hi[lr], gmax + ref);
-            gc += ref;
-            if (L > 32) sm.gC[lr] = gc;
-            const float gCv = L > 32 ? gc : sm.gC[lr];
-            unsafe = fmaxf(gmax - ref, ref - gmin) > kSpanLimit;
-            reinterpret_cast<float *>(img + IMG_EGC)[lr] = expf(gCv);
-            sm.eref[lr] = expf(ref);
-            sm.nrl[lr] = -ref * kLog2e;
-        } else {
-            // (thread = k row, then q row) the norms and beta
-            const int r = tid & (C - 1);
-            const float inv = (r < L) ? rsqrtf(sm.nrm[0][tid] + sm.nrm[1][tid] + p.eps) : 0.f;
-            if (tid >= C) {
-                sm.invq[r] = inv;
-            } else {
-                sm.invk[r] = inv;
-                sm.beta[r] = (r < L) ? sigmoid_f(bval) : 0.f;
+            for (int j = 1; j < 4; ++j)
+                off[j] = __fadd2_rn(off[j - 1], *reinterpret_cast<const float2 *>(&sm.u3.gq.tot[j - 1][c2]));
+            auto off_of = [&](int j) { return j == 0 ? off[0] : j == 1 ? off[1] : j == 2 ? off[2] : off[3]; };
+            const float2 o = off_of(qq);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                *reinterpret_cast<float2 *>(gam + tc::sw128_off(16 * qq + i, c2, C)) = __fadd2_rn(part[i], o);
+            if (qq == 0) {
+                const float2 ref = off[2];  // gamma_31
+                float2 gmin = mn, gmax = mx;
+#pragma unroll
+                for (int j = 1; j < 4; ++j) {
+                    const float2 a = __fadd2_rn(*reinterpret_cast<const float2 *>(&sm.u3.gq.mn[j - 1][c2]), off[j]);
+                    const float2 b = __fadd2_rn(*reinterpret_cast<const float2 *>(&sm.u3.gq.mx[j - 1][c2]), off[j]);
+                    gmin = make_float2(fminf(gmin.x, a.x), fminf(gmin.y, a.y));
+                    gmax = make_float2(fmaxf(gmax.x, b.x), fmaxf(gmax.y, b.y));
+                }
+                const float2 gCv = __fadd2_rn(*reinterpret_cast<const float2 *>(&sm.gC[c2]), off_of((L - 1) >> 4));
+                *reinterpret_cast<float2 *>(&sm.gC[c2]) = gCv;
+                *reinterpret_cast<float2 *>(&sm.ref[c2]) = ref;
+                unsafe = fmaxf(gmax.x - ref.x, ref.x - gmin.x) > kSpanLimit ||
+                         fmaxf(gmax.y - ref.y, ref.y - gmin.y) > kSpanLimit;
+                *reinterpret_cast<float2 *>(img + IMG_EGC + 4 * c2) = make_float2(expf(gCv.x), expf(gCv.y));
+                *reinterpret_cast<float2 *>(&sm.eref[c2]) = make_float2(expf(ref.x), expf(ref.y));
+                *reinterpret_cast<float2 *>(&sm.nrl[c2]) = make_float2(-ref.x * kLog2e, -ref.y * kLog2e);
+            } else if (tid >= 2 * C) {
+                // (threads 128..255 = k row, then q row) the norms and beta
+                const int t = tid - 2 * C, r = t & (C - 1);
+                const float inv = (r < L) ? rsqrtf(sm.nrm[0][t] + sm.nrm[1][t] + p.eps) : 0.f;
+                if (t >= C) {
+                    sm.invq[r] = inv;
+                } else {
+                    sm.invk[r] = inv;
+                    sm.beta[r] = (r < L) ? sigmoid_f(bval) : 0.f;
+                }
             }
         }
         unsafe = __syncthreads_or(unsafe) != 0;
@@ -770,13 +795,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                 x0 = fmaf(As[o + 16 + r0][o + k], t, x0);
                 x1 = fmaf(As[o + 17 + r0][o + k], t, x1);
             }
-            sm.xs[16 * ob + r0][j] = x0;
-            sm.xs[16 * ob + r0 + 1][j] = x1;
+            sm.u3.xs[16 * ob + r0][j] = x0;
+            sm.u3.xs[16 * ob + r0 + 1][j] = x1;
             __syncthreads();
             float y0 = 0.f, y1 = 0.f;
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
-                const float x = sm.xs[16 * ob + m][j];
+                const float x = sm.u3.xs[16 * ob + m][j];
                 y0 = fmaf(Ts[o + 16 + r0][o + 16 + m], x, y0);
                 y1 = fmaf(Ts[o + 17 + r0][o + 16 + m], x, y1);
             }
@@ -799,16 +824,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                 x10 = fmaf(a1, t0, x10);
                 x11 = fmaf(a1, t1, x11);
             }
-            sm.xs[r0][cp] = x00;
-            sm.xs[r0][cp + 16] = x01;
-            sm.xs[r0 + 1][cp] = x10;
-            sm.xs[r0 + 1][cp + 16] = x11;
+            sm.u3.xs[r0][cp] = x00;
+            sm.u3.xs[r0][cp + 16] = x01;
+            sm.u3.xs[r0 + 1][cp] = x10;
+            sm.u3.xs[r0 + 1][cp + 16] = x11;
             __syncthreads();
             float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
 #pragma unroll
             for (int m = 0; m < 32; ++m) {
                 const float a0 = Ts[32 + r0][32 + m], a1 = Ts[33 + r0][32 + m];
-                const float x0 = sm.xs[m][cp], x1 = sm.xs[m][cp + 16];
+                const float x0 = sm.u3.xs[m][cp], x1 = sm.u3.xs[m][cp + 16];
                 y00 = fmaf(a0, x0, y00);
                 y01 = fmaf(a0, x1, y01);
                 y10 = fmaf(a1, x0, y10);
