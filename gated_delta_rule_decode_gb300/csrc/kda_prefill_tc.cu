@@ -115,13 +115,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-__device__ __forceinline__ void sync_for_mma() {
-    fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-}
-
 // Bounded wait on an MMA-completion barrier; the result is made uniform across
 // the CTA and a timeout is recorded in the error flag.  `phase` advances only
 // when the wait succeeded, so after a timeout it still names the pending
