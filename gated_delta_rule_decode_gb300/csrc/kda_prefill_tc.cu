@@ -1327,15 +1327,18 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
                                                                : make_float4(0.f, 0.f, 0.f, 0.f);
             S[e] = v4.x; S[e + 1] = v4.y; S[e + 2] = v4.z; S[e + 3] = v4.w;
         }
-        auto store_s16 = [&]() {
-            uint32_t w[16];
+        auto store_s16 = [&](uint32_t (&w)[16]) {
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const __half2 h2 = __floats2half2_rn(S[2 * e], S[2 * e + 1]);
-                s16max = __hmax2_nan(s16max, __habs2(h2));
                 w[e] = *reinterpret_cast<const uint32_t *>(&h2);
             }
             tc::st16u(taddr(CT_S16 + cq * 16), w);
+        };
+        // the range check of S16, once it has been handed over
+        auto track_s16 = [&](const uint32_t (&w)[16]) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) s16max = __hmax2_nan(s16max, __habs2(*reinterpret_cast<const __half2 *>(&w[e])));
         };
         // outputs of chunk cj (tokens cq * 16 .. + 15 of value row lr), read
         // from its accumulator (complete: acc_done was observed): a full
@@ -1386,8 +1389,12 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
             }
             return true;
         };
-        store_s16();
-        warp_arrive(&sm.s16_ready);
+        {
+            uint32_t w[16];
+            store_s16(w);
+            warp_arrive(&sm.s16_ready);
+            track_s16(w);
+        }
         // snapshot requests of this sequence (the same for every thread)
         int snap_ptr = 0, snap_hi = 0;
         bool snap_bad = false;
@@ -1411,6 +1418,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
             // over S16 of chunk c + 1)
             ok = warp_wait(&sm.acc_done[b], (c >> 1) & 1) && warp_wait(&sm.egc_full[c & 3], (c >> 2) & 1);
             if (!ok) break;
+            uint32_t w[16];
             {
                 float d[32];
                 tc::ld32(taddr(CT_ACC + b * CT_ACC_STRIDE + cq * 32), d);
@@ -1425,9 +1433,10 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
                                                  make_float2(d[4 * j + 2], d[4 * j + 3]));
                     S[4 * j] = lo.x; S[4 * j + 1] = lo.y; S[4 * j + 2] = hi.x; S[4 * j + 3] = hi.y;
                 }
-                store_s16();
+                store_s16(w);
             }
             warp_arrive(&sm.s16_ready);
+            track_s16(w);
             // ---- chunk c's outputs, off the serial path
             ok = output(c);
             if (!ok) break;
