@@ -178,7 +178,7 @@ constexpr int kPrepThreads = 256;
 // A/P product and the channel phase have read them.
 struct InvScratch {
     float As[C][C + 4];  // rows 16-byte aligned; a quarter warp's rows hit distinct banks
-    float Ts[C][C + 1];
+    float Ts[C][C + 4];  // the same: its rows leave as float4 reads, a quarter warp's free of conflicts
 };
 
 struct PrepSmem {
@@ -214,6 +214,7 @@ struct PrepSmem {
 };
 constexpr size_t kPrepSmem = sizeof(PrepSmem) + 1024;
 static_assert(sizeof(InvScratch) <= C * D * 6, "inverse scratch must fit the k staging and the K- tile");
+static_assert(offsetof(InvScratch, Ts) % 16 == 0, "float4 rows of T");
 static_assert(offsetof(PrepSmem, qv) % 1024 == 0 && offsetof(PrepSmem, u2) % 1024 == 0, "TMA boxes");
 static_assert(offsetof(PrepSmem, invk) % 16 == 0 && offsetof(PrepSmem, beta) % 16 == 0, "vector loads");
 static_assert(offsetof(PrepSmem, u3) % 8 == 0 && offsetof(PrepSmem, gC) % 8 == 0, "paired gamma statistics");
@@ -751,7 +752,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         // 32-row block as -T22 (A21 T11); then the lower-left 32 x 32 block of
         // the whole matrix the same way
         float(*As)[C + 4] = sm.u1.inv.As;
-        float(*Ts)[C + 1] = sm.u1.inv.Ts;
+        float(*Ts)[C + 4] = sm.u1.inv.Ts;
         if (tid < C) {
             const int I = tid >> 4, jj = tid & 15, o = 16 * I;
             float col[16];
@@ -841,8 +842,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         // T into its swizzled tile (over gamma, which nothing reads any more)
         for (int idx = tid; idx < C * C / 4; idx += kPrepThreads) {
             const int r = idx / (C / 4), j = (idx % (C / 4)) * 4;
-            *reinterpret_cast<float4 *>(sm.u2.t + tc::sw128_off(r, j, 64)) =
-                make_float4(Ts[r][j], Ts[r][j + 1], Ts[r][j + 2], Ts[r][j + 3]);
+            *reinterpret_cast<float4 *>(sm.u2.t + tc::sw128_off(r, j, 64)) = *reinterpret_cast<const float4 *>(&Ts[r][j]);
         }
         // ---- 7. beta V^T into TMEM (thread = value row lr, tokens 32 hf ..)
         ok = __syncthreads_and(tid == 0 ? mbar_wait(&sm.bar_v, 0) : true) != 0;
