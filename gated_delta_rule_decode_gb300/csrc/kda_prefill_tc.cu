@@ -93,6 +93,9 @@ __device__ __forceinline__ void st_h(unsigned char *tile, int rows, int row, int
     *reinterpret_cast<__half *>(tile + tc::sw128_off16(row, k, rows)) = __float2half_rn(x);
 }
 
+// four consecutive floats of a 16-byte aligned shared-memory row
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+
 // two fp16 values in one 32-bit word: a in the low half, b in the high half
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     const __half2 h = __floats2half2_rn(a, b);
@@ -775,7 +778,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         __syncthreads();
         // The block products keep two outputs (level 1) or a 2 x 2 block of
         // outputs (level 2) per thread, so that each operand load serves two
-        // products.  The upper triangles of the diagonal blocks and the upper
+        // products; the row operands (rows of A or T, 16-byte aligned) are
+        // read four at a time.  The upper triangles of the diagonal blocks and the upper
         // right blocks hold zeros, so the sums run over whole blocks.
         {
             // level 1: X1 = A21 T11 per 32-row block ob (rows 2 rp, 2 rp + 1,
@@ -784,20 +788,30 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             const int r0 = 2 * rp;
             float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const float t = Ts[o + k][o + j];
-                x0 = fmaf(As[o + 16 + r0][o + k], t, x0);
-                x1 = fmaf(As[o + 17 + r0][o + k], t, x1);
+            for (int k4 = 0; k4 < 16; k4 += 4) {
+                const float4 a0 = ld4(&As[o + 16 + r0][o + k4]), a1 = ld4(&As[o + 17 + r0][o + k4]);
+                const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float t = Ts[o + k4 + e][o + j];
+                    x0 = fmaf(av0[e], t, x0);
+                    x1 = fmaf(av1[e], t, x1);
+                }
             }
             sm.u3.xs[16 * ob + r0][j] = x0;
             sm.u3.xs[16 * ob + r0 + 1][j] = x1;
             __syncthreads();
             float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const float x = sm.u3.xs[16 * ob + m][j];
-                y0 = fmaf(Ts[o + 16 + r0][o + 16 + m], x, y0);
-                y1 = fmaf(Ts[o + 17 + r0][o + 16 + m], x, y1);
+            for (int m4 = 0; m4 < 16; m4 += 4) {
+                const float4 a0 = ld4(&Ts[o + 16 + r0][o + 16 + m4]), a1 = ld4(&Ts[o + 17 + r0][o + 16 + m4]);
+                const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float x = sm.u3.xs[16 * ob + m4 + e][j];
+                    y0 = fmaf(av0[e], x, y0);
+                    y1 = fmaf(av1[e], x, y1);
+                }
             }
             Ts[o + 16 + r0][o + j] = -y0;
             Ts[o + 17 + r0][o + j] = -y1;
@@ -810,13 +824,17 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             const int r0 = 2 * rp;
             float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const float a0 = As[32 + r0][k], a1 = As[33 + r0][k];
-                const float t0 = Ts[k][cp], t1 = Ts[k][cp + 16];
-                x00 = fmaf(a0, t0, x00);
-                x01 = fmaf(a0, t1, x01);
-                x10 = fmaf(a1, t0, x10);
-                x11 = fmaf(a1, t1, x11);
+            for (int k4 = 0; k4 < 32; k4 += 4) {
+                const float4 a0 = ld4(&As[32 + r0][k4]), a1 = ld4(&As[33 + r0][k4]);
+                const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float t0 = Ts[k4 + e][cp], t1 = Ts[k4 + e][cp + 16];
+                    x00 = fmaf(av0[e], t0, x00);
+                    x01 = fmaf(av0[e], t1, x01);
+                    x10 = fmaf(av1[e], t0, x10);
+                    x11 = fmaf(av1[e], t1, x11);
+                }
             }
             sm.u3.xs[r0][cp] = x00;
             sm.u3.xs[r0][cp + 16] = x01;
@@ -825,13 +843,17 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             __syncthreads();
             float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
 #pragma unroll
-            for (int m = 0; m < 32; ++m) {
-                const float a0 = Ts[32 + r0][32 + m], a1 = Ts[33 + r0][32 + m];
-                const float x0 = sm.u3.xs[m][cp], x1 = sm.u3.xs[m][cp + 16];
-                y00 = fmaf(a0, x0, y00);
-                y01 = fmaf(a0, x1, y01);
-                y10 = fmaf(a1, x0, y10);
-                y11 = fmaf(a1, x1, y11);
+            for (int m4 = 0; m4 < 32; m4 += 4) {
+                const float4 a0 = ld4(&Ts[32 + r0][32 + m4]), a1 = ld4(&Ts[33 + r0][32 + m4]);
+                const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float x0 = sm.u3.xs[m4 + e][cp], x1 = sm.u3.xs[m4 + e][cp + 16];
+                    y00 = fmaf(av0[e], x0, y00);
+                    y01 = fmaf(av0[e], x1, y01);
+                    y10 = fmaf(av1[e], x0, y10);
+                    y11 = fmaf(av1[e], x1, y11);
+                }
             }
             Ts[32 + r0][cp] = -y00;
             Ts[32 + r0][cp + 16] = -y01;
