@@ -779,8 +779,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         // The block products keep two outputs (level 1) or a 2 x 2 block of
         // outputs (level 2) per thread, so that each operand load serves two
         // products; the row operands (rows of A or T, 16-byte aligned) are
-        // read four at a time.  The upper triangles of the diagonal blocks and the upper
-        // right blocks hold zeros, so the sums run over whole blocks.
+        // read four at a time.  The upper triangles of the diagonal blocks
+        // and the upper right blocks hold zeros, so the sums run over whole
+        // blocks.
         {
             // level 1: X1 = A21 T11 per 32-row block ob (rows 2 rp, 2 rp + 1,
             // column j of the 16 x 16 block), then T21 = -T22 X1
