@@ -697,7 +697,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                             const int j = 32 * hf + j4 + e;
                             a4[e] = (j < r) ? br * g32[j4 + e] : 0.f;
                         }
-                        *reinterpret_cast<float4 *>(&sm.u1.inv.As[r][32 * hf + j4]) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+                        *reinterpret_cast<float4 *>(&sm.u1.inv.As[r][32 * hf + j4]) =
+                            make_float4(a4[0], a4[1], a4[2], a4[3]);
                     }
                 } else {
                     const int r = lr - C;
@@ -865,7 +866,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         // T into its swizzled tile (over gamma, which nothing reads any more)
         for (int idx = tid; idx < C * C / 4; idx += kPrepThreads) {
             const int r = idx / (C / 4), j = (idx % (C / 4)) * 4;
-            *reinterpret_cast<float4 *>(sm.u2.t + tc::sw128_off(r, j, 64)) = *reinterpret_cast<const float4 *>(&Ts[r][j]);
+            *reinterpret_cast<float4 *>(sm.u2.t + tc::sw128_off(r, j, 64)) = ld4(&Ts[r][j]);
         }
         // ---- 7. beta V^T into TMEM (thread = value row lr, tokens 32 hf ..)
         ok = __syncthreads_and(tid == 0 ? mbar_wait(&sm.bar_v, 0) : true) != 0;
@@ -1361,7 +1362,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const PrefillPa
         // the range check of S16, once it has been handed over
         auto track_s16 = [&](const uint32_t (&w)[16]) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) s16max = __hmax2_nan(s16max, __habs2(*reinterpret_cast<const __half2 *>(&w[e])));
+            for (int e = 0; e < 16; ++e)
+                s16max = __hmax2_nan(s16max, __habs2(*reinterpret_cast<const __half2 *>(&w[e])));
         };
         // outputs of chunk cj (tokens cq * 16 .. + 15 of value row lr), read
         // from its accumulator (complete: acc_done was observed): a full
@@ -1648,19 +1650,19 @@ static cudaError_t launch_tc(const PrefillParams &p, cudaStream_t st) {
         if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
     // Pipelining: when few (sequence, head) chains would walk many chunks
-    // each, the chunks are cut into segments (plan_segments).  Segment k's prep runs beside segment k - 1's chain (programmatic
-    // dependent launch: the chain lets it start at once; one of its CTAs
-    // waits for that chain before the grid ends), and segment k's chain, an
-    // ordinary launch, follows its prep and so the previous chain.  The last
-    // segment takes every remaining chunk.  Only the last chain is exposed.
+    // each, the chunks are cut into segments (plan_segments).  Segment k's
+    // prep runs beside segment k - 1's chain (programmatic dependent launch:
+    // the chain lets it start at once; one of its CTAs waits for that chain
+    // before the grid ends), and segment k's chain, an ordinary launch,
+    // follows its prep and so the previous chain.  The last segment takes
+    // every remaining chunk.  Only the last chain is exposed.
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                   cudaSuccess)
         sms = 1;
     int lo_k[kMaxSegments + 1];
-    const int nseg = any && p.num_seqs > 0
-                         ? plan_segments((int64_t)p.num_seqs * p.H, sms, (p.total_tokens + C - 1) / C / p.num_seqs, lo_k)
-                         : 1;
+    const int64_t per_seq = p.num_seqs > 0 ? (p.total_tokens + C - 1) / C / p.num_seqs : 0;
+    const int nseg = any && p.num_seqs > 0 ? plan_segments((int64_t)p.num_seqs * p.H, sms, per_seq, lo_k) : 1;
     lo_k[0] = 0;
     const dim3 cgrid((unsigned)p.num_seqs, (unsigned)p.H);
     for (int k = 0; k < nseg; ++k) {
