@@ -33,9 +33,9 @@ constexpr int kFusedWarps = 4;
 constexpr int kFusedThreads = kFusedWarps * 32;
 constexpr int kFusedGroups = kFusedWarps * kGroupsPerWarp;  // 16 row groups per CTA
 
-__device__ __forceinline__ float silu_f(float x) {
-    return __fdiv_rn(x, __fadd_rn(1.0f, expf(-x)));
-}
+// SiLU with the fast exponential and division (a few ulp; the prefill's
+// conv uses the same)
+__device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
