@@ -33,8 +33,7 @@ constexpr int kFusedWarps = 4;
 constexpr int kFusedThreads = kFusedWarps * 32;
 constexpr int kFusedGroups = kFusedWarps * kGroupsPerWarp;  // 16 row groups per CTA
 
-// SiLU with the fast exponential and division (a few ulp; the prefill's
-// conv uses the same)
+// SiLU with the fast exponential and division (a few ulp)
 __device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 __device__ __forceinline__ uint32_t cluster_rank() {

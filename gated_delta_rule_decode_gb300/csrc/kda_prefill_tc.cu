@@ -257,11 +257,8 @@ __device__ __forceinline__ float &st_f32(unsigned char *tile, int r, int c) {
 
 constexpr int kConvChannels = 3 * D;  // q | k | v channels of a head
 
-// SiLU and the sigmoid gate with the fast exponential and reciprocal (a few
-// ulp; the prefill's operands are rounded to fp16 right after)
-__device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
-
-// sigmoid(z), the output gate
+// sigmoid(z), the output gate, with the fast exponential and division (a
+// few ulp)
 __device__ __forceinline__ float sigmoid_gate(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 // The three raw inputs before token t0 of conv channel ch (q | k | v order)
@@ -285,13 +282,30 @@ __device__ __forceinline__ void conv_history(const PrefillParams &p, bool first,
     }
 }
 
-// silu(w . (x_{t-3}, x_{t-2}, x_{t-1}, x_t)) in the fused decode's order
-__device__ __forceinline__ float conv_tap(float4 w, float x0, float x1, float x2, float x3) {
-    float acc = __fmul_rn(w.x, x0);
-    acc = __fmaf_rn(w.y, x1, acc);
-    acc = __fmaf_rn(w.z, x2, acc);
-    acc = __fmaf_rn(w.w, x3, acc);
-    return silu_f(acc);
+// 1/x with the special function unit's approximate reciprocal
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// silu of two values: a / (1 + e^{-a}), e^{-a} = 2^{-a log2(e)}, on the
+// approximate exponential and reciprocal (a few ulp; the convolved k and q
+// are rounded to fp16 right after, v enters beta V^T in fp32)
+__device__ __forceinline__ float2 silu2(float2 a) {
+    const float2 t = __fmul2_rn(a, make_float2(-kLog2e, -kLog2e));
+    const float2 d = __fadd2_rn(make_float2(ex2_approx(t.x), ex2_approx(t.y)), make_float2(1.f, 1.f));
+    return __fmul2_rn(a, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+}
+
+// silu(w . (x_{t-3}, x_{t-2}, x_{t-1}, x_t)) at two consecutive tokens t
+// (inputs x0..x3) and t + 1 (x1..x4), in the fused decode's order of taps
+__device__ __forceinline__ float2 conv_tap2(float4 w, float x0, float x1, float x2, float x3, float x4) {
+    float2 acc = __fmul2_rn(make_float2(w.x, w.x), make_float2(x0, x1));
+    acc = __ffma2_rn(make_float2(w.y, w.y), make_float2(x1, x2), acc);
+    acc = __ffma2_rn(make_float2(w.z, w.z), make_float2(x2, x3), acc);
+    acc = __ffma2_rn(make_float2(w.w, w.w), make_float2(x3, x4), acc);
+    return silu2(acc);
 }
 
 template <typename T, bool FUSED>
@@ -433,7 +447,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         // blocks of 16 rows from the top: the block's 16 inputs and the three
         // below it are loaded first (those rows are still raw: only rows
         // above have been overwritten), then its 16 outputs are stored
-        float ymax = 0.f;
 #pragma unroll 1
         for (int blk = (L - 1) >> 4; blk >= 0; --blk) {
             float x[19];  // x[i] = input of row 16 blk - 3 + i
@@ -442,19 +455,20 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                 const int r = 16 * blk - 3 + i;
                 x[i] = r < L ? x_at(r) : 0.f;
             }
+            // rows r and r + 1 at once; a row past the chunk is neither
+            // stored nor range-checked (an overflow shows as infinity in hmax)
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < 16; j += 2) {
                 const int r = 16 * blk + j;
                 if (r < L) {
-                    const float y = conv_tap(w, x[j], x[j + 1], x[j + 2], x[j + 3]);
-                    ymax = fmaxf(ymax, fabsf(y));
-                    *reinterpret_cast<__half *>(at(r)) = __float2half_rn(y);
+                    const float2 y = conv_tap2(w, x[j], x[j + 1], x[j + 2], x[j + 3], x[j + 4]);
+                    const __half2 h2 = __floats2half2_rn(y.x, r + 1 < L ? y.y : 0.f);
+                    hmax = __hmax2(hmax, __habs2(h2));
+                    *reinterpret_cast<__half *>(at(r)) = __low2half(h2);
+                    if (r + 1 < L) *reinterpret_cast<__half *>(at(r + 1)) = __high2half(h2);
                 }
             }
         }
-        // an overflow of the fp16 values shows as infinity in the running maximum
-        const __half ym = __float2half_rn(ymax);
-        hmax = __hmax2(hmax, __halves2half2(ym, ym));
         __syncthreads();
     }
     if (ok) {
@@ -913,13 +927,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
                 }
                 float x0 = hist[0], x1 = hist[1], x2 = hist[2];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
+                for (int i = 0; i < 32; i += 2) {
                     const int r = 32 * hf + i;
-                    const float x3 = st_bf16(qv, r, lr);
-                    bv[i] = r < L ? sm.beta[r] * conv_tap(w, x0, x1, x2, x3) : 0.f;
-                    x0 = x1;
-                    x1 = x2;
-                    x2 = x3;
+                    const float x3 = st_bf16(qv, r, lr), x4 = st_bf16(qv, r + 1, lr);
+                    const float2 y = __fmul2_rn(*reinterpret_cast<const float2 *>(&sm.beta[r]),
+                                                conv_tap2(w, x0, x1, x2, x3, x4));
+                    bv[i] = r < L ? y.x : 0.f;
+                    bv[i + 1] = r + 1 < L ? y.y : 0.f;
+                    x0 = x2;
+                    x1 = x3;
+                    x2 = x4;
                 }
             }
             tc::st16(tc::lane_addr(tm, warp, PT_BV + 32 * hf), *reinterpret_cast<float(*)[16]>(&bv[0]));
