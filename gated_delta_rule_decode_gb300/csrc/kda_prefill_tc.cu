@@ -793,16 +793,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
         __syncthreads();
         // The block products keep two outputs (level 1) or a 2 x 2 block of
         // outputs (level 2) per thread, so that each operand load serves two
-        // products; the row operands (rows of A or T, 16-byte aligned) are
-        // read four at a time.  The upper triangles of the diagonal blocks
-        // and the upper right blocks hold zeros, so the sums run over whole
-        // blocks.
+        // products, which run as one paired fp32 fused multiply-add; the row
+        // operands (rows of A or T, 16-byte aligned) are read four at a time.
+        // The upper triangles of the diagonal blocks and the upper right
+        // blocks hold zeros, so the sums run over whole blocks.
         {
             // level 1: X1 = A21 T11 per 32-row block ob (rows 2 rp, 2 rp + 1,
             // column j of the 16 x 16 block), then T21 = -T22 X1
             const int ob = tid >> 7, o = 32 * ob, rp = (tid >> 4) & 7, j = tid & 15;
             const int r0 = 2 * rp;
-            float x0 = 0.f, x1 = 0.f;
+            float2 x01 = make_float2(0.f, 0.f);  // rows r0, r0 + 1
 #pragma unroll
             for (int k4 = 0; k4 < 16; k4 += 4) {
                 const float4 a0 = ld4(&As[o + 16 + r0][o + k4]), a1 = ld4(&As[o + 17 + r0][o + k4]);
@@ -810,14 +810,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float t = Ts[o + k4 + e][o + j];
-                    x0 = fmaf(av0[e], t, x0);
-                    x1 = fmaf(av1[e], t, x1);
+                    x01 = __ffma2_rn(make_float2(av0[e], av1[e]), make_float2(t, t), x01);
                 }
             }
-            sm.u3.xs[16 * ob + r0][j] = x0;
-            sm.u3.xs[16 * ob + r0 + 1][j] = x1;
+            sm.u3.xs[16 * ob + r0][j] = x01.x;
+            sm.u3.xs[16 * ob + r0 + 1][j] = x01.y;
             __syncthreads();
-            float y0 = 0.f, y1 = 0.f;
+            float2 y01 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int m4 = 0; m4 < 16; m4 += 4) {
                 const float4 a0 = ld4(&Ts[o + 16 + r0][o + 16 + m4]), a1 = ld4(&Ts[o + 17 + r0][o + 16 + m4]);
@@ -825,12 +824,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float x = sm.u3.xs[16 * ob + m4 + e][j];
-                    y0 = fmaf(av0[e], x, y0);
-                    y1 = fmaf(av1[e], x, y1);
+                    y01 = __ffma2_rn(make_float2(av0[e], av1[e]), make_float2(x, x), y01);
                 }
             }
-            Ts[o + 16 + r0][o + j] = -y0;
-            Ts[o + 17 + r0][o + j] = -y1;
+            Ts[o + 16 + r0][o + j] = -y01.x;
+            Ts[o + 17 + r0][o + j] = -y01.y;
         }
         __syncthreads();
         {
@@ -838,43 +836,40 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_tc_kernel(const PrefillP
             // 2 rp + 1; columns cp, cp + 16), then T21 = -T22 X2
             const int rp = tid >> 4, cp = tid & 15;
             const int r0 = 2 * rp;
-            float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
+            // row r0 (x0) and r0 + 1 (x1), columns (cp, cp + 16) as pairs
+            float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int k4 = 0; k4 < 32; k4 += 4) {
                 const float4 a0 = ld4(&As[32 + r0][k4]), a1 = ld4(&As[33 + r0][k4]);
                 const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float t0 = Ts[k4 + e][cp], t1 = Ts[k4 + e][cp + 16];
-                    x00 = fmaf(av0[e], t0, x00);
-                    x01 = fmaf(av0[e], t1, x01);
-                    x10 = fmaf(av1[e], t0, x10);
-                    x11 = fmaf(av1[e], t1, x11);
+                    const float2 t = make_float2(Ts[k4 + e][cp], Ts[k4 + e][cp + 16]);
+                    x0 = __ffma2_rn(make_float2(av0[e], av0[e]), t, x0);
+                    x1 = __ffma2_rn(make_float2(av1[e], av1[e]), t, x1);
                 }
             }
-            sm.u3.xs[r0][cp] = x00;
-            sm.u3.xs[r0][cp + 16] = x01;
-            sm.u3.xs[r0 + 1][cp] = x10;
-            sm.u3.xs[r0 + 1][cp + 16] = x11;
+            sm.u3.xs[r0][cp] = x0.x;
+            sm.u3.xs[r0][cp + 16] = x0.y;
+            sm.u3.xs[r0 + 1][cp] = x1.x;
+            sm.u3.xs[r0 + 1][cp + 16] = x1.y;
             __syncthreads();
-            float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
+            float2 y0 = make_float2(0.f, 0.f), y1 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int m4 = 0; m4 < 32; m4 += 4) {
                 const float4 a0 = ld4(&Ts[32 + r0][32 + m4]), a1 = ld4(&Ts[33 + r0][32 + m4]);
                 const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float x0 = sm.u3.xs[m4 + e][cp], x1 = sm.u3.xs[m4 + e][cp + 16];
-                    y00 = fmaf(av0[e], x0, y00);
-                    y01 = fmaf(av0[e], x1, y01);
-                    y10 = fmaf(av1[e], x0, y10);
-                    y11 = fmaf(av1[e], x1, y11);
+                    const float2 x = make_float2(sm.u3.xs[m4 + e][cp], sm.u3.xs[m4 + e][cp + 16]);
+                    y0 = __ffma2_rn(make_float2(av0[e], av0[e]), x, y0);
+                    y1 = __ffma2_rn(make_float2(av1[e], av1[e]), x, y1);
                 }
             }
-            Ts[32 + r0][cp] = -y00;
-            Ts[32 + r0][cp + 16] = -y01;
-            Ts[33 + r0][cp] = -y10;
-            Ts[33 + r0][cp + 16] = -y11;
+            Ts[32 + r0][cp] = -y0.x;
+            Ts[32 + r0][cp + 16] = -y0.y;
+            Ts[33 + r0][cp] = -y1.x;
+            Ts[33 + r0][cp + 16] = -y1.y;
         }
         __syncthreads();
         // T into its swizzled tile (over gamma, which nothing reads any more)
