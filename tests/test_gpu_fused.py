@@ -160,3 +160,43 @@ def test_fused_decode_full_size_sampled():
     touched[x.slot_ids.long()] = True
     assert torch.equal(x.pool[~touched], pool0[~touched])
     assert torch.equal(ex.conv_state[~touched], c0[~touched])
+
+
+def _preactivations(x, ex, dk):
+    """The conv pre-activations w . (x_{t-3}, x_{t-2}, x_{t-1}, x_t) of every
+    (sequence, head, channel) of the step, from the slots' conv states."""
+    slots = x.slot_ids.long()
+    hist = to_np64(ex.conv_state[slots])                          # [B, H, 3, nc]
+    cur = np.concatenate([to_np64(x.q), to_np64(x.k), to_np64(x.v)], axis=-1)  # [B, H, nc]
+    w = to_np64(ex.conv_w)                                        # [H, nc, 4]
+    return (w[None, :, :, 0] * hist[:, :, 0] + w[None, :, :, 1] * hist[:, :, 1] +
+            w[None, :, :, 2] * hist[:, :, 2] + w[None, :, :, 3] * cur)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_fused_decode_saturated_conv(dtype):
+    """Conv taps 40 times the usual ones: a few percent of the SiLU arguments
+    lie beyond +-88, where e^{-x} leaves the fp32 range, so the fast
+    exponential and division must give silu(x) = -0 for x << 0 and x for
+    x >> 0 (no NaN), and the step still matches the oracle."""
+    kda = _kda()
+    B, H, NS, d = 7, 3, 9, 128
+    x = inputs.decode_inputs(B, H, d, d, dtype=dtype, num_slots=NS, seed=77)
+    ex = inputs.fused_extras(B, H, d, d, dtype=dtype, num_slots=NS, seed=77)
+    ex.conv_w = ex.conv_w * 40.0
+    pre = _preactivations(x, ex, d)
+    assert (pre < -88).sum() > 20 and (pre > 88).sum() > 20
+    pool, cst = x.pool.cuda(), ex.conv_state.cuda()
+    flag = err_flag()
+    out = kda.decode_fused(x.q.cuda(), x.k.cuda(), x.v.cuda(), x.g.cuda(), x.b.cuda(), ex.z.cuda(),
+                           x.slot_ids.cuda(), pool, cst, ex.conv_w.cuda(), ex.norm_w.cuda(),
+                           eps_o=1e-5, err_flag=flag)
+    o_ref, p_ref, c_ref, e = _oracle_step(x, ex, x.slot_ids, x.pool, ex.conv_state, d, 1e-5)
+    torch.cuda.synchronize()
+    assert e == 0 and flag.item() == 0
+    assert torch.isfinite(out).all() and torch.isfinite(pool).all()
+    dt = inputs.torch_dtype(dtype)
+    atol, rtol = tol_for(dt)
+    assert_close(to_np64(out), round_to(o_ref, dt), atol, rtol, "outputs")
+    assert_close(to_np64(pool), p_ref, atol, rtol, "pool")
+    assert np.array_equal(to_np64(cst), c_ref)
