@@ -16,6 +16,17 @@ def test_silu_closed_forms():
     assert abs(megakda.silu(-math.log(3.0)) + 0.25 * math.log(3.0)) < 1e-15
 
 
+def test_silu_odd_part_and_far_arguments():
+    # sigmoid(x) + sigmoid(-x) = 1, so silu(x) - silu(-x) = x at any scale,
+    # including the saturated arguments the fused kernels' tests reach
+    x = np.array([0.5, 3.0, 40.0, 88.5, 300.0])
+    np.testing.assert_allclose(megakda.silu(x) - megakda.silu(-x), x, rtol=1e-15)
+    # far arguments: silu(x) = x for x >> 0 and -|x| e^{-|x|} for x << 0, to
+    # fp64 precision (the corrections are of order e^{-|x|})
+    assert megakda.silu(300.0) == 300.0
+    np.testing.assert_allclose(megakda.silu(-300.0), -300.0 * math.exp(-300.0), rtol=1e-14)
+
+
 def test_short_conv_taps_pick_the_right_inputs():
     rng = np.random.default_rng(0)
     d = 5
